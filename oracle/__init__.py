@@ -1,0 +1,37 @@
+"""CPU oracle for the NVFP4 block-scaled batched GEMV.
+
+THIS PACKAGE IS TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference arm of ``bench.py`` may import it.  The product (``decode_nvfp4_gemv_gb300``:
+the CUDA kernels, the C ABI and its Python binding) never imports, links or calls anything here,
+and this package shares no code, table or helper with it.  The only module both sides use is the
+seeded input generator ``workloads``, which holds none of the GEMV's arithmetic.
+
+Contents, each written from the pages' definitions (citations in each module):
+
+* ``codecs``   E2M1 / E4M3FN decoders from their bit layouts, nibble unpacking, fp16 rounding.
+* ``nvfp4_gemv`` the GEMV definition in fp64 (``gemv``, ``gemv_rows``) and an independent exact
+               integer formulation (``gemv_exact_units``).
+
+Pins (tests that tie the oracle to something other than itself):
+
+* E2M1 table == the magnitude list printed in bridge.py "Constants", plus sign symmetry;
+* E4M3FN: all 256 bytes == torch's float8_e4m3fn -> float32 cast, plus hand anchors;
+* all 16 x 16 code products == exact integer quarter-units (brute force);
+* fp16 rounding: every binary16 value round-trips, every midpoint ties to even, checked against
+  exact rational arithmetic;
+* hand-worked examples under ``tests/golden/`` (values derived from the pages' table and formula);
+* algebraic invariants (zero scale, doubled scale, nibble swap, negation, block permutation,
+  batch independence);
+* ``gemv`` == ``gemv_exact_units`` bit for bit on all five workloads (sampled rows at full size);
+* planted mistakes (swapped nibbles, dropped scale, off-by-one block index, ...) each fail a pin.
+
+No function in this package is "parity unpinned".
+"""
+from .codecs import (E2M1_TABLE, E4M3FN_TABLE, e2m1_value, e4m3fn_value, fp16_round,
+                     unpack_e2m1_codes)
+from .nvfp4_gemv import BLOCK, TERM_UNIT_EXP, gemv, gemv_exact_units, gemv_fp16, gemv_rows
+
+__all__ = [
+    "E2M1_TABLE", "E4M3FN_TABLE", "e2m1_value", "e4m3fn_value", "fp16_round", "unpack_e2m1_codes",
+    "BLOCK", "TERM_UNIT_EXP", "gemv", "gemv_exact_units", "gemv_fp16", "gemv_rows",
+]
