@@ -1,0 +1,494 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 block-scaled batched GEMV on GB300.
+
+One step is one GEMV call (the whole path: stream A and its block scales, stage the vector,
+decode, scale, reduce, fp16 store) over one batch of seeded synthetic input.  The default workload
+is the decode GEMV M=7168, K=16384, L=1 (66.1 MB per call).  Prints ONE JSON line:
+
+  metric / value / unit   achieved HBM GB/s of algorithmic bytes (M*K*L/2 + M*K*L/16 + K*L/2 +
+                          K*L/16 + 2*M*L per call), whole job over all ranks, inputs resident in HBM
+  us_per_call, pct_of_peak
+  e2e                     the same metric through the public call with host buffers: every step
+                          copies its inputs from pinned host memory and reads back c
+  roofline                dominant kernel vs the measured HBM copy bandwidth
+  cpu_baseline            the CPU oracle on a bounded sample of the same workload
+  clocks                  nvidia-smi samples taken during the timed region
+
+Timing: W warm-up steps, then exactly K steps timed with CUDA events on the launching stream,
+barrier + synchronize on both sides, max over ranks.  L2 residency is defeated by rotating over
+copies of the inputs totalling more than 3x the L2 size (each step reads a different copy).  The
+launches are captured in CUDA graphs (1000 calls per graph) so the host launch rate cannot limit
+the measurement.
+
+Multi-GPU (torchrun): the GEMV needs no exchange between GPUs, so each rank runs an independent
+replica on its own GPU (weak scaling) and rank 0 reports the sum of bytes over the max time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "NVFP4 batched GEMV achieved HBM GB/s (% of GB300 peak) and us/call per MxKxL"
+GRAPH_CHUNK = 1000
+DEFAULT_PEAK_GBS = 6800.0   # only if MEASURED_PEAKS.json is absent
+
+
+# ---------------------------------------------------------------------------- distributed helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def reduce_scalar(dist, x: float, op: str) -> float:
+    """max / sum of a host scalar over ranks (gloo; no data-path collective)."""
+    if dist is None:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate(dist, bytes_per_rank: float, seconds: float):
+    """Whole-job throughput: bytes summed over ranks / slowest rank's time."""
+    total = reduce_scalar(dist, bytes_per_rank, "sum")
+    slowest = reduce_scalar(dist, seconds, "max")
+    return total, slowest
+
+
+# ---------------------------------------------------------------------------- peaks, clocks
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return DEFAULT_PEAK_GBS, "fallback"
+
+
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of one GPU while the timed region runs."""
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def query_once(self):
+        try:
+            out = subprocess.run(["nvidia-smi", "-i", self.gpu_id, "--format=csv,noheader,nounits",
+                                  "--query-gpu=" + ",".join(CLOCK_FIELDS)],
+                                 capture_output=True, text=True, timeout=20)
+            return [ln for ln in out.stdout.splitlines() if ln.strip()]
+        except (OSError, subprocess.SubprocessError):
+            return []
+
+    def __enter__(self):
+        self.before = self.query_once()
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--format=csv,noheader,nounits", "-lms", "200",
+                 "--query-gpu=" + ",".join(CLOCK_FIELDS)], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=10)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+        self.after = self.query_once()
+        return False
+
+    def summary(self):
+        lines = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                lines = [ln for ln in f.read().splitlines() if ln.strip()]
+            os.unlink(self.path)
+        rows = [r.split(", ") for r in (lines or (self.before + self.after))]
+        rows = [r for r in rows if len(r) == len(CLOCK_FIELDS)]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+# ---------------------------------------------------------------------------- traffic record
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "decode_nvfp4_gemv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on these sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{workload_name}.txt")
+    try:
+        kv = {}
+        with open(path) as f:
+            for ln in f:
+                if "=" in ln and not ln.lstrip().startswith("#"):
+                    k, v = ln.split("=", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_sources_sha256_16") != kernel_source_digest():
+            return None
+        return float(kv["dram_bytes_read_per_launch"]) + float(kv["dram_bytes_write_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------- our arm
+
+def _device_inputs(w, n_copies, device):
+    import torch
+
+    base = {k: torch.from_numpy(np.ascontiguousarray(getattr(w, k))).to(device)
+            for k in ("A", "sfa", "b", "sfb")}
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_copies - 1)]
+    return sets
+
+
+def time_device(pkg, w, sets, outs, plan, steps, warmup, stream):
+    """Returns (seconds for exactly `steps` calls, launches)."""
+    import torch
+
+    n = len(sets)
+
+    def call(i):
+        s = sets[i % n]
+        pkg.nvfp4_gemv_batched_ex(s["A"], s["sfa"], w.g_a, s["b"], s["sfb"], w.g_b, outs[i % n],
+                                  w.M, w.K, w.L, stream=stream, plan=plan)
+
+    def make_graph(count, offset):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(count):
+                call(offset + i)
+        return g
+
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 1)):            # uncaptured warm-up (also caches device info)
+            call(i)
+    stream.synchronize()
+    chunk = min(GRAPH_CHUNK, steps)
+    g_full = make_graph(chunk, 0) if chunk else None
+    rem = steps % chunk if chunk else 0
+    g_rem = make_graph(rem, 0) if rem else None
+    for _ in range(2):                             # graph warm-up
+        g_full.replay()
+    stream.synchronize()
+    return g_full, g_rem, chunk, rem
+
+
+def run_ours(args):
+    import torch
+
+    import decode_nvfp4_gemv_gb300 as pkg
+
+    world, rank, local = dist_env()
+    dist = dist_init(world)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pkg.load_library()
+    w = workloads.make(args.config)
+    bytes_call = w.algorithmic_bytes
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    n_copies = max(2, -(-3 * l2 // bytes_call) + 1)
+    sets = _device_inputs(w, n_copies, device)
+    outs = [torch.empty((w.L, w.M), dtype=torch.float16, device=device) for _ in range(n_copies)]
+    plan = json.loads(args.plan) if args.plan else None
+    stream = torch.cuda.Stream(device)
+    g_full, g_rem, chunk, rem = time_device(pkg, w, sets, outs, plan, args.steps, args.warmup,
+                                            stream)
+    used_plan = pkg.nvfp4_gemv_plan(w.M, w.K, w.L).as_dict() if plan is None else plan
+    uuid = str(torch.cuda.get_device_properties(device).uuid)
+    gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_id)
+    with sampler:
+        barrier(dist)
+        torch.cuda.synchronize(device)
+        ev0.record(stream)
+        for _ in range(args.steps // chunk):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(dist)
+    seconds = ev0.elapsed_time(ev1) / 1e3
+    clocks = sampler.summary()
+
+    total_bytes, slowest = aggregate(dist, bytes_call * args.steps, seconds)
+    value = total_bytes / slowest / 1e9
+    per_call_s = seconds / args.steps
+    achieved = bytes_call / per_call_s / 1e9
+    peak, peak_kind = measured_peak_gbs()
+    traffic = recorded_traffic(args.config)
+
+    # correctness spot check of the timed launches' last output (NaN would mean an unwritten c)
+    assert not torch.isnan(outs[(args.steps - 1) % n_copies]).any().item()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = time_e2e(pkg, w, plan, device, stream, min(args.steps, args.e2e_steps), dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(slowest / args.steps * 1e3, 6),
+            "us_per_call": round(per_call_s * 1e6, 3),
+            "pct_of_peak": round(100.0 * achieved / peak, 2),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "e2m1/e4m3 in, f16x2 block sums, f32 accumulate, f16 out",
+            "data": "synthetic (seeded splitmix64; " + w.recipe + ")",
+            "config": {
+                "workload": f"NVFP4 decode GEMV M={w.M} K={w.K} L={w.L} ({args.config})",
+                "M": w.M, "K": w.K, "L": w.L,
+                "bytes_per_call": bytes_call,
+                "l2": f"inputs rotated over {n_copies} copies "
+                      f"({n_copies * bytes_call / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
+                "plan": used_plan,
+                "launch": f"CUDA graphs of {chunk} calls",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            },
+            "roofline": {
+                "bound": "hbm",
+                "kernel": "gemv_stream_kernel" if used_plan.get("kernel", 2) == 2 else
+                          "gemv_simple_kernel",
+                "achieved": round(achieved, 2),
+                "peak": peak,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
+                "traffic": traffic,
+            },
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+        if e2e is not None:
+            line["e2e"] = e2e
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    barrier(dist)
+
+
+def time_e2e(pkg, w, plan, device, stream, steps, dist):
+    """GB/s of algorithmic bytes when every step copies its inputs from pinned host memory, runs
+    the GEMV through the public call and reads c back to pinned host memory."""
+    import torch
+
+    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(w, k))).pin_memory()
+            for k in ("A", "sfa", "b", "sfb")}
+    devb = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    c_dev = torch.empty((w.L, w.M), dtype=torch.float16, device=device)
+    c_host = torch.empty((w.L, w.M), dtype=torch.float16).pin_memory()
+    h2d = sum(v.numel() for v in host.values())
+    d2h = c_host.numel() * 2
+
+    def step():
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        pkg.nvfp4_gemv_batched_ex(devb["A"], devb["sfa"], w.g_a, devb["b"], devb["sfb"], w.g_b,
+                                  c_dev, w.M, w.K, w.L, stream=stream, plan=plan)
+        c_host.copy_(c_dev, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        barrier(dist)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        stream.synchronize()
+        barrier(dist)
+    seconds = ev0.elapsed_time(ev1) / 1e3
+    total, slowest = aggregate(dist, w.algorithmic_bytes * steps, seconds)
+    return {"value": round(total / slowest / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
+            "us_per_step": round(seconds / steps * 1e6, 2)}
+
+
+# ---------------------------------------------------------------------------- the oracle on the CPU
+
+def _oracle_rows(w, rows):
+    import oracle
+
+    ls, ms = np.divmod(np.asarray(rows, dtype=np.int64), w.M)
+    oracle.gemv_rows(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, w.M, w.K, w.L, ls, ms)
+
+
+def _row_bytes(w, n_rows):
+    """Algorithmic bytes of n_rows outputs (their share of the vector bytes included)."""
+    return w.algorithmic_bytes * n_rows / (w.M * w.L)
+
+
+def cpu_baseline(w, seconds: float):
+    """The oracle as it stands (numpy, fp64) timed on this host on consecutive output rows until
+    about `seconds` have passed (or the workload is done)."""
+    total = w.M * w.L
+    chunk = max(1, (1 << 22) // w.K)
+    done = 0
+    t0 = time.perf_counter()
+    while done < total and time.perf_counter() - t0 < seconds:
+        n = min(chunk, total - done)
+        _oracle_rows(w, range(done, done + n))
+        done += n
+    elapsed = time.perf_counter() - t0
+    return {"value": round(_row_bytes(w, done) / elapsed / 1e9, 4), "unit": "GB/s",
+            "cores": 1, "kind": "oracle",
+            "sample": f"{done} of {total} output rows ({100.0 * done / total:.1f}% of the "
+                      f"workload), {elapsed:.1f} s, numpy fp64, single thread"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.make(args.config)
+    per_step_budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    t0 = time.perf_counter()
+    _oracle_rows(w, range(0, 1))
+    t_row = max(time.perf_counter() - t0, 1e-4)
+    rows = int(max(1, min(w.M * w.L, per_step_budget / t_row)))
+    for i in range(args.warmup):
+        _oracle_rows(w, range((i * rows) % (w.M * w.L - rows + 1), (i * rows) % (w.M * w.L - rows + 1) + rows))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        s = (i * rows) % (w.M * w.L - rows + 1)
+        _oracle_rows(w, range(s, s + rows))
+    elapsed = time.perf_counter() - t0
+    value = _row_bytes(w, rows) * args.steps / elapsed / 1e9
+    sample = (f"{rows} consecutive output rows per step of the M={w.M} K={w.K} L={w.L} workload, "
+              f"numpy fp64 oracle, single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"NVFP4 decode GEMV M={w.M} K={w.K} L={w.L} ({args.config})",
+                       "M": w.M, "K": w.K, "L": w.L},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50000)
+    ap.add_argument("--warmup", type=int, default=1000)
+    ap.add_argument("--config", default="c2", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--plan", default="", help="JSON plan fields forced on every call")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-seconds", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

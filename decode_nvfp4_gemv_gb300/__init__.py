@@ -1,0 +1,231 @@
+"""GB300-native NVFP4 block-scaled batched GEMV.
+
+Python binding of ``libnvfp4_gemv.so`` (C ABI in ``include/nvfp4_gemv.h``).  It only marshals
+arguments: every step of the GEMV runs in the library's CUDA kernels.  PyTorch provides device
+memory and streams.  The entry points have the C names:
+
+    nvfp4_gemv_batched(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream=None)
+    nvfp4_gemv_batched_ex(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream=None, plan=None)
+    nvfp4_gemv_plan(M, K, L) -> Plan
+    nvfp4_max_stream_k(), nvfp4_status_string(status), nvfp4_last_error(), nvfp4_abi_version()
+
+Tensor arguments are contiguous CUDA tensors (A, sfa, b, sfb: uint8; c: float16, or uint16/int16
+holding fp16 bits) or raw integer device addresses.  The binding checks tensor sizes against
+(M, K, L) before calling, so a shape mistake raises instead of reading out of bounds.  A non-zero
+library status raises ``NVFP4Error``.  If the library is not built, calls raise ``RuntimeError``:
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from .build import LIB_PATH
+
+__all__ = [
+    "NVFP4Error", "Plan", "KERNEL_AUTO", "KERNEL_SIMPLE", "KERNEL_STREAM", "library_path",
+    "load_library", "nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_plan",
+    "nvfp4_max_stream_k", "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version", "gemv",
+]
+
+KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM = 0, 1, 2
+
+OK, ERR_INVALID_VALUE, ERR_MISALIGNED, ERR_UNSUPPORTED_SHAPE, ERR_ARCH, ERR_CUDA = range(6)
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"nvfp4 status {status} ({nvfp4_status_string(status)}): {message}")
+        self.status = status
+        self.message = message
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("rows_per_warp", ctypes.c_int32),
+                ("k_split", ctypes.c_int32), ("ctas_per_batch", ctypes.c_int32),
+                ("warps_per_cta", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+    def __repr__(self):
+        return f"Plan({self.as_dict()})"
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library():
+    """Load libnvfp4_gemv.so once (raises RuntimeError if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m decode_nvfp4_gemv_gb300.build` (or __graft_entry__.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    u8p, u16p, vp = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+    i64, f32 = ctypes.c_int64, ctypes.c_float
+    lib.nvfp4_gemv_batched.argtypes = [u8p, u8p, f32, u8p, u8p, f32, u16p, i64, i64, i64, vp]
+    lib.nvfp4_gemv_batched.restype = ctypes.c_int
+    lib.nvfp4_gemv_batched_ex.argtypes = [u8p, u8p, f32, u8p, u8p, f32, u16p, i64, i64, i64, vp,
+                                          ctypes.POINTER(Plan)]
+    lib.nvfp4_gemv_batched_ex.restype = ctypes.c_int
+    lib.nvfp4_gemv_plan.argtypes = [i64, i64, i64, ctypes.POINTER(Plan)]
+    lib.nvfp4_gemv_plan.restype = ctypes.c_int
+    lib.nvfp4_max_stream_k.argtypes = []
+    lib.nvfp4_max_stream_k.restype = ctypes.c_int64
+    lib.nvfp4_status_string.argtypes = [ctypes.c_int]
+    lib.nvfp4_status_string.restype = ctypes.c_char_p
+    lib.nvfp4_last_error.argtypes = []
+    lib.nvfp4_last_error.restype = ctypes.c_char_p
+    lib.nvfp4_abi_version.argtypes = []
+    lib.nvfp4_abi_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def nvfp4_status_string(status: int) -> str:
+    return load_library().nvfp4_status_string(int(status)).decode()
+
+
+def nvfp4_last_error() -> str:
+    return load_library().nvfp4_last_error().decode()
+
+
+def nvfp4_abi_version() -> int:
+    return load_library().nvfp4_abi_version()
+
+
+def nvfp4_max_stream_k() -> int:
+    return int(load_library().nvfp4_max_stream_k())
+
+
+def _check(status: int):
+    if status != OK:
+        raise NVFP4Error(status, nvfp4_last_error())
+
+
+# ------------------------------------------------------------------ argument marshalling
+
+_ITEM = {"A": 1, "sfa": 1, "b": 1, "sfb": 1, "c": 2}
+
+
+def _ptr(name, x, need_bytes):
+    """Device address of a tensor (checking dtype, contiguity and size) or of a raw integer."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    import torch
+
+    if not isinstance(x, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor or an integer address")
+    if name == "c":
+        if x.dtype not in (torch.float16, torch.uint16, torch.int16):
+            raise TypeError("c must be float16 (or 16-bit integers holding fp16 bits)")
+    elif x.dtype not in (torch.uint8, torch.int8):
+        raise TypeError(f"{name} must be uint8 (packed FP4 / FP8 bytes)")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (use the host path in bench/tests to copy)")
+    have = x.numel() * x.element_size()
+    if have < need_bytes:
+        raise ValueError(f"{name} holds {have} bytes, (M, K, L) needs {need_bytes}")
+    return x.data_ptr()
+
+
+def _stream_handle(stream, tensors):
+    if stream is None:
+        import torch
+
+        dev = next((t.device for t in tensors if hasattr(t, "device")), None)
+        return torch.cuda.current_stream(dev).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _marshal(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream):
+    M, K, L = int(M), int(K), int(L)
+    if M < 0 or K <= 0 or L < 0 or K % 16:
+        # let the library produce the status for invalid shapes (no memory is touched)
+        need = {k: 0 for k in _ITEM}
+    else:
+        need = {"A": M * L * K // 2, "sfa": M * L * K // 16, "b": L * K // 2, "sfb": L * K // 16,
+                "c": 2 * M * L}
+    ptrs = [_ptr(n, x, need[n]) for n, x in (("A", A), ("sfa", sfa), ("b", b), ("sfb", sfb),
+                                                 ("c", c))]
+    h = _stream_handle(stream, [A, sfa, b, sfb, c])
+    return ptrs, ctypes.c_float(g_a), ctypes.c_float(g_b), M, K, L, h
+
+
+class _on_device:
+    """Makes the device of the first tensor argument current for the duration of a call (the
+    library works on the calling thread's current device)."""
+
+    def __init__(self, tensors):
+        self.dev = next((t.device for t in tensors if hasattr(t, "device") and t.is_cuda), None)
+        self.prev = None
+
+    def __enter__(self):
+        if self.dev is not None:
+            import torch
+
+            self.prev = torch.cuda.current_device()
+            if self.prev != self.dev.index:
+                torch.cuda.set_device(self.dev)
+            else:
+                self.prev = None
+
+    def __exit__(self, *exc):
+        if self.prev is not None:
+            import torch
+
+            torch.cuda.set_device(self.prev)
+
+
+def nvfp4_gemv_batched(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream=None):
+    """Enqueue c = fp16(g_a g_b A (x) b) per batch on ``stream`` (default: torch's current stream)."""
+    with _on_device([A, sfa, b, sfb, c]):
+        (pA, pSA, pB, pSB, pC), ga, gb, M, K, L, h = _marshal(A, sfa, g_a, b, sfb, g_b, c, M, K,
+                                                              L, stream)
+        _check(load_library().nvfp4_gemv_batched(pA, pSA, ga, pB, pSB, gb, pC, M, K, L, h))
+
+
+def nvfp4_gemv_batched_ex(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream=None, plan=None):
+    """As ``nvfp4_gemv_batched`` with a forced ``Plan`` (or a dict of its fields; None = auto)."""
+    pl = None
+    if plan is not None:
+        pl = Plan(**plan) if isinstance(plan, dict) else plan
+    with _on_device([A, sfa, b, sfb, c]):
+        (pA, pSA, pB, pSB, pC), ga, gb, M, K, L, h = _marshal(A, sfa, g_a, b, sfb, g_b, c, M, K,
+                                                              L, stream)
+        _check(load_library().nvfp4_gemv_batched_ex(pA, pSA, ga, pB, pSB, gb, pC, M, K, L, h,
+                                                    ctypes.byref(pl) if pl is not None else None))
+
+
+def nvfp4_gemv_plan(M, K, L) -> Plan:
+    out = Plan()
+    _check(load_library().nvfp4_gemv_plan(int(M), int(K), int(L), ctypes.byref(out)))
+    return out
+
+
+def gemv(A, sfa, g_a, b, sfb, g_b, out=None, stream=None, plan=None):
+    """Shape-inferring convenience wrapper: A [L][M][K/2], sfa [L][M][K/16], b [L][K/2],
+    sfb [L][K/16] (uint8 CUDA tensors).  Returns c [L][M] float16 (allocated if ``out`` is None)."""
+    import torch
+
+    if A.dim() != 3:
+        raise ValueError("A must be [L][M][K/2]")
+    L, M, K2 = A.shape
+    K = 2 * K2
+    if out is None:
+        out = torch.empty((L, M), dtype=torch.float16, device=A.device)
+    nvfp4_gemv_batched_ex(A, sfa, g_a, b, sfb, g_b, out, M, K, L, stream, plan)
+    return out

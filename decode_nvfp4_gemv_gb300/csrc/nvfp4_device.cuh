@@ -1,0 +1,111 @@
+// Device helpers for the NVFP4 GEMV kernels (sm_103a): format conversions, packed-half math and
+// streaming loads, as inline PTX.
+//
+// Format facts used here (the C header states them with their sources): an E2M1 byte holds the
+// element with even k in its low nibble; an E4M3FN block scale covers 16 consecutive k.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace nvfp4 {
+
+// Four packed E2M1 bytes (8 elements, byte j = elements 2j, 2j+1) -> four f16x2 words; word j
+// holds byte j's two elements in the same nibble -> half order the conversion uses for every
+// operand, so lane-wise products of two such words pair equal k.  Exact: every E2M1 value is an
+// f16 value.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t& h0, uint32_t& h1,
+                                                  uint32_t& h2, uint32_t& h3) {
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "mov.b32 {q0, q1, q2, q3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, q1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, q2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, q3;\n\t}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w));
+}
+
+// One packed E2M1 byte (low 8 bits of v) -> f16x2.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t v) {
+  uint32_t h;
+  asm("{\n\t.reg .b8 q0, q1, q2, q3;\n\t"
+      "mov.b32 {q0, q1, q2, q3}, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, q0;\n\t}"
+      : "=r"(h)
+      : "r"(v));
+  return h;
+}
+
+// Two E4M3FN bytes (low byte = first scale) -> f16x2 (low half = first scale).  Exact: every
+// E4M3FN value, subnormals and NaN included, is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+  return h;
+}
+
+// acc += a * b on both halves (f16x2, round-to-nearest).
+__device__ __forceinline__ void hfma2(uint32_t& acc, uint32_t a, uint32_t b) {
+  asm("fma.rn.f16x2 %0, %1, %2, %0;" : "+r"(acc) : "r"(a), "r"(b));
+}
+
+// Both halves of an f16x2 widened to f32 (exact).
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, u;\n\t"
+      "mov.b32 {l, u}, %2;\n\t"
+      "cvt.f32.f16 %0, l;\n\t"
+      "cvt.f32.f16 %1, u;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h));
+  return make_float2(lo, hi);
+}
+
+// low half + high half, in f32 (one widening and one mixed-precision add).
+__device__ __forceinline__ float f16x2_hsum_f32(uint32_t h) {
+  float r;
+  asm("{\n\t.reg .b16 l, u;\n\t.reg .f32 t;\n\t"
+      "mov.b32 {l, u}, %1;\n\t"
+      "cvt.f32.f16 t, l;\n\t"
+      "add.rn.f32.f16 %0, u, t;\n\t}"
+      : "=f"(r)
+      : "r"(h));
+  return r;
+}
+
+// 16-byte read-only streaming load: not allocated in L1 (each byte of A is read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ld_ro_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ld_ro_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// fp32 -> IEEE binary16 bits, round-to-nearest-even, overflow to +-inf.
+__device__ __forceinline__ uint16_t f32_to_f16_bits(float x) {
+  return __half_as_ushort(__float2half_rn(x));
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,364 @@
+// C ABI of the NVFP4 batched GEMV (declared in include/nvfp4_gemv.h): argument validation, the
+// launch planner and the launches.  Nothing here allocates, synchronizes or reads device memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/nvfp4_gemv.h"
+#include "gemv_kernels.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(NVFP4_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------- per-device properties (cached)
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  cudaError_t err = cudaSuccess;
+  int major = 0, minor = 0;
+  int sms = 0;
+  int max_smem_optin = 0;   // bytes of shared memory one CTA may opt into
+  int pageable_access = 0;  // the device can read pageable host memory
+};
+
+std::once_flag g_dev_once[kMaxDevices];
+DeviceInfo g_dev[kMaxDevices];
+
+template <int R>
+cudaError_t prepare_stream_kernel(int max_smem) {
+  return cudaFuncSetAttribute(nvfp4::gemv_stream_kernel<R>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+}
+
+void init_device(int dev) {
+  DeviceInfo& d = g_dev[dev];
+  cudaError_t e;
+  if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+      (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+      (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) ||
+      (e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                  dev)) ||
+      (e = cudaDeviceGetAttribute(&d.pageable_access, cudaDevAttrPageableMemoryAccess, dev))) {
+    d.err = e;
+    return;
+  }
+  if (d.major != 10 || d.minor != 3) return;  // no kernels for other architectures
+  if ((e = prepare_stream_kernel<1>(d.max_smem_optin)) ||
+      (e = prepare_stream_kernel<2>(d.max_smem_optin)) ||
+      (e = prepare_stream_kernel<4>(d.max_smem_optin))) {
+    d.err = e;
+    return;
+  }
+}
+
+int current_device(const DeviceInfo** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(NVFP4_ERR_CUDA, "device ordinal %d", dev);
+  std::call_once(g_dev_once[dev], init_device, dev);
+  const DeviceInfo& d = g_dev[dev];
+  if (d.err != cudaSuccess) return cuda_fail(d.err, "device query");
+  if (d.major != 10 || d.minor != 3)
+    return fail(NVFP4_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a only",
+                dev, d.major, d.minor);
+  *out = &d;
+  return NVFP4_OK;
+}
+
+// ---------------------------------------------------------------- argument checks
+bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
+int check_args(const uint8_t* A, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
+               const uint16_t* c, int64_t M, int64_t K, int64_t L, bool* noop) {
+  *noop = false;
+  if (M < 0 || L < 0 || K <= 0)
+    return fail(NVFP4_ERR_INVALID_VALUE, "need M >= 0, L >= 0, K > 0 (M=%lld K=%lld L=%lld)",
+                (long long)M, (long long)K, (long long)L);
+  if (K % 16 != 0)
+    return fail(NVFP4_ERR_INVALID_VALUE, "K=%lld is not a multiple of 16", (long long)K);
+  const int64_t kMax = (int64_t(1) << 31) - 1;
+  if (M > kMax || L > kMax || K / 2 > kMax)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "M, L and K/2 must be below 2^31");
+  if (M == 0 || L == 0) {
+    *noop = true;
+    return NVFP4_OK;
+  }
+  if (!A || !sfa || !b || !sfb || !c) return fail(NVFP4_ERR_INVALID_VALUE, "NULL pointer");
+  if (((uintptr_t)A | (uintptr_t)sfa | (uintptr_t)b | (uintptr_t)sfb) & 15u)
+    return fail(NVFP4_ERR_MISALIGNED, "A, sfa, b and sfb must be 16-byte aligned");
+  if ((uintptr_t)c & 1u) return fail(NVFP4_ERR_MISALIGNED, "c must be 2-byte aligned");
+  // products fit easily: M, L < 2^31 and K/2 < 2^31 would overflow int64 only beyond 2^62
+  const int64_t nA = M * L * (K / 2), nSA = M * L * (K / 16), nB = L * (K / 2),
+                nSB = L * (K / 16), nC = 2 * M * L;
+  if (overlaps(c, nC, A, nA) || overlaps(c, nC, sfa, nSA) || overlaps(c, nC, b, nB) ||
+      overlaps(c, nC, sfb, nSB))
+    return fail(NVFP4_ERR_INVALID_VALUE, "c overlaps an input");
+  return NVFP4_OK;
+}
+
+// Rejects host pointers the device cannot dereference and device pointers of another device.
+int check_access(const DeviceInfo& d, const void* p, const char* name) {
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "cudaPointerGetAttributes");
+  }
+  if (at.type == cudaMemoryTypeUnregistered && !d.pageable_access)
+    return fail(NVFP4_ERR_INVALID_VALUE, "%s is host memory the device cannot access", name);
+  if (at.type == cudaMemoryTypeDevice) {
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (at.device != dev)
+      return fail(NVFP4_ERR_INVALID_VALUE, "%s lives on device %d, current device is %d", name,
+                  at.device, dev);
+  }
+  return NVFP4_OK;
+}
+
+// ---------------------------------------------------------------- planner
+constexpr int64_t kStreamThreads = 256;
+
+int64_t stream_smem_bytes(int64_t K, int64_t S, int64_t rows_cap) {
+  return 2 * K + K / 4 + 4 * S * rows_cap;
+}
+
+int64_t max_stream_k(const DeviceInfo& d) {
+  // vector words + scales for K, plus a small partial array (keep 8 KiB for it)
+  const int64_t budget = d.max_smem_optin - 8192;
+  int64_t k = (budget * 4) / 9;  // 2.25 bytes per element
+  return k - k % 32;
+}
+
+int stream_occupancy(const DeviceInfo& d, int R, int threads, int64_t smem) {
+  int n = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  if (R == 1)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, nvfp4::gemv_stream_kernel<1>, threads,
+                                                      (size_t)smem);
+  else if (R == 2)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, nvfp4::gemv_stream_kernel<2>, threads,
+                                                      (size_t)smem);
+  else
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, nvfp4::gemv_stream_kernel<4>, threads,
+                                                      (size_t)smem);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return std::max(n, 1);
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Fills every field of *pl for (M, K, L); `forced` fields (non-zero) are honoured or rejected.
+int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan* forced,
+              nvfp4_plan* pl) {
+  nvfp4_plan f;
+  memset(&f, 0, sizeof f);
+  if (forced) f = *forced;
+  if (f.reserved[0] || f.reserved[1] || f.reserved[2])
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "plan.reserved must be zero");
+  const bool stream_ok = (K % 32 == 0) && K <= max_stream_k(d);
+  int kernel = f.kernel;
+  if (kernel == NVFP4_KERNEL_AUTO) kernel = stream_ok ? NVFP4_KERNEL_STREAM : NVFP4_KERNEL_SIMPLE;
+  if (kernel != NVFP4_KERNEL_SIMPLE && kernel != NVFP4_KERNEL_STREAM)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown kernel %d", kernel);
+  if (kernel == NVFP4_KERNEL_STREAM && !stream_ok)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                "stream kernel needs K %% 32 == 0 and K <= %lld (K=%lld)",
+                (long long)max_stream_k(d), (long long)K);
+  if (f.warps_per_cta < 0 || f.warps_per_cta > 32 || f.rows_per_warp < 0 || f.k_split < 0 ||
+      f.ctas_per_batch < 0)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "negative or oversized plan field");
+  memset(pl, 0, sizeof *pl);
+  pl->kernel = kernel;
+
+  if (kernel == NVFP4_KERNEL_SIMPLE) {
+    if (f.warps_per_cta > 8)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "simple kernel: at most 8 warps per CTA");
+    const int W = f.warps_per_cta ? f.warps_per_cta : 8;
+    const int64_t rows = M * L;
+    int64_t ctas = f.ctas_per_batch ? (int64_t)f.ctas_per_batch * L
+                                    : std::min<int64_t>(ceil_div(rows, W), (int64_t)d.sms * 8);
+    if (ctas > (int64_t(1) << 31) - 1) ctas = (int64_t(1) << 31) - 1;
+    pl->warps_per_cta = W;
+    pl->ctas_per_batch = (int32_t)std::max<int64_t>(1, ceil_div(ctas, L));
+    pl->rows_per_warp = 1;
+    pl->k_split = 1;
+    return NVFP4_OK;
+  }
+
+  if (f.warps_per_cta > 16)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "stream kernel: at most 16 warps per CTA");
+  const int W = f.warps_per_cta ? f.warps_per_cta : (int)(kStreamThreads / 32);
+  const int64_t steps = ceil_div(K, nvfp4::kStep);
+  // One wave: as many CTAs as fit on the device at once, split evenly over the batches, each
+  // owning a contiguous run of rows.
+  const int occ = stream_occupancy(d, 4, W * 32, stream_smem_bytes(K, 1, 1024));
+  const int64_t slots = (int64_t)d.sms * occ;
+  int64_t P = f.ctas_per_batch ? f.ctas_per_batch : std::max<int64_t>(1, slots / L);
+  P = std::min(P, M);
+  int64_t rows_cap = ceil_div(M, P);
+  while (!f.ctas_per_batch && stream_smem_bytes(K, 1, rows_cap) > d.max_smem_optin && P < M) {
+    P = std::min(M, 2 * P);  // very tall matrices: more, shorter CTAs
+    rows_cap = ceil_div(M, P);
+  }
+  if (P * L > (int64_t(1) << 31) - 1) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
+  const int R = f.rows_per_warp ? f.rows_per_warp : (rows_cap >= 8 ? 4 : rows_cap >= 2 ? 2 : 1);
+  if (R != 1 && R != 2 && R != 4)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "rows_per_warp must be 1, 2 or 4");
+  const int64_t G = ceil_div(rows_cap, R);
+  // K slices: the fewest that minimise the busiest warp's step count, ceil(units / W) * steps per
+  // slice (units = row groups x slices), within the shared-memory budget.
+  int64_t S = f.k_split;
+  if (S == 0) {
+    int64_t best = -1;
+    for (int64_t s = 1; s <= steps; ++s) {
+      const int64_t ss = ceil_div(steps, s), se = ceil_div(steps, ss);
+      if (se != s) continue;
+      if (stream_smem_bytes(K, se, rows_cap) > d.max_smem_optin) break;
+      const int64_t crit = ceil_div(G * se, W) * ss;
+      if (best < 0 || crit < best) {
+        best = crit;
+        S = se;
+      }
+    }
+    if (S == 0) S = 1;
+  }
+  if (S < 1 || S > steps) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "k_split out of range");
+  const int64_t slice_steps = ceil_div(steps, S);
+  S = ceil_div(steps, slice_steps);
+  if (stream_smem_bytes(K, S, rows_cap) > d.max_smem_optin)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "plan needs %lld bytes of shared memory",
+                (long long)stream_smem_bytes(K, S, rows_cap));
+  pl->rows_per_warp = R;
+  pl->k_split = (int32_t)S;
+  pl->ctas_per_batch = (int32_t)P;
+  pl->warps_per_cta = W;
+  return NVFP4_OK;
+}
+
+int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const uint8_t* sfa,
+           float g_a, const uint8_t* b, const uint8_t* sfb, float g_b, uint16_t* c, int64_t M,
+           int64_t K, int64_t L, cudaStream_t stream) {
+  (void)d;
+  const int threads = pl.warps_per_cta * 32;
+  if (pl.kernel == NVFP4_KERNEL_SIMPLE) {
+    const int64_t grid = std::min<int64_t>((int64_t)pl.ctas_per_batch * L, (int64_t(1) << 31) - 1);
+    nvfp4::gemv_simple_kernel<<<(unsigned)grid, threads, 0, stream>>>(A, sfa, b, sfb, g_a, g_b, c,
+                                                                      M, K, L);
+  } else {
+    nvfp4::StreamArgs a;
+    a.A = A; a.sfa = sfa; a.b = b; a.sfb = sfb; a.c = c;
+    a.g_a = g_a; a.g_b = g_b;
+    a.M = M; a.K = K; a.L = L;
+    a.P = pl.ctas_per_batch;
+    const int64_t steps = ceil_div(K, nvfp4::kStep);
+    a.slice_steps = (int32_t)ceil_div(steps, pl.k_split);
+    a.S = (int32_t)ceil_div(steps, a.slice_steps);
+    a.rows_cap = (int32_t)ceil_div(M, pl.ctas_per_batch);
+    const size_t smem = (size_t)stream_smem_bytes(K, a.S, a.rows_cap);
+    const unsigned grid = (unsigned)(pl.ctas_per_batch * L);
+    switch (pl.rows_per_warp) {
+      case 1: nvfp4::gemv_stream_kernel<1><<<grid, threads, smem, stream>>>(a); break;
+      case 2: nvfp4::gemv_stream_kernel<2><<<grid, threads, smem, stream>>>(a); break;
+      default: nvfp4::gemv_stream_kernel<4><<<grid, threads, smem, stream>>>(a); break;
+    }
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return NVFP4_OK;
+}
+
+int gemv_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
+              const uint8_t* sfb, float g_b, uint16_t* c, int64_t M, int64_t K, int64_t L,
+              void* stream, const nvfp4_plan* forced) {
+  g_last_error[0] = '\0';
+  bool noop = false;
+  int st = check_args(A, sfa, b, sfb, c, M, K, L, &noop);
+  if (st != NVFP4_OK || noop) return st;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if ((st = check_access(*d, A, "A")) || (st = check_access(*d, sfa, "sfa")) ||
+      (st = check_access(*d, b, "b")) || (st = check_access(*d, sfb, "sfb")) ||
+      (st = check_access(*d, c, "c")))
+    return st;
+  nvfp4_plan pl;
+  if ((st = make_plan(*d, M, K, L, forced, &pl)) != NVFP4_OK) return st;
+  return launch(*d, pl, A, sfa, g_a, b, sfb, g_b, c, M, K, L, (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int nvfp4_gemv_batched(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
+                       const uint8_t* sfb, float g_b, uint16_t* c, int64_t M, int64_t K, int64_t L,
+                       void* stream) {
+  return gemv_impl(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream, nullptr);
+}
+
+int nvfp4_gemv_batched_ex(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
+                          const uint8_t* sfb, float g_b, uint16_t* c, int64_t M, int64_t K,
+                          int64_t L, void* stream, const nvfp4_plan* plan) {
+  return gemv_impl(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream, plan);
+}
+
+int nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, nvfp4_plan* out) {
+  g_last_error[0] = '\0';
+  if (!out) return fail(NVFP4_ERR_INVALID_VALUE, "out is NULL");
+  if (M <= 0 || L <= 0 || K <= 0 || K % 16)
+    return fail(NVFP4_ERR_INVALID_VALUE, "need M, L > 0 and K a positive multiple of 16");
+  const DeviceInfo* d = nullptr;
+  int st = current_device(&d);
+  if (st != NVFP4_OK) return st;
+  return make_plan(*d, M, K, L, nullptr, out);
+}
+
+int64_t nvfp4_max_stream_k(void) {
+  const DeviceInfo* d = nullptr;
+  if (current_device(&d) != NVFP4_OK) return 0;
+  return max_stream_k(*d);
+}
+
+const char* nvfp4_status_string(int status) {
+  switch (status) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_VALUE: return "invalid value";
+    case NVFP4_ERR_MISALIGNED: return "misaligned pointer";
+    case NVFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape or plan";
+    case NVFP4_ERR_ARCH: return "unsupported device architecture";
+    case NVFP4_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char* nvfp4_last_error(void) { return g_last_error; }
+
+int nvfp4_abi_version(void) { return NVFP4_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,134 @@
+/*
+ * nvfp4_gemv.h -- C ABI of the GB300 (sm_103a) NVFP4 block-scaled batched GEMV library
+ * (libnvfp4_gemv.so).
+ *
+ * The operation ("nvFP4 Batch GEMV算子系列(下)", section "NVFP4 Batched GEMV 概念阐述": blocks of
+ * 16 K-elements share one FP8 scale, a single fp32 global scale per operand multiplies the result,
+ * floor(k/16) is the block id; the page's formula image is lost and this is its written form):
+ *
+ *   c[l][m] = fp16( g_a * g_b * sum_{k<K} e2m1(A[l][m][k]) * e2m1(b[l][k])
+ *                                        * e4m3(sfa[l][m][k/16]) * e4m3(sfb[l][k/16]) )
+ *
+ * for l < L, m < M.  This is the blog's per-batch matrix-vector product (section
+ * "pytorch实现NVFP4 batch gemv": one (m x k) by (k x 1) product per batch l, fp16 out), without its
+ * N = 128 padding of the vector and its 128x4 scale tiles, which served a tensor-core GEMM.
+ *
+ * Element formats:
+ *   e2m1  4-bit float: sign bit 3, exponent bits 2..1 (bias 1), mantissa bit 0; magnitudes
+ *         0, 0.5, 1, 1.5, 2, 3, 4, 6 (cutedsl/bridge.py, "Constants": E2M1_MAGNITUDES).
+ *         Two per byte: element 2j in the low nibble of byte j, element 2j+1 in the high nibble
+ *         (bridge.py, "Quantization": packed = (odd << 4) | even).
+ *   e4m3  float8_e4m3fn block scale (blog, "准备数据"): sign, 4 exponent bits (bias 7), 3 mantissa
+ *         bits; no infinity; 0x7F / 0xFF are NaN and make the outputs that use them NaN.
+ *   c     IEEE binary16 bits; fp32 accumulation, one fp32 multiply by g_a and one by g_b, then
+ *         round-to-nearest-even, overflow to +-inf.
+ *
+ * Layouts (dense, row-major, K contiguous; all sizes in elements unless stated):
+ *   A   uint8 [L][M][K/2]    sfa uint8 [L][M][K/16]
+ *   b   uint8 [L][K/2]       sfb uint8 [L][K/16]
+ *   c   uint16 [L][M]        (fp16 bits; written, never read)
+ *
+ * Memory and ownership: every pointer is memory the device can read (c: write) -- device memory of
+ * the calling thread's current CUDA device, or host memory the device can access.  The caller owns
+ * every buffer; the library keeps no pointer after a call returns and allocates no memory in any
+ * call.  c must not overlap any input.
+ *
+ * Execution: the call validates its arguments on the host, then enqueues its kernel(s) on `stream`
+ * (a cudaStream_t; NULL = the legacy default stream) and returns without synchronizing.  Errors of
+ * the launched kernels surface at the caller's next synchronization.  Calls are deterministic:
+ * the same inputs give the same output bits.  No call synchronizes, allocates or reads device
+ * memory on the host, so calls can be captured in a CUDA graph once the device has been used by
+ * one uncaptured call (which caches its properties).
+ *
+ * Errors (checked in this order, before anything is enqueued; nothing is written on error):
+ *   NVFP4_ERR_INVALID_VALUE   M < 0, L < 0, K <= 0, K % 16 != 0, a NULL pointer when M*L > 0,
+ *                             c overlapping an input, or an inaccessible pointer
+ *   NVFP4_ERR_UNSUPPORTED_SHAPE  M, L or K/2 above 2^31 - 1, or an invalid forced plan
+ *   NVFP4_ERR_MISALIGNED      A, sfa, b or sfb not 16-byte aligned, or c not 2-byte aligned
+ *   NVFP4_ERR_ARCH            the current device is not compute capability 10.3 (GB300)
+ *   NVFP4_ERR_CUDA            a CUDA runtime call or the launch failed (nvfp4_last_error() has
+ *                             the runtime's message)
+ *   M * L == 0 with valid K is a successful no-op.
+ */
+#ifndef NVFP4_GEMV_H_
+#define NVFP4_GEMV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NVFP4_ABI_VERSION 1
+
+typedef enum nvfp4_status {
+  NVFP4_OK = 0,
+  NVFP4_ERR_INVALID_VALUE = 1,
+  NVFP4_ERR_MISALIGNED = 2,
+  NVFP4_ERR_UNSUPPORTED_SHAPE = 3,
+  NVFP4_ERR_ARCH = 4,
+  NVFP4_ERR_CUDA = 5
+} nvfp4_status;
+
+/* Kernel families a plan may force. */
+typedef enum nvfp4_kernel {
+  NVFP4_KERNEL_AUTO = 0,    /* the planner's choice */
+  NVFP4_KERNEL_SIMPLE = 1,  /* one warp per output row, byte loads; any K % 16 == 0 */
+  NVFP4_KERNEL_STREAM = 2   /* 128-bit streaming loads, vector staged in shared memory, intra-CTA
+                               split-K; needs K % 32 == 0 and K <= nvfp4_max_stream_k() */
+} nvfp4_kernel;
+
+/*
+ * Launch plan.  Zero in any field means "planner's choice" for that field.  Used by
+ * nvfp4_gemv_batched_ex to force a decomposition (tests cover every plan on the same inputs; the
+ * output must not depend on it beyond fp32 summation order) and returned by nvfp4_gemv_plan.
+ */
+typedef struct nvfp4_plan {
+  int32_t kernel;          /* nvfp4_kernel */
+  int32_t rows_per_warp;   /* STREAM: rows a warp processes together (1, 2 or 4) */
+  int32_t k_split;         /* STREAM: K slices per row inside a CTA (1 .. ceil(K/1024)) */
+  int32_t ctas_per_batch;  /* STREAM/SIMPLE: CTAs sharing one batch's rows (1 .. M) */
+  int32_t warps_per_cta;   /* SIMPLE: 1 .. 8; STREAM: 1 .. 16 */
+  int32_t reserved[3];     /* must be zero */
+} nvfp4_plan;
+
+/*
+ * c = fp16(g_a * g_b * A (x) b) per batch, as described above.  A, sfa, g_a: the matrix operand and
+ * its block and global scales; b, sfb, g_b: the vector operand and its scales; c: the output;
+ * M, K, L: rows, reduction length, batches; stream: cudaStream_t to enqueue on.
+ * Returns an nvfp4_status.
+ */
+int nvfp4_gemv_batched(const uint8_t* A, const uint8_t* sfa, float g_a,
+                       const uint8_t* b, const uint8_t* sfb, float g_b,
+                       uint16_t* c, int64_t M, int64_t K, int64_t L, void* stream);
+
+/* As nvfp4_gemv_batched, with a plan (NULL = automatic).  Fields of `plan` the planner cannot
+ * honour (e.g. the STREAM kernel when K % 32 != 0) give NVFP4_ERR_UNSUPPORTED_SHAPE. */
+int nvfp4_gemv_batched_ex(const uint8_t* A, const uint8_t* sfa, float g_a,
+                          const uint8_t* b, const uint8_t* sfb, float g_b,
+                          uint16_t* c, int64_t M, int64_t K, int64_t L, void* stream,
+                          const nvfp4_plan* plan);
+
+/* The plan nvfp4_gemv_batched would use for (M, K, L) on the current device, with every field
+ * filled in.  Touches no memory other than *out.  Returns an nvfp4_status. */
+int nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, nvfp4_plan* out);
+
+/* Largest K the STREAM kernel accepts on the current device (its shared-memory bound), or 0 if the
+ * device cannot be queried. */
+int64_t nvfp4_max_stream_k(void);
+
+/* Static English name of a status code ("unknown status" for other values). */
+const char* nvfp4_status_string(int status);
+
+/* Detail text of the last non-OK status returned to the calling thread ("" if none).  The pointer
+ * stays valid until that thread's next call into the library. */
+const char* nvfp4_last_error(void);
+
+/* NVFP4_ABI_VERSION of the built library. */
+int nvfp4_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GEMV_H_ */

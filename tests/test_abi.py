@@ -1,0 +1,98 @@
+"""The C ABI library without a GPU: it builds for sm_103a, loads, exports every function declared in
+include/*.h, and returns the documented statuses for arguments rejected before any device work.
+No call here reaches a kernel launch (every call is rejected on the host first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from decode_nvfp4_gemv_gb300 import build
+
+    build.build()
+    import decode_nvfp4_gemv_gb300 as pkg
+
+    return pkg.load_library()
+
+
+def _declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(nvfp4_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_plan",
+              "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_abi_version_and_status_strings(lib):
+    import decode_nvfp4_gemv_gb300 as pkg
+
+    assert pkg.nvfp4_abi_version() == 1
+    assert pkg.nvfp4_status_string(0) == "ok"
+    assert pkg.nvfp4_status_string(2) == "misaligned pointer"
+    assert pkg.nvfp4_status_string(99) == "unknown status"
+
+
+def _call(lib, A=0x1000, sfa=0x2000, b=0x3000, sfb=0x4000, c=0x5000, M=4, K=256, L=1):
+    vp = ctypes.c_void_p
+    return lib.nvfp4_gemv_batched(vp(A), vp(sfa), ctypes.c_float(1.0), vp(b), vp(sfb),
+                                  ctypes.c_float(1.0), vp(c), M, K, L, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), 1), (dict(L=-2), 1), (dict(K=0), 1), (dict(K=24), 1), (dict(K=-16), 1),
+    (dict(A=0), 1), (dict(sfb=0), 1), (dict(c=0), 1),
+    (dict(A=0x1008), 2), (dict(sfa=0x2001), 2), (dict(b=0x3004), 2), (dict(c=0x5001), 2),
+    (dict(c=0x1000), 1),                        # c overlaps A
+    (dict(M=1 << 31), 3), (dict(K=1 << 33), 3),
+])
+def test_rejected_before_device_work(lib, kw, status):
+    """Every case is rejected by the host-side checks, which run before any CUDA call."""
+    assert _call(lib, **kw) == status
+    import decode_nvfp4_gemv_gb300 as pkg
+
+    assert pkg.nvfp4_last_error() != ""
+
+
+def test_empty_problem_is_a_noop(lib):
+    assert _call(lib, M=0, A=0, sfa=0, b=0, sfb=0, c=0) == 0
+    assert _call(lib, L=0, A=0, sfa=0, b=0, sfb=0, c=0) == 0
+
+
+def test_binding_checks_sizes_before_calling(lib):
+    torch = pytest.importorskip("torch")
+    import decode_nvfp4_gemv_gb300 as pkg
+
+    small = torch.zeros(10, dtype=torch.uint8)
+    with pytest.raises((ValueError, TypeError)):
+        pkg.nvfp4_gemv_batched(small, small, 1.0, small, small, 1.0,
+                               torch.zeros(4, dtype=torch.float16), 4, 256, 1)
+
+
+def test_plan_query_without_gpu(lib):
+    import decode_nvfp4_gemv_gb300 as pkg
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: covered by the GPU tests")
+    with pytest.raises(pkg.NVFP4Error) as e:
+        pkg.nvfp4_gemv_plan(128, 256, 1)
+    assert e.value.status == 5          # CUDA error: no device

@@ -1,0 +1,77 @@
+"""Host-side logic of bench.py without a GPU: the multi-rank aggregation (two gloo ranks on the CPU,
+as torchrun would start them), the reference arm's JSON line, and the traffic record lookup."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import bench
+
+    dist = bench.dist_init(world)
+    # rank r moved (r + 1) GB in (r + 1) * 0.5 s
+    total, slowest = bench.aggregate(dist, (rank + 1) * 1e9, (rank + 1) * 0.5)
+    q.put((rank, total, slowest))
+    dist.destroy_process_group()
+
+
+def test_two_rank_aggregation_is_sum_over_max():
+    import torch.multiprocessing as mp
+
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    for _, total, slowest in res:
+        assert total == 3e9 and slowest == 1.0     # whole-job bytes over the slowest rank
+
+
+def test_reference_arm_json_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--config", "c1", "--steps", "5", "--warmup", "3",
+                          "--reference-seconds", "2"], capture_output=True, text=True,
+                         timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_warmup_below_three_is_rejected():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert out.returncode != 0
+
+
+def test_traffic_record_requires_matching_sources(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert len(bench.kernel_source_digest()) == 16
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (prof / "traffic_c9.txt").write_text(
+        "kernel_sources_sha256_16 = 0000000000000000\n"
+        "dram_bytes_read_per_launch = 100\ndram_bytes_write_per_launch = 20\n")
+    monkeypatch.setattr(bench, "kernel_source_digest", lambda: "0000000000000000")
+    assert bench.recorded_traffic("c9") == 120.0
+    monkeypatch.setattr(bench, "kernel_source_digest", lambda: "ffffffffffffffff")
+    assert bench.recorded_traffic("c9") is None
