@@ -248,8 +248,9 @@ def time_device(pkg, w, sets, outs, plan, steps, warmup, stream):
     g_full = make_graph(chunk, 0) if chunk else None
     rem = steps % chunk if chunk else 0
     g_rem = make_graph(rem, 0) if rem else None
-    for _ in range(2):                             # graph warm-up
-        g_full.replay()
+    with torch.cuda.stream(stream):                # graph warm-up
+        for _ in range(2):
+            g_full.replay()
     stream.synchronize()
     return g_full, g_rem, chunk, rem
 
@@ -281,7 +282,7 @@ def run_ours(args):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_id)
-    with sampler:
+    with sampler, torch.cuda.stream(stream):        # graphs replay on the current stream
         barrier(dist)
         torch.cuda.synchronize(device)
         ev0.record(stream)

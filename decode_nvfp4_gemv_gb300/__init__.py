@@ -153,8 +153,8 @@ def _stream_handle(stream, tensors):
 
 def _marshal(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream):
     M, K, L = int(M), int(K), int(L)
-    if M < 0 or K <= 0 or L < 0 or K % 16:
-        # let the library produce the status for invalid shapes (no memory is touched)
+    if M <= 0 or K <= 0 or L <= 0 or K % 16:
+        # empty problems touch no memory; invalid shapes get the library's status
         need = {k: 0 for k in _ITEM}
     else:
         need = {"A": M * L * K // 2, "sfa": M * L * K // 16, "b": L * K // 2, "sfb": L * K // 16,
