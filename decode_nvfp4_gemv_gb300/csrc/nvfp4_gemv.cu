@@ -11,6 +11,7 @@
 
 #include "../../include/nvfp4_gemv.h"
 #include "gemv_kernels.cuh"
+#include "gemv_tma.cuh"
 
 namespace {
 
@@ -37,6 +38,7 @@ struct DeviceInfo {
   int major = 0, minor = 0;
   int sms = 0;
   int max_smem_optin = 0;   // bytes of shared memory one CTA may opt into
+  int max_smem_sm = 0;      // bytes of shared memory per SM
   int pageable_access = 0;  // the device can read pageable host memory
 };
 
@@ -57,6 +59,8 @@ void init_device(int dev) {
       (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) ||
       (e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                   dev)) ||
+      (e = cudaDeviceGetAttribute(&d.max_smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                  dev)) ||
       (e = cudaDeviceGetAttribute(&d.pageable_access, cudaDevAttrPageableMemoryAccess, dev))) {
     d.err = e;
     return;
@@ -64,7 +68,9 @@ void init_device(int dev) {
   if (d.major != 10 || d.minor != 3) return;  // no kernels for other architectures
   if ((e = prepare_stream_kernel<1>(d.max_smem_optin)) ||
       (e = prepare_stream_kernel<2>(d.max_smem_optin)) ||
-      (e = prepare_stream_kernel<4>(d.max_smem_optin))) {
+      (e = prepare_stream_kernel<4>(d.max_smem_optin)) ||
+      (e = cudaFuncSetAttribute(nvfp4::gemv_tma_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin))) {
     d.err = e;
     return;
   }
@@ -174,44 +180,32 @@ int stream_occupancy(const DeviceInfo& d, int R, int threads, int64_t smem) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Fills every field of *pl for (M, K, L); `forced` fields (non-zero) are honoured or rejected.
-int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan* forced,
-              nvfp4_plan* pl) {
-  nvfp4_plan f;
-  memset(&f, 0, sizeof f);
-  if (forced) f = *forced;
-  if (f.reserved[0] || f.reserved[1] || f.reserved[2])
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "plan.reserved must be zero");
-  const bool stream_ok = (K % 32 == 0) && K <= max_stream_k(d);
-  int kernel = f.kernel;
-  if (kernel == NVFP4_KERNEL_AUTO) kernel = stream_ok ? NVFP4_KERNEL_STREAM : NVFP4_KERNEL_SIMPLE;
-  if (kernel != NVFP4_KERNEL_SIMPLE && kernel != NVFP4_KERNEL_STREAM)
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown kernel %d", kernel);
-  if (kernel == NVFP4_KERNEL_STREAM && !stream_ok)
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool stream_ok(const DeviceInfo& d, int64_t K) { return K % 32 == 0 && K <= max_stream_k(d); }
+
+int plan_simple(const DeviceInfo& d, int64_t M, int64_t L, const nvfp4_plan& f, nvfp4_plan* pl) {
+  if (f.warps_per_cta > 8)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "simple kernel: at most 8 warps per CTA");
+  const int W = f.warps_per_cta ? f.warps_per_cta : 8;
+  const int64_t rows = M * L;
+  int64_t ctas = f.ctas_per_batch ? (int64_t)f.ctas_per_batch * L
+                                  : std::min<int64_t>(ceil_div(rows, W), (int64_t)d.sms * 8);
+  if (ctas > (int64_t(1) << 31) - 1) ctas = (int64_t(1) << 31) - 1;
+  pl->kernel = NVFP4_KERNEL_SIMPLE;
+  pl->warps_per_cta = W;
+  pl->ctas_per_batch = (int32_t)std::max<int64_t>(1, ceil_div(ctas, L));
+  pl->rows_per_warp = 1;
+  pl->k_split = 1;
+  return NVFP4_OK;
+}
+
+int plan_stream(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan& f,
+                nvfp4_plan* pl) {
+  if (!stream_ok(d, K))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                 "stream kernel needs K %% 32 == 0 and K <= %lld (K=%lld)",
                 (long long)max_stream_k(d), (long long)K);
-  if (f.warps_per_cta < 0 || f.warps_per_cta > 32 || f.rows_per_warp < 0 || f.k_split < 0 ||
-      f.ctas_per_batch < 0)
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "negative or oversized plan field");
-  memset(pl, 0, sizeof *pl);
-  pl->kernel = kernel;
-
-  if (kernel == NVFP4_KERNEL_SIMPLE) {
-    if (f.warps_per_cta > 8)
-      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "simple kernel: at most 8 warps per CTA");
-    const int W = f.warps_per_cta ? f.warps_per_cta : 8;
-    const int64_t rows = M * L;
-    int64_t ctas = f.ctas_per_batch ? (int64_t)f.ctas_per_batch * L
-                                    : std::min<int64_t>(ceil_div(rows, W), (int64_t)d.sms * 8);
-    if (ctas > (int64_t(1) << 31) - 1) ctas = (int64_t(1) << 31) - 1;
-    pl->warps_per_cta = W;
-    pl->ctas_per_batch = (int32_t)std::max<int64_t>(1, ceil_div(ctas, L));
-    pl->rows_per_warp = 1;
-    pl->k_split = 1;
-    return NVFP4_OK;
-  }
-
   if (f.warps_per_cta > 16)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "stream kernel: at most 16 warps per CTA");
   const int W = f.warps_per_cta ? f.warps_per_cta : (int)(kStreamThreads / 32);
@@ -255,11 +249,118 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
   if (stream_smem_bytes(K, S, rows_cap) > d.max_smem_optin)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "plan needs %lld bytes of shared memory",
                 (long long)stream_smem_bytes(K, S, rows_cap));
+  pl->kernel = NVFP4_KERNEL_STREAM;
   pl->rows_per_warp = R;
   pl->k_split = (int32_t)S;
   pl->ctas_per_batch = (int32_t)P;
   pl->warps_per_cta = W;
   return NVFP4_OK;
+}
+
+// Shared-memory layout of the TMA kernel: barriers and abort flag, the decoded vector, its fp32
+// block scales, the per-(row, warp) partial sums, then NS ring stages of TR rows (A rows, then sfa
+// rows).  Every region starts 16-byte aligned, ring stages 128-byte aligned.
+struct TmaLayout {
+  int64_t b_off, sb_off, part_off, ring_off, sfa_off, stage_bytes, total;
+};
+
+TmaLayout tma_layout(int64_t K, int64_t TR, int64_t NS, int64_t rows_cap, int64_t Wc) {
+  TmaLayout t;
+  t.b_off = 256;
+  t.sb_off = t.b_off + 2 * K;
+  t.part_off = align_up(t.sb_off + K / 4, 16);
+  t.ring_off = align_up(t.part_off + 4 * rows_cap * Wc, 128);
+  t.sfa_off = align_up(TR * (K / 2), 128);
+  t.stage_bytes = align_up(t.sfa_off + TR * (K / 16), 128);
+  t.total = t.ring_off + NS * t.stage_bytes;
+  return t;
+}
+
+constexpr int64_t kTmaStageTarget = 32768;  // A bytes per ring stage the planner aims for
+
+int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan& f,
+             nvfp4_plan* pl) {
+  if (K % 256 != 0)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernel needs K %% 256 == 0 (K=%lld)",
+                (long long)K);
+  if (f.warps_per_cta > 16)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernel: at most 16 consumer warps");
+  if (f.rows_per_warp && f.rows_per_warp != 4)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernel processes 4 rows per warp");
+  if (f.tile_rows < 0 || f.tile_rows > 256 || f.stages < 0 || f.stages == 1 ||
+      f.stages > nvfp4::kTmaMaxStages)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tile_rows must be 1..256, stages 2..%d",
+                nvfp4::kTmaMaxStages);
+  const int64_t Wc = f.warps_per_cta ? f.warps_per_cta : 8;
+  // two CTAs per SM if the ring fits, else one
+  for (int occ = 2; occ >= 1; --occ) {
+    const int64_t budget =
+        std::min<int64_t>(d.max_smem_optin, d.max_smem_sm / occ - 1024);
+    const int64_t slots = (int64_t)d.sms * occ;
+    int64_t P = f.ctas_per_batch ? f.ctas_per_batch : std::max<int64_t>(1, slots / L);
+    P = std::min(P, M);
+    const int64_t rows_cap = ceil_div(M, P);
+    int64_t TR = f.tile_rows;
+    if (TR == 0) {
+      TR = std::max<int64_t>(1, kTmaStageTarget / (K / 2));
+      if (TR >= 4) TR -= TR % 4;
+      TR = std::min<int64_t>(TR, std::max<int64_t>(4, align_up(rows_cap, 4)));
+    }
+    int64_t NS = f.stages;
+    if (NS == 0) {
+      for (int64_t ns = nvfp4::kTmaMaxStages; ns >= 2; --ns)
+        if (tma_layout(K, TR, ns, rows_cap, Wc).total <= budget) {
+          NS = ns;
+          break;
+        }
+      if (NS == 0) continue;
+    }
+    if (tma_layout(K, TR, NS, rows_cap, Wc).total > d.max_smem_optin) continue;
+    if (P * L > (int64_t(1) << 31) - 1)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
+    pl->kernel = NVFP4_KERNEL_TMA;
+    pl->rows_per_warp = 4;
+    pl->k_split = 1;
+    pl->ctas_per_batch = (int32_t)P;
+    pl->warps_per_cta = (int32_t)Wc;
+    pl->tile_rows = (int32_t)TR;
+    pl->stages = (int32_t)NS;
+    return NVFP4_OK;
+  }
+  return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernel: K=%lld does not fit shared memory",
+              (long long)K);
+}
+
+// Fills every field of *pl for (M, K, L); `forced` fields (non-zero) are honoured or rejected.
+int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan* forced,
+              nvfp4_plan* pl) {
+  nvfp4_plan f;
+  memset(&f, 0, sizeof f);
+  if (forced) f = *forced;
+  if (f.reserved) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "plan.reserved must be zero");
+  if (f.warps_per_cta < 0 || f.rows_per_warp < 0 || f.k_split < 0 || f.ctas_per_batch < 0 ||
+      f.tile_rows < 0 || f.stages < 0)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "negative plan field");
+  memset(pl, 0, sizeof *pl);
+  switch (f.kernel) {
+    case NVFP4_KERNEL_SIMPLE: return plan_simple(d, M, L, f, pl);
+    case NVFP4_KERNEL_STREAM: return plan_stream(d, M, K, L, f, pl);
+    case NVFP4_KERNEL_TMA: return plan_tma(d, M, K, L, f, pl);
+    case NVFP4_KERNEL_AUTO: break;
+    default: return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown kernel %d", f.kernel);
+  }
+  // automatic: the TMA ring when every CTA gets at least 8 rows, else the stream kernel, else the
+  // simple kernel
+  const int64_t rows_per_cta = (M * L) / std::max<int64_t>(1, (int64_t)d.sms * 2);
+  if (K % 256 == 0 && rows_per_cta >= 8) {
+    char saved[sizeof g_last_error];
+    memcpy(saved, g_last_error, sizeof saved);
+    if (plan_tma(d, M, K, L, f, pl) == NVFP4_OK) return NVFP4_OK;
+    memcpy(g_last_error, saved, sizeof saved);
+    memset(pl, 0, sizeof *pl);
+  }
+  if (stream_ok(d, K)) return plan_stream(d, M, K, L, f, pl);
+  return plan_simple(d, M, L, f, pl);
 }
 
 int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const uint8_t* sfa,
@@ -271,7 +372,7 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     const int64_t grid = std::min<int64_t>((int64_t)pl.ctas_per_batch * L, (int64_t(1) << 31) - 1);
     nvfp4::gemv_simple_kernel<<<(unsigned)grid, threads, 0, stream>>>(A, sfa, b, sfb, g_a, g_b, c,
                                                                       M, K, L);
-  } else {
+  } else if (pl.kernel == NVFP4_KERNEL_STREAM) {
     nvfp4::StreamArgs a;
     a.A = A; a.sfa = sfa; a.b = b; a.sfb = sfb; a.c = c;
     a.g_a = g_a; a.g_b = g_b;
@@ -288,6 +389,24 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
       case 2: nvfp4::gemv_stream_kernel<2><<<grid, threads, smem, stream>>>(a); break;
       default: nvfp4::gemv_stream_kernel<4><<<grid, threads, smem, stream>>>(a); break;
     }
+  } else {
+    nvfp4::TmaArgs a;
+    a.A = A; a.sfa = sfa; a.b = b; a.sfb = sfb; a.c = c;
+    a.g_a = g_a; a.g_b = g_b;
+    a.M = M; a.K = K; a.L = L;
+    a.P = pl.ctas_per_batch;
+    a.tile_rows = pl.tile_rows;
+    a.stages = pl.stages;
+    a.rows_cap = (int32_t)ceil_div(M, pl.ctas_per_batch);
+    const TmaLayout t = tma_layout(K, pl.tile_rows, pl.stages, a.rows_cap, pl.warps_per_cta);
+    a.stage_bytes = (uint32_t)t.stage_bytes;
+    a.sfa_off = (uint32_t)t.sfa_off;
+    a.b_off = (uint32_t)t.b_off;
+    a.sb_off = (uint32_t)t.sb_off;
+    a.part_off = (uint32_t)t.part_off;
+    a.ring_off = (uint32_t)t.ring_off;
+    const unsigned grid = (unsigned)(pl.ctas_per_batch * L);
+    nvfp4::gemv_tma_kernel<<<grid, threads + 32, (size_t)t.total, stream>>>(a);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");

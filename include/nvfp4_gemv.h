@@ -74,8 +74,10 @@ typedef enum nvfp4_status {
 typedef enum nvfp4_kernel {
   NVFP4_KERNEL_AUTO = 0,    /* the planner's choice */
   NVFP4_KERNEL_SIMPLE = 1,  /* one warp per output row, byte loads; any K % 16 == 0 */
-  NVFP4_KERNEL_STREAM = 2   /* 128-bit streaming loads, vector staged in shared memory, intra-CTA
+  NVFP4_KERNEL_STREAM = 2,  /* 128-bit streaming loads, vector staged in shared memory, intra-CTA
                                split-K; needs K % 32 == 0 and K <= nvfp4_max_stream_k() */
+  NVFP4_KERNEL_TMA = 3      /* row tiles streamed into a shared-memory ring by bulk async copies
+                               (TMA) and mbarriers; needs K % 256 == 0 and at least 4 rows per CTA */
 } nvfp4_kernel;
 
 /*
@@ -85,11 +87,14 @@ typedef enum nvfp4_kernel {
  */
 typedef struct nvfp4_plan {
   int32_t kernel;          /* nvfp4_kernel */
-  int32_t rows_per_warp;   /* STREAM: rows a warp processes together (1, 2 or 4) */
+  int32_t rows_per_warp;   /* STREAM: rows a warp processes together (1, 2 or 4); TMA: 4 */
   int32_t k_split;         /* STREAM: K slices per row inside a CTA (1 .. ceil(K/1024)) */
-  int32_t ctas_per_batch;  /* STREAM/SIMPLE: CTAs sharing one batch's rows (1 .. M) */
-  int32_t warps_per_cta;   /* SIMPLE: 1 .. 8; STREAM: 1 .. 16 */
-  int32_t reserved[3];     /* must be zero */
+  int32_t ctas_per_batch;  /* all kernels: CTAs sharing one batch's rows (1 .. M) */
+  int32_t warps_per_cta;   /* SIMPLE: 1 .. 8; STREAM: 1 .. 16; TMA: consumer warps 1 .. 16 (one
+                              producer warp is added) */
+  int32_t tile_rows;       /* TMA: rows per ring stage (1 .. 256) */
+  int32_t stages;          /* TMA: ring stages (2 .. 8) */
+  int32_t reserved;        /* must be zero */
 } nvfp4_plan;
 
 /*
