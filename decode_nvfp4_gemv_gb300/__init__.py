@@ -24,12 +24,13 @@ from .build import LIB_PATH
 
 __all__ = [
     "NVFP4Error", "Plan", "KERNEL_AUTO", "KERNEL_SIMPLE", "KERNEL_STREAM", "KERNEL_TMA",
-    "library_path",
+    "KERNEL_TMA_RV", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "library_path",
     "load_library", "nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_plan",
     "nvfp4_max_stream_k", "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version", "gemv",
 ]
 
-KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV = 0, 1, 2, 3, 4
+FLAG_EARLY_WEIGHTS, FLAG_NO_PDL = 1, 2
 
 OK, ERR_INVALID_VALUE, ERR_MISALIGNED, ERR_UNSUPPORTED_SHAPE, ERR_ARCH, ERR_CUDA = range(6)
 
@@ -45,10 +46,10 @@ class Plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("rows_per_warp", ctypes.c_int32),
                 ("k_split", ctypes.c_int32), ("ctas_per_batch", ctypes.c_int32),
                 ("warps_per_cta", ctypes.c_int32), ("tile_rows", ctypes.c_int32),
-                ("stages", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("stages", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
     def as_dict(self):
-        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+        return {f: getattr(self, f) for f, _ in self._fields_}
 
     def __repr__(self):
         return f"Plan({self.as_dict()})"

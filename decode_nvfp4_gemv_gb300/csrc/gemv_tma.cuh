@@ -1,30 +1,43 @@
-// TMA-ring NVFP4 GEMV kernel for GB300 (sm_103a): the bandwidth path for K % 256 == 0.
+// TMA-ring NVFP4 GEMV kernels for GB300 (sm_103a): the bandwidth path for K % 256 == 0.
 //
-// Why: the work is a read-once stream of A (8/9 of the bytes) and sfa (1/9).  Holding enough
-// bytes in flight to cover HBM latency with per-thread loads costs registers and occupancy; the
-// Tensor Memory Accelerator's bulk copies instead move whole row tiles into shared memory with one
-// instruction each and need no registers to keep them in flight.
+// Why: the work is a read-once stream of A (8/9 of the bytes) and sfa (1/9).  Holding enough bytes
+// in flight to cover HBM latency with per-thread loads costs registers and occupancy; the Tensor
+// Memory Accelerator's bulk copies move whole row tiles into shared memory with one instruction
+// each and need no registers to keep them in flight.  (Measured on GB300: many small bulk copies
+// are slow, so tiles are whole rows and one copy each.)
 //
 // Decomposition.  CTA (l, p), p < P, owns the contiguous rows [M*p/P, M*(p+1)/P) of batch l.
 // Because rows are contiguous in memory, the CTA's A bytes (and its sfa bytes) form one
 // contiguous run, cut into tiles of TR whole rows.  Warp W_c (the last) is the producer: one lane
 // walks the tiles and, for each, waits until ring stage s = T mod NS is free, then issues two
 // cp.async.bulk copies (the tile's A rows and sfa rows) that complete the stage's `full` mbarrier
-// by transaction count.  Warps 0 .. W_c-1 are consumers: while the first copies are in flight they
-// decode b[l] into shared memory (one f16x2 word per packed byte, swizzled as in the stream
-// kernel) and sfb[l] into fp32; then, for each tile, they wait on `full`, process their items, and
-// release the stage by arriving on its `empty` mbarrier (one arrival per consumer warp).
+// by transaction count.  Warps 0 .. W_c-1 consume: for each tile they wait on `full`, process
+// their items and release the stage by arriving on its `empty` mbarrier (one arrival per warp).
 //
-// Items.  A tile of TR rows and K columns is cut into groups of 4 rows x 1024-element segments;
-// item i goes to consumer warp i mod W_c.  For an item, lane t takes 16 bytes (32 elements, two
-// scale blocks) of each of the 4 rows at k = 1024 * seg + 32 t, multiplies them with the staged
-// vector words by packed f16 FMAs (exact block partials, as in the stream kernel), scales each
-// block partial by sfa * sfb in fp32 and accumulates per row.  A warp's items within a tile come in
-// increasing order, so its row group changes monotonically; when it changes (and at the tile end)
-// the 4 row sums are reduced across the warp and written to partial[row][warp] in shared memory
-// (each slot is written at most once; slots a warp never touches stay zero).  After the last
-// tile, thread t sums partial[t][0 .. W_c) in warp order (deterministic), applies g_a and g_b in
-// fp32 and stores fp16.
+// Items.  A tile is cut into groups of 4 rows x 1024-element segments.  For an item, lane t takes
+// 16 bytes (32 elements, two scale blocks) of each of the 4 rows at k = 1024 * seg + 32 t,
+// multiplies them with the vector's f16x2 words by packed f16 FMAs (exact block partials), scales
+// each block partial by sfa * sfb in fp32 and accumulates per row.  A warp reduces its 4 row sums
+// across lanes and writes them to partial[row][slot] in shared memory; after the last tile,
+// thread t sums partial[t][0 .. slots) in slot order (deterministic), applies g_a and g_b in fp32
+// and stores fp16.
+//
+// Two variants differ in where the vector lives:
+//   gemv_tma_kernel        b[l] decoded into shared memory (one f16x2 word per packed byte,
+//                          swizzled as in the stream kernel) and sfb[l] as fp32; item i goes to
+//                          warp i mod W_c.  Any K % 256 == 0 within the shared-memory budget.
+//   gemv_tma_rv_kernel<NSW> when W_c divides the segment count nseg (each warp owns NSW = nseg/W_c
+//                          segments, for every row group) or nseg divides W_c (each warp owns one
+//                          segment and every (W_c/nseg)-th row group): a warp touches the same
+//                          segments in every tile, so it decodes its slice of b into registers once.
+//                          No vector reads in the inner loop, and the ring gets the shared memory.
+//
+// Programmatic dependent launch.  The host launches with programmatic stream serialization, so the
+// next kernel in the stream may be scheduled while this one drains.  Every thread executes
+// griddepcontrol.wait before its first access to memory a preceding kernel may write; with the
+// `early_weights` flag (the caller guarantees that no kernel still running writes A or sfa) the
+// producer starts streaming A and sfa before that wait and only the vector, its scales and the
+// outputs wait.  griddepcontrol.wait returns at once for a launch without the attribute.
 //
 // Bounded waits.  Every mbarrier wait gives up after one second of wall time (%globaltimer).  A
 // consumer that gives up sets a shared abort flag; a producer that gives up waits (again bounded)
@@ -41,6 +54,7 @@ namespace nvfp4 {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 constexpr int kTmaMaxStages = 8;
+constexpr uint32_t kTmaHeaderBytes = 256;         // barriers (16 B per stage) + abort flag
 
 struct TmaArgs {
   const uint8_t* A;
@@ -50,99 +64,193 @@ struct TmaArgs {
   uint16_t* c;
   float g_a, g_b;
   int64_t M, K, L;
-  int32_t P;           // CTAs per batch
-  int32_t tile_rows;   // TR: rows per ring stage (a multiple of 4, or less than 4 only if M is)
-  int32_t stages;      // NS <= kTmaMaxStages
-  int32_t rows_cap;    // ceil(M / P)
+  int32_t P;             // CTAs per batch
+  int32_t tile_rows;     // TR: rows per ring stage
+  int32_t stages;        // NS <= kTmaMaxStages
+  int32_t rows_cap;      // ceil(M / P)
+  int32_t slots;         // partial sums per row (consumer warps, or segments for the rv kernel)
+  int32_t early_weights; // 1: stream A and sfa before the programmatic-launch wait
   uint32_t stage_bytes;  // bytes per ring stage (A rows, then sfa rows at sfa_off)
   uint32_t sfa_off;      // offset of the sfa rows inside a stage (16-byte aligned)
-  uint32_t b_off, sb_off, part_off, ring_off;  // shared-memory layout (bytes)
+  uint32_t b_off, sb_off, part_off, ring_off;  // shared-memory layout (bytes); b/sb unused by rv
 };
 
-__device__ __forceinline__ void tma_flush(float (&acc)[4], int lane, int rg, int rows_t,
-                                          float* part_tile, int Wc, int cw) {
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+
+// One row group (4 rows) times one 32-element lane slice: decode, exact block partials, scale.
+// bw: the 16 vector words for this lane's 32 elements; sb: the two vector block scales.
+__device__ __forceinline__ void item_compute4(const uint4 (&av)[4], const uint16_t (&sv)[4],
+                                              const uint32_t (&bw)[16], float2 sb,
+                                              float (&acc)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t h[16];
+    e2m1x8_to_f16x2x4(av[i].x, h[0], h[1], h[2], h[3]);
+    e2m1x8_to_f16x2x4(av[i].y, h[4], h[5], h[6], h[7]);
+    e2m1x8_to_f16x2x4(av[i].z, h[8], h[9], h[10], h[11]);
+    e2m1x8_to_f16x2x4(av[i].w, h[12], h[13], h[14], h[15]);
+    uint32_t p0 = 0u, p1 = 0u;  // f16x2 zeros
+#pragma unroll
+    for (int q = 0; q < 8; ++q) hfma2(p0, h[q], bw[q]);
+#pragma unroll
+    for (int q = 8; q < 16; ++q) hfma2(p1, h[q], bw[q]);
+    const float2 sa = f16x2_to_f32x2(e4m3x2_to_f16x2(sv[i]));
+    acc[i] = fmaf(f16x2_hsum_f32(p0), sa.x * sb.x, acc[i]);
+    acc[i] = fmaf(f16x2_hsum_f32(p1), sa.y * sb.y, acc[i]);
+  }
+}
+
+// Reduces the 4 row sums of a group across the warp and stores them to partial[row][slot].
+__device__ __forceinline__ void tma_flush(float (&acc)[4], int lane, int row0, int rows_t,
+                                          float* part_tile, int slots, int slot) {
   const float v = warp_reduce_rows<4>(acc, lane);
   const int j = lane >> 3;  // lanes 8j .. 8j+7 hold row j of the group
-  if ((lane & 7) == 0 && 4 * rg + j < rows_t) part_tile[(4 * rg + j) * Wc + cw] = v;
+  if ((lane & 7) == 0 && row0 + j < rows_t) part_tile[(row0 + j) * slots + slot] = v;
 #pragma unroll
   for (int i = 0; i < 4; ++i) acc[i] = 0.f;
 }
 
+// Shared prologue: CTA geometry, barrier initialisation, dependent-launch trigger.
+struct TmaCta {
+  int64_t l, m0;
+  int n, NT, Wc;
+};
+
+__device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
+                                            volatile int* abort_flag) {
+  TmaCta g;
+  g.l = blockIdx.x / p.P;
+  const int64_t pi = blockIdx.x - g.l * p.P;
+  g.m0 = (p.M * pi) / p.P;
+  const int64_t m1 = (p.M * (pi + 1)) / p.P;
+  g.n = (int)(m1 - g.m0);
+  g.NT = (g.n + p.tile_rows - 1) / p.tile_rows;
+  g.Wc = (blockDim.x >> 5) - 1;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(smem_addr(&bars[s]), 1);                          // producer's arrive + bytes
+      mbar_init(smem_addr(&bars[p.stages + s]), (uint32_t)g.Wc);  // one arrival per consumer
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  return g;
+}
+
+// The producer lane: streams the CTA's row tiles into the ring.
+__device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, uint64_t* bars,
+                                            volatile int* abort_flag, uint8_t* ring) {
+  const int64_t K2 = p.K >> 1, K16 = p.K >> 4;
+  const int NS = p.stages, TR = p.tile_rows;
+  const uint64_t pol = l2_evict_first_policy();
+  const uint8_t* A_c = p.A + (g.l * p.M + g.m0) * K2;
+  const uint8_t* S_c = p.sfa + (g.l * p.M + g.m0) * K16;
+  int issued = 0;
+  bool ok = true;
+  for (int T = 0; T < g.NT; ++T) {
+    const int s = T % NS;
+    if (T >= NS &&
+        !mbar_wait_bounded(smem_addr(&bars[NS + s]), ((T / NS) - 1) & 1, kWaitLimitNs)) {
+      ok = false;
+      break;
+    }
+    if (*abort_flag) {
+      ok = false;
+      break;
+    }
+    const int rows_t = min(TR, g.n - T * TR);
+    const uint32_t bytesA = (uint32_t)(rows_t * K2), bytesS = (uint32_t)(rows_t * K16);
+    const uint32_t full = smem_addr(&bars[s]);
+    uint8_t* st = ring + (size_t)s * p.stage_bytes;
+    mbar_arrive_expect_tx(full, bytesA + bytesS);
+    bulk_copy_g2s(smem_addr(st), A_c + (int64_t)T * TR * K2, bytesA, full, pol);
+    bulk_copy_g2s(smem_addr(st + p.sfa_off), S_c + (int64_t)T * TR * K16, bytesS, full, pol);
+    issued = T + 1;
+  }
+  if (!ok) {
+    *abort_flag = 1;
+    // let every copy already issued land before this warp (and so the CTA) can exit
+    for (int T = max(0, issued - NS); T < issued; ++T)
+      mbar_wait_bounded(smem_addr(&bars[T % NS]), (T / NS) & 1, kWaitLimitNs);
+  }
+}
+
+// Consumer wait for tile T; the verdict is voted so the whole warp leaves together.
+__device__ __forceinline__ bool tma_consume_wait(const TmaArgs& p, uint64_t* bars,
+                                                 volatile int* abort_flag, int T, int lane) {
+  const bool ready =
+      mbar_wait_bounded(smem_addr(&bars[T % p.stages]), (T / p.stages) & 1, kWaitLimitNs);
+  if (!__all_sync(kFullMask, ready && *abort_flag == 0)) {
+    if (lane == 0) *abort_flag = 1;
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void tma_release(const TmaArgs& p, uint64_t* bars, int T, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_addr(&bars[p.stages + T % p.stages]));
+}
+
+__device__ __forceinline__ void tma_epilogue(const TmaArgs& p, const TmaCta& g, const float* part,
+                                             volatile int* abort_flag) {
+  const bool failed = *abort_flag != 0;
+  uint16_t* c_c = p.c + g.l * p.M + g.m0;
+  for (int t = threadIdx.x; t < g.n; t += 32 * g.Wc) {
+    float v = 0.f;
+    for (int q = 0; q < p.slots; ++q) v += part[t * p.slots + q];
+    c_c[t] = failed ? (uint16_t)0x7E00 : f32_to_f16_bits((v * p.g_a) * p.g_b);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Vector in shared memory (general K).
+// ------------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int64_t K = p.K, K2 = p.K >> 1, K16 = p.K >> 4;
-  const int NS = p.stages;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);  // full[0..NS), empty[NS..2NS)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kTmaMaxStages);
   uint32_t* bq = reinterpret_cast<uint32_t*>(smem + p.b_off);
   float* sbf = reinterpret_cast<float*>(smem + p.sb_off);
   float* part = reinterpret_cast<float*>(smem + p.part_off);
   uint8_t* ring = smem + p.ring_off;
+  const int64_t K = p.K, K2 = p.K >> 1, K16 = p.K >> 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int Wc = (blockDim.x >> 5) - 1;  // consumer warps; warp Wc produces
-  const int64_t l = blockIdx.x / p.P;
-  const int64_t pi = blockIdx.x - l * p.P;
-  const int64_t m0 = (p.M * pi) / p.P, m1 = (p.M * (pi + 1)) / p.P;
-  const int n = (int)(m1 - m0);
-  const int TR = p.tile_rows;
-  const int NT = (n + TR - 1) / TR;
-
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(smem_addr(&bars[s]), 1);            // producer's arrive + copy bytes
-      mbar_init(smem_addr(&bars[NS + s]), (uint32_t)Wc);  // one arrival per consumer warp
-    }
-    *abort_flag = 0;
-    mbar_init_fence();
-  }
-  __syncthreads();
-
-  if (warp == Wc) {
-    // ------------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      const uint8_t* A_c = p.A + (l * p.M + m0) * K2;
-      const uint8_t* S_c = p.sfa + (l * p.M + m0) * K16;
-      int issued = 0;
-      bool ok = true;
-      for (int T = 0; T < NT; ++T) {
-        const int s = T % NS;
-        if (T >= NS && !mbar_wait_bounded(smem_addr(&bars[NS + s]), ((T / NS) - 1) & 1,
-                                          kWaitLimitNs)) {
-          ok = false;
-          break;
-        }
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        const int rows_t = min(TR, n - T * TR);
-        const uint32_t bytesA = (uint32_t)(rows_t * K2), bytesS = (uint32_t)(rows_t * K16);
-        const uint32_t full = smem_addr(&bars[s]);
-        uint8_t* st = ring + (size_t)s * p.stage_bytes;
-        mbar_arrive_expect_tx(full, bytesA + bytesS);
-        bulk_copy_g2s(smem_addr(st), A_c + (int64_t)T * TR * K2, bytesA, full, pol);
-        bulk_copy_g2s(smem_addr(st + p.sfa_off), S_c + (int64_t)T * TR * K16, bytesS, full, pol);
-        issued = T + 1;
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        // let every copy already issued land before this warp (and so the CTA) can exit
-        for (int T = max(0, issued - NS); T < issued; ++T)
-          mbar_wait_bounded(smem_addr(&bars[T % NS]), (T / NS) & 1, kWaitLimitNs);
-      }
-    }
+  const TmaCta g = tma_setup(p, bars, abort_flag);
+  if (!p.early_weights) pdl_wait();
+  if (warp == g.Wc) {
+    if (lane == 0) tma_produce(p, g, bars, abort_flag, ring);
     return;
   }
+  if (p.early_weights) pdl_wait();
 
-  // -------------------------------------------------------------------- consumers
-  const int cw = warp;
-  const int ctid = tid;  // 0 .. 32*Wc - 1
-  const int cthreads = 32 * Wc;
-
-  const uint8_t* b_l = p.b + l * K2;
-  for (int64_t i = ctid; i < K2 / 16; i += cthreads) {
+  const int Wc = g.Wc, cw = warp, cthreads = 32 * Wc;
+  const uint8_t* b_l = p.b + g.l * K2;
+  for (int64_t i = threadIdx.x; i < K2 / 16; i += cthreads) {
     const uint4 v = ld_ro_v4(b_l + 16 * i);
     uint4 w0, w1, w2, w3;
     e2m1x8_to_f16x2x4(v.x, w0.x, w0.y, w0.z, w0.w);
@@ -156,66 +264,163 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
     dst[swz_chunk(q + 2)] = w2;
     dst[swz_chunk(q + 3)] = w3;
   }
-  const uint8_t* sfb_l = p.sfb + l * K16;
-  for (int64_t i = ctid; i < K16 / 2; i += cthreads) {
+  const uint8_t* sfb_l = p.sfb + g.l * K16;
+  for (int64_t i = threadIdx.x; i < K16 / 2; i += cthreads) {
     const float2 sc = f16x2_to_f32x2(e4m3x2_to_f16x2(ld_ro_u16(sfb_l + 2 * i)));
     sbf[2 * i] = sc.x;
     sbf[2 * i + 1] = sc.y;
   }
-  for (int i = ctid; i < p.rows_cap * Wc; i += cthreads) part[i] = 0.f;
+  for (int i = threadIdx.x; i < p.rows_cap * p.slots; i += cthreads) part[i] = 0.f;
   named_barrier(1, (uint32_t)cthreads);
 
+  // Per-thread constants: a lane's chunk swizzle term is (lane >> 1) & 3 for every segment.
   const int nseg = (int)((K + kStep - 1) / kStep);
+  const uint32_t K2u = (uint32_t)K2, K16u = (uint32_t)K16, Ku = (uint32_t)K;
+  const uint32_t ring32 = smem_addr(ring), bq32 = smem_addr(bq), sb32 = smem_addr(sbf);
+  const uint32_t x = ((uint32_t)lane >> 1) & 3u;
+  const uint32_t bsw[4] = {16u * (0u ^ x), 16u * (1u ^ x), 16u * (2u ^ x), 16u * (3u ^ x)};
+  const int rg0 = cw / nseg, sg0 = cw - rg0 * nseg;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  bool aborted = false;
-  for (int T = 0; T < NT; ++T) {
-    const int s = T % NS;
-    // the verdict is voted so the whole warp leaves together (shuffles follow)
-    const bool ready = mbar_wait_bounded(smem_addr(&bars[s]), (T / NS) & 1, kWaitLimitNs);
-    if (!__all_sync(kFullMask, ready && *abort_flag == 0)) {
-      if (lane == 0) *abort_flag = 1;
-      aborted = true;
-      break;
-    }
-    const int rows_t = min(TR, n - T * TR);
-    const uint8_t* stA = ring + (size_t)s * p.stage_bytes;
-    const uint8_t* stS = stA + p.sfa_off;
-    float* part_tile = part + (size_t)T * TR * Wc;
-    const int items = ((rows_t + 3) >> 2) * nseg;
-    int cur_rg = -1;
-    for (int it = cw; it < items; it += Wc) {
-      const int rg = it / nseg, sg = it - rg * nseg;
-      if (rg != cur_rg) {
-        if (cur_rg >= 0) tma_flush(acc, lane, cur_rg, rows_t, part_tile, Wc, cw);
-        cur_rg = rg;
+  for (int T = 0; T < g.NT; ++T) {
+    if (!tma_consume_wait(p, bars, abort_flag, T, lane)) break;
+    const int rows_t = min(p.tile_rows, g.n - T * p.tile_rows);
+    const uint32_t stA = ring32 + (uint32_t)(T % p.stages) * p.stage_bytes;
+    const uint32_t stS = stA + p.sfa_off;
+    float* part_tile = part + (size_t)T * p.tile_rows * p.slots;
+    const int rgs = (rows_t + 3) >> 2;
+    int rg = rg0, sg = sg0, cur = -1;
+    uint32_t aoff[4], soff[4];
+    while (rg < rgs) {  // this warp's items it = cw, cw + Wc, ... as (row group, segment)
+      if (rg != cur) {
+        if (cur >= 0) tma_flush(acc, lane, 4 * cur, rows_t, part_tile, p.slots, cw);
+        cur = rg;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t r = (uint32_t)min(4 * rg + i, rows_t - 1);  // re-read the last row
+          aoff[i] = stA + r * K2u + 16u * lane;
+          soff[i] = stS + r * K16u + 2u * lane;
+        }
       }
-      const int64_t k = (int64_t)sg * kStep + 32 * lane;
-      if (k < K) {
+      if ((uint32_t)sg * 1024u + 32u * lane < Ku) {
+        const uint32_t so = (uint32_t)sg;
         uint4 av[4];
         uint16_t sv[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int r = min(4 * rg + i, rows_t - 1);  // rows past the tile re-read its last row
-          av[i] = *reinterpret_cast<const uint4*>(stA + (int64_t)r * K2 + (k >> 1));
-          sv[i] = *reinterpret_cast<const uint16_t*>(stS + (int64_t)r * K16 + (k >> 4));
+          av[i] = lds_v4(aoff[i] + so * 512u);
+          sv[i] = lds_u16(soff[i] + so * 64u);
         }
-        stream_compute<4>(bq, sbf, k, av, sv, acc);
+        const uint32_t bb = bq32 + so * 2048u + 64u * lane;
+        uint32_t bw[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 t = lds_v4(bb + bsw[j]);
+          bw[4 * j] = t.x;
+          bw[4 * j + 1] = t.y;
+          bw[4 * j + 2] = t.z;
+          bw[4 * j + 3] = t.w;
+        }
+        const float2 sb = lds_f2(sb32 + so * 256u + 8u * lane);
+        item_compute4(av, sv, bw, sb, acc);
+      }
+      sg += Wc;
+      while (sg >= nseg) {
+        sg -= nseg;
+        ++rg;
       }
     }
-    if (cur_rg >= 0) tma_flush(acc, lane, cur_rg, rows_t, part_tile, Wc, cw);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&bars[NS + s]));
+    if (cur >= 0) tma_flush(acc, lane, 4 * cur, rows_t, part_tile, p.slots, cw);
+    tma_release(p, bars, T, lane);
   }
-  (void)aborted;
+  named_barrier(1, (uint32_t)cthreads);
+  tma_epilogue(p, g, part, abort_flag);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Vector slice in registers (W_c divides the segment count, or the segment count divides W_c).
+// ------------------------------------------------------------------------------------------------
+template <int NSW>
+__global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kTmaMaxStages);
+  float* part = reinterpret_cast<float*>(smem + p.part_off);
+  uint8_t* ring = smem + p.ring_off;
+  const int64_t K = p.K, K2 = p.K >> 1, K16 = p.K >> 4;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  const TmaCta g = tma_setup(p, bars, abort_flag);
+  if (!p.early_weights) pdl_wait();
+  if (warp == g.Wc) {
+    if (lane == 0) tma_produce(p, g, bars, abort_flag, ring);
+    return;
+  }
+  if (p.early_weights) pdl_wait();
+
+  const int Wc = g.Wc, cthreads = 32 * Wc;
+  const int nseg = (int)((K + kStep - 1) / kStep);
+  const bool many = nseg >= Wc;                     // Wc | nseg: all row groups, NSW segments
+  const int rg_first = many ? 0 : warp / nseg;      // nseg | Wc: one segment, every rg_step-th
+  const int rg_step = many ? 1 : Wc / nseg;         //   row group
+  const int slot = many ? warp : warp % nseg;
+  int seg[NSW];
+  bool live[NSW];
+  uint32_t bw[NSW][16];
+  float2 sb[NSW];
+#pragma unroll
+  for (int j = 0; j < NSW; ++j) {
+    seg[j] = many ? warp + j * Wc : warp % nseg;
+    const int64_t k = (int64_t)seg[j] * kStep + 32 * lane;
+    live[j] = k < K;
+    const int64_t kk = live[j] ? k : 0;  // lanes past K read element 0 and never use it
+    const uint4 v = ld_ro_v4(p.b + g.l * K2 + (kk >> 1));
+    e2m1x8_to_f16x2x4(v.x, bw[j][0], bw[j][1], bw[j][2], bw[j][3]);
+    e2m1x8_to_f16x2x4(v.y, bw[j][4], bw[j][5], bw[j][6], bw[j][7]);
+    e2m1x8_to_f16x2x4(v.z, bw[j][8], bw[j][9], bw[j][10], bw[j][11]);
+    e2m1x8_to_f16x2x4(v.w, bw[j][12], bw[j][13], bw[j][14], bw[j][15]);
+    sb[j] = f16x2_to_f32x2(e4m3x2_to_f16x2(ld_ro_u16(p.sfb + g.l * K16 + (kk >> 4))));
+  }
+  for (int i = threadIdx.x; i < p.rows_cap * p.slots; i += cthreads) part[i] = 0.f;
   named_barrier(1, (uint32_t)cthreads);
 
-  const bool failed = *abort_flag != 0;
-  uint16_t* c_c = p.c + l * p.M + m0;
-  for (int t = ctid; t < n; t += cthreads) {
-    float v = 0.f;
-    for (int w = 0; w < Wc; ++w) v += part[t * Wc + w];
-    c_c[t] = failed ? (uint16_t)0x7E00 : f32_to_f16_bits((v * p.g_a) * p.g_b);
+  const uint32_t ring32 = smem_addr(ring);
+  const uint32_t K2u = (uint32_t)K2, K16u = (uint32_t)K16;
+  for (int T = 0; T < g.NT; ++T) {
+    if (!tma_consume_wait(p, bars, abort_flag, T, lane)) break;
+    const int rows_t = min(p.tile_rows, g.n - T * p.tile_rows);
+    const int rgs = (rows_t + 3) >> 2;
+    const uint32_t stA = ring32 + (uint32_t)(T % p.stages) * p.stage_bytes;
+    const uint32_t stS = stA + p.sfa_off;
+    float* part_tile = part + (size_t)T * p.tile_rows * p.slots;
+    for (int rg = rg_first; rg < rgs; rg += rg_step) {
+      uint32_t aoff[4], soff[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t r = (uint32_t)min(4 * rg + i, rows_t - 1);  // re-read the last row
+        aoff[i] = stA + r * K2u + 16u * lane;
+        soff[i] = stS + r * K16u + 2u * lane;
+      }
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < NSW; ++j) {
+        if (live[j]) {
+          const uint32_t so = (uint32_t)seg[j];
+          uint4 av[4];
+          uint16_t sv[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            av[i] = lds_v4(aoff[i] + so * 512u);
+            sv[i] = lds_u16(soff[i] + so * 64u);
+          }
+          item_compute4(av, sv, bw[j], sb[j], acc);
+        }
+      }
+      tma_flush(acc, lane, 4 * rg, rows_t, part_tile, p.slots, slot);
+    }
+    tma_release(p, bars, T, lane);
   }
+  named_barrier(1, (uint32_t)cthreads);
+  tma_epilogue(p, g, part, abort_flag);
 }
 
 }  // namespace nvfp4

@@ -51,6 +51,14 @@ cudaError_t prepare_stream_kernel(int max_smem) {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
 }
 
+// Shared memory up to the opt-in limit and the largest carveout, so two ~110 KiB CTAs fit per SM.
+cudaError_t prepare_tma_kernel(void (*k)(const nvfp4::TmaArgs), int max_smem) {
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              (int)cudaSharedmemCarveoutMaxShared);
+}
+
 void init_device(int dev) {
   DeviceInfo& d = g_dev[dev];
   cudaError_t e;
@@ -69,8 +77,9 @@ void init_device(int dev) {
   if ((e = prepare_stream_kernel<1>(d.max_smem_optin)) ||
       (e = prepare_stream_kernel<2>(d.max_smem_optin)) ||
       (e = prepare_stream_kernel<4>(d.max_smem_optin)) ||
-      (e = cudaFuncSetAttribute(nvfp4::gemv_tma_kernel,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin))) {
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_kernel, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2>, d.max_smem_optin))) {
     d.err = e;
     return;
   }
@@ -257,19 +266,20 @@ int plan_stream(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp
   return NVFP4_OK;
 }
 
-// Shared-memory layout of the TMA kernel: barriers and abort flag, the decoded vector, its fp32
-// block scales, the per-(row, warp) partial sums, then NS ring stages of TR rows (A rows, then sfa
-// rows).  Every region starts 16-byte aligned, ring stages 128-byte aligned.
+// Shared-memory layout of the TMA kernels: barriers and abort flag, the decoded vector and its fp32
+// block scales (shared-memory-vector variant only), the per-(row, slot) partial sums, then NS ring
+// stages of TR rows (A rows, then sfa rows).  Every region starts 16-byte aligned, ring stages
+// 128-byte aligned.
 struct TmaLayout {
   int64_t b_off, sb_off, part_off, ring_off, sfa_off, stage_bytes, total;
 };
 
-TmaLayout tma_layout(int64_t K, int64_t TR, int64_t NS, int64_t rows_cap, int64_t Wc) {
+TmaLayout tma_layout(bool rv, int64_t K, int64_t TR, int64_t NS, int64_t rows_cap, int64_t slots) {
   TmaLayout t;
-  t.b_off = 256;
-  t.sb_off = t.b_off + 2 * K;
-  t.part_off = align_up(t.sb_off + K / 4, 16);
-  t.ring_off = align_up(t.part_off + 4 * rows_cap * Wc, 128);
+  t.b_off = nvfp4::kTmaHeaderBytes;
+  t.sb_off = t.b_off + (rv ? 0 : 2 * K);
+  t.part_off = align_up(t.sb_off + (rv ? 0 : K / 4), 16);
+  t.ring_off = align_up(t.part_off + 4 * rows_cap * slots, 128);
   t.sfa_off = align_up(TR * (K / 2), 128);
   t.stage_bytes = align_up(t.sfa_off + TR * (K / 16), 128);
   t.total = t.ring_off + NS * t.stage_bytes;
@@ -277,58 +287,95 @@ TmaLayout tma_layout(int64_t K, int64_t TR, int64_t NS, int64_t rows_cap, int64_
 }
 
 constexpr int64_t kTmaStageTarget = 32768;  // A bytes per ring stage the planner aims for
+constexpr int64_t kTmaRingTarget = 81920;   // ring bytes per CTA the planner aims for
 
-int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan& f,
+// Consumer warps for the register-vector variant: they must divide the K-segment count (NSW = 1
+// or 2 segments per warp) or be a multiple of it.  Returns 0 if no such count fits.
+int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw) {
+  auto ok = [&](int64_t w) -> bool {
+    if (w < 1 || w > 16) return false;
+    if (nseg >= w) {
+      if (nseg % w || nseg / w > 2) return false;
+      *nsw = nseg / w;
+      return true;
+    }
+    if (w % nseg) return false;
+    *nsw = 1;
+    return true;
+  };
+  if (forced) return ok(forced) ? forced : 0;
+  // prefer 8 consumer warps (two CTAs per SM), then the nearest counts
+  for (int64_t w : {8, 7, 6, 9, 10, 12, 5, 4, 11, 13, 14, 15, 16, 3, 2, 1})
+    if (ok(w)) return w;
+  return 0;
+}
+
+int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan& f, bool rv,
              nvfp4_plan* pl) {
   if (K % 256 != 0)
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernel needs K %% 256 == 0 (K=%lld)",
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernels need K %% 256 == 0 (K=%lld)",
                 (long long)K);
   if (f.warps_per_cta > 16)
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernel: at most 16 consumer warps");
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernels: at most 16 consumer warps");
   if (f.rows_per_warp && f.rows_per_warp != 4)
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernel processes 4 rows per warp");
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernels process 4 rows per warp");
   if (f.tile_rows < 0 || f.tile_rows > 256 || f.stages < 0 || f.stages == 1 ||
       f.stages > nvfp4::kTmaMaxStages)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tile_rows must be 1..256, stages 2..%d",
                 nvfp4::kTmaMaxStages);
-  const int64_t Wc = f.warps_per_cta ? f.warps_per_cta : 8;
+  const int64_t nseg = ceil_div(K, nvfp4::kStep);
+  int64_t Wc = f.warps_per_cta ? f.warps_per_cta : 8, nsw = 1;
+  if (rv) {
+    Wc = rv_warps(nseg, f.warps_per_cta, &nsw);
+    if (!Wc)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                  "register-vector TMA kernel: no warp count fits %lld K segments",
+                  (long long)nseg);
+  }
+  const int64_t slots = rv ? std::min(Wc, nseg) : Wc;
+  const int64_t rg_step = (rv && nseg < Wc) ? Wc / nseg : 1;
   // two CTAs per SM if the ring fits, else one
   for (int occ = 2; occ >= 1; --occ) {
     const int64_t budget =
         std::min<int64_t>(d.max_smem_optin, d.max_smem_sm / occ - 1024);
-    const int64_t slots = (int64_t)d.sms * occ;
-    int64_t P = f.ctas_per_batch ? f.ctas_per_batch : std::max<int64_t>(1, slots / L);
+    const int64_t slots_sm = (int64_t)d.sms * occ;
+    int64_t P = f.ctas_per_batch ? f.ctas_per_batch : std::max<int64_t>(1, slots_sm / L);
     P = std::min(P, M);
     const int64_t rows_cap = ceil_div(M, P);
     int64_t TR = f.tile_rows;
     if (TR == 0) {
       TR = std::max<int64_t>(1, kTmaStageTarget / (K / 2));
-      if (TR >= 4) TR -= TR % 4;
+      const int64_t unit = 4 * rg_step;  // rows one round of the consumer warps covers
+      if (TR >= unit) TR -= TR % unit;
+      else if (TR >= 4) TR -= TR % 4;
       TR = std::min<int64_t>(TR, std::max<int64_t>(4, align_up(rows_cap, 4)));
     }
     int64_t NS = f.stages;
     if (NS == 0) {
-      for (int64_t ns = nvfp4::kTmaMaxStages; ns >= 2; --ns)
-        if (tma_layout(K, TR, ns, rows_cap, Wc).total <= budget) {
+      // at least two stages; more only while the ring stays near its target size
+      const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots).stage_bytes;
+      const int64_t want = std::max<int64_t>(2, kTmaRingTarget / stage);
+      for (int64_t ns = std::min<int64_t>(want, nvfp4::kTmaMaxStages); ns >= 2; --ns)
+        if (tma_layout(rv, K, TR, ns, rows_cap, slots).total <= budget) {
           NS = ns;
           break;
         }
       if (NS == 0) continue;
     }
-    if (tma_layout(K, TR, NS, rows_cap, Wc).total > d.max_smem_optin) continue;
+    if (tma_layout(rv, K, TR, NS, rows_cap, slots).total > d.max_smem_optin) continue;
     if (P * L > (int64_t(1) << 31) - 1)
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
-    pl->kernel = NVFP4_KERNEL_TMA;
+    pl->kernel = rv ? NVFP4_KERNEL_TMA_RV : NVFP4_KERNEL_TMA;
     pl->rows_per_warp = 4;
-    pl->k_split = 1;
+    pl->k_split = (int32_t)nsw;
     pl->ctas_per_batch = (int32_t)P;
     pl->warps_per_cta = (int32_t)Wc;
     pl->tile_rows = (int32_t)TR;
     pl->stages = (int32_t)NS;
     return NVFP4_OK;
   }
-  return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernel: K=%lld does not fit shared memory",
-              (long long)K);
+  return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+              "TMA kernel: K=%lld with this plan does not fit shared memory", (long long)K);
 }
 
 // Fills every field of *pl for (M, K, L); `forced` fields (non-zero) are honoured or rejected.
@@ -337,30 +384,43 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
   nvfp4_plan f;
   memset(&f, 0, sizeof f);
   if (forced) f = *forced;
-  if (f.reserved) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "plan.reserved must be zero");
+  if (f.flags & ~(NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_NO_PDL))
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown plan flags 0x%x", (unsigned)f.flags);
   if (f.warps_per_cta < 0 || f.rows_per_warp < 0 || f.k_split < 0 || f.ctas_per_batch < 0 ||
       f.tile_rows < 0 || f.stages < 0)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "negative plan field");
   memset(pl, 0, sizeof *pl);
+  int st = NVFP4_OK;
   switch (f.kernel) {
-    case NVFP4_KERNEL_SIMPLE: return plan_simple(d, M, L, f, pl);
-    case NVFP4_KERNEL_STREAM: return plan_stream(d, M, K, L, f, pl);
-    case NVFP4_KERNEL_TMA: return plan_tma(d, M, K, L, f, pl);
-    case NVFP4_KERNEL_AUTO: break;
+    case NVFP4_KERNEL_SIMPLE: st = plan_simple(d, M, L, f, pl); break;
+    case NVFP4_KERNEL_STREAM: st = plan_stream(d, M, K, L, f, pl); break;
+    case NVFP4_KERNEL_TMA: st = plan_tma(d, M, K, L, f, false, pl); break;
+    case NVFP4_KERNEL_TMA_RV: st = plan_tma(d, M, K, L, f, true, pl); break;
+    case NVFP4_KERNEL_AUTO: {
+      // the TMA ring (vector in registers if the warp mapping allows) when every CTA gets at least
+      // 8 rows, else the stream kernel, else the simple kernel
+      const int64_t rows_per_cta = (M * L) / std::max<int64_t>(1, (int64_t)d.sms * 2);
+      st = -1;
+      if (K % 256 == 0 && rows_per_cta >= 8) {
+        char saved[sizeof g_last_error];
+        memcpy(saved, g_last_error, sizeof saved);
+        for (bool rv : {true, false}) {
+          if (plan_tma(d, M, K, L, f, rv, pl) == NVFP4_OK) {
+            st = NVFP4_OK;
+            break;
+          }
+          memset(pl, 0, sizeof *pl);
+        }
+        memcpy(g_last_error, saved, sizeof saved);
+      }
+      if (st != NVFP4_OK)
+        st = stream_ok(d, K) ? plan_stream(d, M, K, L, f, pl) : plan_simple(d, M, L, f, pl);
+      break;
+    }
     default: return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown kernel %d", f.kernel);
   }
-  // automatic: the TMA ring when every CTA gets at least 8 rows, else the stream kernel, else the
-  // simple kernel
-  const int64_t rows_per_cta = (M * L) / std::max<int64_t>(1, (int64_t)d.sms * 2);
-  if (K % 256 == 0 && rows_per_cta >= 8) {
-    char saved[sizeof g_last_error];
-    memcpy(saved, g_last_error, sizeof saved);
-    if (plan_tma(d, M, K, L, f, pl) == NVFP4_OK) return NVFP4_OK;
-    memcpy(g_last_error, saved, sizeof saved);
-    memset(pl, 0, sizeof *pl);
-  }
-  if (stream_ok(d, K)) return plan_stream(d, M, K, L, f, pl);
-  return plan_simple(d, M, L, f, pl);
+  pl->flags = f.flags;
+  return st;
 }
 
 int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const uint8_t* sfa,
@@ -390,6 +450,7 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
       default: nvfp4::gemv_stream_kernel<4><<<grid, threads, smem, stream>>>(a); break;
     }
   } else {
+    const bool rv = pl.kernel == NVFP4_KERNEL_TMA_RV;
     nvfp4::TmaArgs a;
     a.A = A; a.sfa = sfa; a.b = b; a.sfb = sfb; a.c = c;
     a.g_a = g_a; a.g_b = g_b;
@@ -398,15 +459,31 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     a.tile_rows = pl.tile_rows;
     a.stages = pl.stages;
     a.rows_cap = (int32_t)ceil_div(M, pl.ctas_per_batch);
-    const TmaLayout t = tma_layout(K, pl.tile_rows, pl.stages, a.rows_cap, pl.warps_per_cta);
+    const int64_t nseg = ceil_div(K, nvfp4::kStep);
+    a.slots = (int32_t)(rv ? std::min<int64_t>(pl.warps_per_cta, nseg) : pl.warps_per_cta);
+    a.early_weights = (pl.flags & NVFP4_FLAG_EARLY_WEIGHTS) ? 1 : 0;
+    const TmaLayout t = tma_layout(rv, K, pl.tile_rows, pl.stages, a.rows_cap, a.slots);
     a.stage_bytes = (uint32_t)t.stage_bytes;
     a.sfa_off = (uint32_t)t.sfa_off;
     a.b_off = (uint32_t)t.b_off;
     a.sb_off = (uint32_t)t.sb_off;
     a.part_off = (uint32_t)t.part_off;
     a.ring_off = (uint32_t)t.ring_off;
-    const unsigned grid = (unsigned)(pl.ctas_per_batch * L);
-    nvfp4::gemv_tma_kernel<<<grid, threads + 32, (size_t)t.total, stream>>>(a);
+    void (*kern)(const nvfp4::TmaArgs) = nvfp4::gemv_tma_kernel;
+    if (rv) kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2> : nvfp4::gemv_tma_rv_kernel<1>;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(pl.ctas_per_batch * L));
+    cfg.blockDim = dim3((unsigned)(threads + 32));
+    cfg.dynamicSmemBytes = (size_t)t.total;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (pl.flags & NVFP4_FLAG_NO_PDL) ? 0 : 1;
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, a);
+    if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");

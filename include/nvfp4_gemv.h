@@ -35,7 +35,10 @@
  *
  * Execution: the call validates its arguments on the host, then enqueues its kernel(s) on `stream`
  * (a cudaStream_t; NULL = the legacy default stream) and returns without synchronizing.  Errors of
- * the launched kernels surface at the caller's next synchronization.  Calls are deterministic:
+ * the launched kernels surface at the caller's next synchronization.  TMA kernels are launched with
+ * programmatic dependent launch: they may be scheduled while the preceding kernel drains, but every
+ * thread waits for the preceding work before touching memory it may write (unless
+ * NVFP4_FLAG_EARLY_WEIGHTS says A and sfa are safe to read early), so stream order is kept.  Calls are deterministic:
  * the same inputs give the same output bits.  No call synchronizes, allocates or reads device
  * memory on the host, so calls can be captured in a CUDA graph once the device has been used by
  * one uncaptured call (which caches its properties).
@@ -76,9 +79,22 @@ typedef enum nvfp4_kernel {
   NVFP4_KERNEL_SIMPLE = 1,  /* one warp per output row, byte loads; any K % 16 == 0 */
   NVFP4_KERNEL_STREAM = 2,  /* 128-bit streaming loads, vector staged in shared memory, intra-CTA
                                split-K; needs K % 32 == 0 and K <= nvfp4_max_stream_k() */
-  NVFP4_KERNEL_TMA = 3      /* row tiles streamed into a shared-memory ring by bulk async copies
-                               (TMA) and mbarriers; needs K % 256 == 0 and at least 4 rows per CTA */
+  NVFP4_KERNEL_TMA = 3,     /* row tiles streamed into a shared-memory ring by bulk async copies
+                               (TMA) and mbarriers, vector in shared memory; needs K % 256 == 0 */
+  NVFP4_KERNEL_TMA_RV = 4   /* as TMA with each consumer warp's vector slice held in registers;
+                               needs K % 256 == 0 and the warp count to divide the number of
+                               1024-element K segments (or be a multiple of it) */
 } nvfp4_kernel;
+
+/* Plan flags. */
+enum {
+  /* The caller guarantees that no kernel that may still be running when this call's kernel starts
+     (the preceding work in the stream) writes A or sfa -- as for static weights.  The kernel then
+     starts streaming A and sfa before it waits for that work to finish. */
+  NVFP4_FLAG_EARLY_WEIGHTS = 1,
+  /* Launch without programmatic dependent launch (plain stream order). */
+  NVFP4_FLAG_NO_PDL = 2
+};
 
 /*
  * Launch plan.  Zero in any field means "planner's choice" for that field.  Used by
@@ -87,14 +103,15 @@ typedef enum nvfp4_kernel {
  */
 typedef struct nvfp4_plan {
   int32_t kernel;          /* nvfp4_kernel */
-  int32_t rows_per_warp;   /* STREAM: rows a warp processes together (1, 2 or 4); TMA: 4 */
-  int32_t k_split;         /* STREAM: K slices per row inside a CTA (1 .. ceil(K/1024)) */
+  int32_t rows_per_warp;   /* STREAM: rows a warp processes together (1, 2 or 4); TMA*: 4 */
+  int32_t k_split;         /* STREAM: K slices per row inside a CTA (1 .. ceil(K/1024));
+                              TMA_RV: 1024-element segments per warp (filled in by the planner) */
   int32_t ctas_per_batch;  /* all kernels: CTAs sharing one batch's rows (1 .. M) */
-  int32_t warps_per_cta;   /* SIMPLE: 1 .. 8; STREAM: 1 .. 16; TMA: consumer warps 1 .. 16 (one
+  int32_t warps_per_cta;   /* SIMPLE: 1 .. 8; STREAM: 1 .. 16; TMA*: consumer warps 1 .. 16 (one
                               producer warp is added) */
-  int32_t tile_rows;       /* TMA: rows per ring stage (1 .. 256) */
-  int32_t stages;          /* TMA: ring stages (2 .. 8) */
-  int32_t reserved;        /* must be zero */
+  int32_t tile_rows;       /* TMA*: rows per ring stage (1 .. 256) */
+  int32_t stages;          /* TMA*: ring stages (2 .. 8) */
+  int32_t flags;           /* NVFP4_FLAG_* (honoured by the automatic plan too) */
 } nvfp4_plan;
 
 /*

@@ -61,8 +61,9 @@ def stream_plan(R=0, S=0, P=0, W=0):
     return dict(kernel=2, rows_per_warp=R, k_split=S, ctas_per_batch=P, warps_per_cta=W)
 
 
-def tma_plan(TR=0, NS=0, P=0, W=0):
-    return dict(kernel=3, tile_rows=TR, stages=NS, ctas_per_batch=P, warps_per_cta=W)
+def tma_plan(TR=0, NS=0, P=0, W=0, rv=False, flags=0):
+    return dict(kernel=4 if rv else 3, tile_rows=TR, stages=NS, ctas_per_batch=P,
+                warps_per_cta=W, flags=flags)
 
 
 # ------------------------------------------------------------------ worked examples (exact)
@@ -109,7 +110,10 @@ PLANS = [None, SIMPLE, stream_plan(R=1), stream_plan(R=2), stream_plan(R=4),
          stream_plan(R=4, S=2), stream_plan(R=2, S=3, P=2), stream_plan(R=4, P=1, W=1),
          stream_plan(R=1, P=1, W=16), stream_plan(R=4, S=5, P=3, W=3)]
 TMA_PLANS = [tma_plan(), tma_plan(TR=1, NS=2), tma_plan(TR=4, NS=3, P=1), tma_plan(TR=8, W=1),
-             tma_plan(TR=12, NS=2, W=16), tma_plan(TR=5, NS=8, P=2, W=3)]
+             tma_plan(TR=12, NS=2, W=16), tma_plan(TR=5, NS=8, P=2, W=3),
+             tma_plan(rv=True), tma_plan(rv=True, TR=4, NS=2), tma_plan(rv=True, TR=3, NS=5, P=2),
+             tma_plan(rv=True, flags=1), tma_plan(flags=1), tma_plan(rv=True, flags=2),
+             tma_plan(rv=True, TR=16, NS=2, P=1)]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"{m}x{k}x{l}" for m, k, l in SHAPES])
@@ -139,7 +143,7 @@ def test_ragged_shapes_all_plans(pkg, shape):
         try:
             c = run(pkg, w, plan)
         except pkg.NVFP4Error as e:       # a forced ring too large for shared memory
-            assert e.status == 3 and "shared memory" in e.message, e
+            assert e.status == 3 and ("shared memory" in e.message or "warp count" in e.message), e
             continue
         check(w, c, f"{shape} {plan}")
 
@@ -157,18 +161,18 @@ def test_auto_plans_are_complete(pkg):
     for M, K, L in [(7168, 16384, 1), (4096, 7168, 8), (7168, 2048, 4), (3584, 6144, 16),
                     (128, 256, 1), (1, 16, 1)]:
         p = pkg.nvfp4_gemv_plan(M, K, L)
-        assert p.kernel in (1, 2, 3) and p.warps_per_cta >= 1 and p.ctas_per_batch >= 1
+        assert p.kernel in (1, 2, 3, 4) and p.warps_per_cta >= 1 and p.ctas_per_batch >= 1
         if K % 32 == 0:
-            assert p.kernel in (2, 3) and p.rows_per_warp in (1, 2, 4) and p.k_split >= 1
+            assert p.kernel in (2, 3, 4) and p.rows_per_warp in (1, 2, 4) and p.k_split >= 1
         if K % 256 == 0 and M * L >= 8 * 304:
-            assert p.kernel == 3 and p.stages >= 2 and p.tile_rows >= 1
+            assert p.kernel in (3, 4) and p.stages >= 2 and p.tile_rows >= 1
 
 
 def test_largest_stream_k_and_beyond(pkg):
     kmax = pkg.nvfp4_max_stream_k()
     assert kmax >= 65536
     w = workloads.random_workload(6, kmax, 1, seed=3)
-    assert pkg.nvfp4_gemv_plan(6, kmax, 1).kernel in (2, 3)
+    assert pkg.nvfp4_gemv_plan(6, kmax, 1).kernel in (2, 3, 4)
     check(w, run(pkg, w), f"K={kmax}")
     w2 = workloads.random_workload(3, kmax + 32, 1, seed=4)
     assert pkg.nvfp4_gemv_plan(3, kmax + 32, 1).kernel == 1
@@ -196,7 +200,8 @@ def test_c1_matches_committed_oracle_fixture(pkg, workload):
                   np.array([float(v) for v in fx["T"]]), "c1 fixture")
 
 
-@pytest.mark.parametrize("plan", [SIMPLE, stream_plan()], ids=["simple", "stream"])
+@pytest.mark.parametrize("plan", [SIMPLE, stream_plan(), tma_plan(), tma_plan(rv=True, flags=1)],
+                         ids=["simple", "stream", "tma", "tma-rv-early"])
 def test_other_kernels_agree_at_full_size(pkg, workload, plan):
     w = workload("c2")
     check(w, run(pkg, w, plan), f"c2 {plan}")
@@ -244,7 +249,7 @@ def test_batches_are_independent(pkg, mid):
 def test_plans_agree_within_tolerance(pkg, mid):
     for plan in PLANS + TMA_PLANS:
         check(mid, run(pkg, mid, plan), f"mid {plan}")
-    assert pkg.nvfp4_gemv_plan(mid.M, mid.K, mid.L).kernel in (2, 3)
+    assert pkg.nvfp4_gemv_plan(mid.M, mid.K, mid.L).kernel in (2, 3, 4)
 
 
 def test_zero_scale_block(pkg, mid):
@@ -290,7 +295,8 @@ def test_empty_problem_leaves_c_untouched(pkg):
 # ------------------------------------------------------------------ memory safety
 
 @pytest.mark.parametrize("plan", [None, SIMPLE, stream_plan(R=4, S=3), tma_plan(TR=4, NS=2),
-                                  tma_plan(TR=3, NS=5, P=2)])
+                                  tma_plan(TR=3, NS=5, P=2), tma_plan(rv=True, TR=3, NS=3),
+                                  tma_plan(rv=True, flags=1)])
 def test_guard_bands_and_poisoned_tails(pkg, plan):
     M, K, L = 77, 3328, 3
     w = workloads.random_workload(M, K, L, seed=5)
@@ -343,7 +349,7 @@ def test_error_statuses_with_real_buffers(pkg):
     assert status(c=t["A"][:16].view(torch.float16)) == 1   # c overlaps A
     with pytest.raises(pkg.NVFP4Error) as e:
         pkg.nvfp4_gemv_batched_ex(t["A"], t["sfa"], 1.0, t["b"], t["sfb"], 1.0, c, 8, 256, 1,
-                                  plan=pkg.Plan(kernel=2, reserved=1))
+                                  plan=pkg.Plan(kernel=2, flags=64))
     assert e.value.status == 3
     with pytest.raises(pkg.NVFP4Error) as e:
         pkg.nvfp4_gemv_batched_ex(t["A"], t["sfa"], 1.0, t["b"], t["sfb"], 1.0, c, 8, 256, 1,
