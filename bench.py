@@ -47,6 +47,9 @@ import workloads  # noqa: E402
 
 METRIC = "NVFP4 batched GEMV achieved HBM GB/s (% of GB300 peak) and us/call per MxKxL"
 GRAPH_CHUNK = 1000
+FLAG_EARLY_WEIGHTS = 1      # nvfp4_plan.flags: A and sfa are not written by preceding work
+KERNEL_NAMES = {1: "gemv_simple_kernel", 2: "gemv_stream_kernel", 3: "gemv_tma_kernel",
+                4: "gemv_tma_rv_kernel"}
 DEFAULT_PEAK_GBS = 6800.0   # only if MEASURED_PEAKS.json is absent
 
 
@@ -271,11 +274,15 @@ def run_ours(args):
     n_copies = max(2, -(-3 * l2 // bytes_call) + 1)
     sets = _device_inputs(w, n_copies, device)
     outs = [torch.empty((w.L, w.M), dtype=torch.float16, device=device) for _ in range(n_copies)]
-    plan = json.loads(args.plan) if args.plan else None
+    # Static weights: the same A and sfa are read by every call and written by none, so the calls
+    # declare it (NVFP4_FLAG_EARLY_WEIGHTS) and each kernel starts streaming A while the previous
+    # call drains.  The strict-order number (no flag) is reported beside it.
+    plan = json.loads(args.plan) if args.plan else {"flags": FLAG_EARLY_WEIGHTS}
     stream = torch.cuda.Stream(device)
     g_full, g_rem, chunk, rem = time_device(pkg, w, sets, outs, plan, args.steps, args.warmup,
                                             stream)
-    used_plan = pkg.nvfp4_gemv_plan(w.M, w.K, w.L).as_dict() if plan is None else plan
+    used_plan = pkg.nvfp4_gemv_plan(w.M, w.K, w.L).as_dict()
+    used_plan.update({k: v for k, v in plan.items() if v})
     uuid = str(torch.cuda.get_device_properties(device).uuid)
     gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
 
@@ -306,9 +313,33 @@ def run_ours(args):
     # correctness spot check of the timed launches' last output (NaN would mean an unwritten c)
     assert not torch.isnan(outs[(args.steps - 1) % n_copies]).any().item()
 
+    strict = None
+    if not args.plan and not args.no_strict:
+        steps_s = min(args.steps, 20000)
+        gs_full, gs_rem, chunk_s, _ = time_device(pkg, w, sets, outs, {"flags": 0}, steps_s,
+                                                  args.warmup, stream)
+        with torch.cuda.stream(stream):
+            barrier(dist)
+            torch.cuda.synchronize(device)
+            ev0.record(stream)
+            for _ in range(steps_s // chunk_s):
+                gs_full.replay()
+            if gs_rem is not None:
+                gs_rem.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize(device)
+            barrier(dist)
+        sec_s = ev0.elapsed_time(ev1) / 1e3
+        tot_s, slow_s = aggregate(dist, bytes_call * steps_s, sec_s)
+        strict = {"value": round(tot_s / slow_s / 1e9, 2), "unit": "GB/s",
+                  "us_per_call": round(sec_s / steps_s * 1e6, 3), "steps": steps_s,
+                  "flags": "none (every thread waits for the preceding call before any read)"}
+        del gs_full, gs_rem
+
     e2e = None
     if not args.no_e2e:
-        e2e = time_e2e(pkg, w, plan, device, stream, min(args.steps, args.e2e_steps), dist)
+        # host buffers are copied in before every call, so A is written by preceding work: no flag
+        e2e = time_e2e(pkg, w, None, device, stream, min(args.steps, args.e2e_steps), dist)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -342,8 +373,7 @@ def run_ours(args):
             },
             "roofline": {
                 "bound": "hbm",
-                "kernel": "gemv_stream_kernel" if used_plan.get("kernel", 2) == 2 else
-                          "gemv_simple_kernel",
+                "kernel": KERNEL_NAMES.get(used_plan.get("kernel"), "?"),
                 "achieved": round(achieved, 2),
                 "peak": peak,
                 "unit": "GB/s",
@@ -354,6 +384,8 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clocks,
         }
+        if strict is not None:
+            line["strict_order"] = strict
         if e2e is not None:
             line["e2e"] = e2e
         if cpu is not None:
@@ -476,6 +508,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--plan", default="", help="JSON plan fields forced on every call")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-strict", action="store_true",
+                    help="skip the second timing without the early-weights flag")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

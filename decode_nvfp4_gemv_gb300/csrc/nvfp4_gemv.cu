@@ -286,8 +286,11 @@ TmaLayout tma_layout(bool rv, int64_t K, int64_t TR, int64_t NS, int64_t rows_ca
   return t;
 }
 
-constexpr int64_t kTmaStageTarget = 32768;  // A bytes per ring stage the planner aims for
-constexpr int64_t kTmaRingTarget = 81920;   // ring bytes per CTA the planner aims for
+// Ring sizing, from sweeps on GB300 over the four large decode shapes: two stages of up to ~56 KiB
+// (A and sfa rows) per CTA and two CTAs per SM; deeper rings of smaller stages were slower, and a
+// ring that leaves room for only one CTA per SM was much slower.
+constexpr int64_t kTmaStageTarget = 57344;  // stage bytes (A + sfa rows) the planner aims for
+constexpr int64_t kTmaSmallStage = 24576;   // stages below this get up to 4 ring slots
 
 // Consumer warps for the register-vector variant: they must divide the K-segment count (NSW = 1
 // or 2 segments per warp) or be a multiple of it.  Returns 0 if no such count fits.
@@ -304,8 +307,9 @@ int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw) {
     return true;
   };
   if (forced) return ok(forced) ? forced : 0;
-  // prefer 8 consumer warps (two CTAs per SM), then the nearest counts
-  for (int64_t w : {8, 7, 6, 9, 10, 12, 5, 4, 11, 13, 14, 15, 16, 3, 2, 1})
+  // preference from sweeps: 12 warps when the mapping allows, else 8, then the nearest counts
+  // (16 would need <= 60 registers per thread for two CTAs per SM)
+  for (int64_t w : {12, 8, 7, 6, 14, 10, 9, 5, 4, 11, 13, 3, 2, 1, 15, 16})
     if (ok(w)) return w;
   return 0;
 }
@@ -342,20 +346,23 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
     int64_t P = f.ctas_per_batch ? f.ctas_per_batch : std::max<int64_t>(1, slots_sm / L);
     P = std::min(P, M);
     const int64_t rows_cap = ceil_div(M, P);
+    const int64_t row_bytes = K / 2 + K / 16;
+    const int64_t unit = 4 * rg_step;  // rows one round of the consumer warps covers
     int64_t TR = f.tile_rows;
     if (TR == 0) {
-      TR = std::max<int64_t>(1, kTmaStageTarget / (K / 2));
-      const int64_t unit = 4 * rg_step;  // rows one round of the consumer warps covers
+      TR = std::max<int64_t>(1, kTmaStageTarget / row_bytes);
       if (TR >= unit) TR -= TR % unit;
       else if (TR >= 4) TR -= TR % 4;
       TR = std::min<int64_t>(TR, std::max<int64_t>(4, align_up(rows_cap, 4)));
+      // shrink by whole rounds until two stages fit this occupancy's budget
+      while (TR > unit && tma_layout(rv, K, TR, 2, rows_cap, slots).total > budget) TR -= unit;
+      while (TR > 4 && tma_layout(rv, K, TR, 2, rows_cap, slots).total > budget) TR -= 4;
     }
     int64_t NS = f.stages;
     if (NS == 0) {
-      // at least two stages; more only while the ring stays near its target size
       const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots).stage_bytes;
-      const int64_t want = std::max<int64_t>(2, kTmaRingTarget / stage);
-      for (int64_t ns = std::min<int64_t>(want, nvfp4::kTmaMaxStages); ns >= 2; --ns)
+      const int64_t want = stage < kTmaSmallStage ? 4 : 2;
+      for (int64_t ns = want; ns >= 2; --ns)
         if (tma_layout(rv, K, TR, ns, rows_cap, slots).total <= budget) {
           NS = ns;
           break;
