@@ -354,6 +354,8 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       if (TR >= unit) TR -= TR % unit;
       else if (TR >= 4) TR -= TR % 4;
       TR = std::min<int64_t>(TR, std::max<int64_t>(4, align_up(rows_cap, 4)));
+      // at least ~4 tiles per CTA, so the last tile's compute is a small part of the CTA's time
+      TR = std::min<int64_t>(TR, std::max<int64_t>(unit, align_up(ceil_div(rows_cap, 4), unit)));
       // shrink by whole rounds until two stages fit this occupancy's budget
       while (TR > unit && tma_layout(rv, K, TR, 2, rows_cap, slots).total > budget) TR -= unit;
       while (TR > 4 && tma_layout(rv, K, TR, 2, rows_cap, slots).total > budget) TR -= 4;
