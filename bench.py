@@ -188,10 +188,11 @@ class ClockSampler:
 # ---------------------------------------------------------------------------- traffic record
 
 def kernel_source_digest() -> str:
+    """Digest of the device-code headers (the kernels); the host planner is not part of it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_nvfp4_gemv_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
+        if f.endswith(".cuh"):
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
