@@ -11,6 +11,9 @@ Contents, each written from the pages' definitions (citations in each module):
 * ``codecs``   E2M1 / E4M3FN decoders from their bit layouts, nibble unpacking, fp16 rounding.
 * ``nvfp4_gemv`` the GEMV definition in fp64 (``gemv``, ``gemv_rows``) and an independent exact
                integer formulation (``gemv_exact_units``).
+* ``quantize`` the NVFP4 activation quantizer with a fixed global scale (bridge.py,
+               ``quantize_activation_nvfp4``): the page's half-step-table rounding and
+               round-to-nearest-even, fp32 steps in the page's order.
 
 Pins (tests that tie the oracle to something other than itself):
 
@@ -24,6 +27,9 @@ Pins (tests that tie the oracle to something other than itself):
   batch independence);
 * ``gemv`` == ``gemv_exact_units`` bit for bit on all five workloads (sampled rows at full size);
 * planted mistakes (swapped nibbles, dropped scale, off-by-one block index, ...) each fail a pin.
+* quantizer: the printed half-step table; its E4M3 encoder against torch's cast; exact grid
+  round-trips; brute-force nearest rounding; error bounds; sign symmetry; bit-for-bit agreement
+  with the workload generator's independently written quantizer.
 
 No function in this package is "parity unpinned".
 """
