@@ -24,13 +24,15 @@ from .build import LIB_PATH
 
 __all__ = [
     "NVFP4Error", "Plan", "KERNEL_AUTO", "KERNEL_SIMPLE", "KERNEL_STREAM", "KERNEL_TMA",
-    "KERNEL_TMA_RV", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "library_path",
+    "KERNEL_TMA_RV", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "ROUND_HALF_STEP_TABLE",
+    "ROUND_NEAREST_EVEN", "nvfp4_quantize_activation", "nvfp4_gemv_batched_bf16", "library_path",
     "load_library", "nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_plan",
     "nvfp4_max_stream_k", "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version", "gemv",
 ]
 
 KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV = 0, 1, 2, 3, 4
 FLAG_EARLY_WEIGHTS, FLAG_NO_PDL = 1, 2
+ROUND_HALF_STEP_TABLE, ROUND_NEAREST_EVEN = 0, 1
 
 OK, ERR_INVALID_VALUE, ERR_MISALIGNED, ERR_UNSUPPORTED_SHAPE, ERR_ARCH, ERR_CUDA = range(6)
 
@@ -78,6 +80,11 @@ def load_library():
     lib.nvfp4_gemv_batched_ex.argtypes = [u8p, u8p, f32, u8p, u8p, f32, u16p, i64, i64, i64, vp,
                                           ctypes.POINTER(Plan)]
     lib.nvfp4_gemv_batched_ex.restype = ctypes.c_int
+    lib.nvfp4_quantize_activation.argtypes = [vp, f32, ctypes.c_int, vp, vp, i64, i64, vp]
+    lib.nvfp4_quantize_activation.restype = ctypes.c_int
+    lib.nvfp4_gemv_batched_bf16.argtypes = [u8p, u8p, f32, vp, f32, ctypes.c_int, vp, vp, u16p,
+                                            i64, i64, i64, vp, ctypes.POINTER(Plan)]
+    lib.nvfp4_gemv_batched_bf16.restype = ctypes.c_int
     lib.nvfp4_gemv_plan.argtypes = [i64, i64, i64, ctypes.POINTER(Plan)]
     lib.nvfp4_gemv_plan.restype = ctypes.c_int
     lib.nvfp4_max_stream_k.argtypes = []
@@ -232,3 +239,50 @@ def gemv(A, sfa, g_a, b, sfb, g_b, out=None, stream=None, plan=None):
         out = torch.empty((L, M), dtype=torch.float16, device=A.device)
     nvfp4_gemv_batched_ex(A, sfa, g_a, b, sfb, g_b, out, M, K, L, stream, plan)
     return out
+
+
+def _bf16_ptr(name, x, need_bytes):
+    """Address of a bf16 tensor (or a 16-bit integer tensor holding bf16 bits)."""
+    if x is None or isinstance(x, int):
+        return x
+    import torch
+
+    if x.dtype not in (torch.bfloat16, torch.uint16, torch.int16):
+        raise TypeError(f"{name} must be bfloat16 (or 16-bit integers holding bf16 bits)")
+    if not x.is_contiguous() or not x.is_cuda:
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if x.numel() * 2 < need_bytes:
+        raise ValueError(f"{name} holds {x.numel() * 2} bytes, (K, L) needs {need_bytes}")
+    return x.data_ptr()
+
+
+def nvfp4_quantize_activation(x, global_scale, b, sfb, K, L, rounding=ROUND_HALF_STEP_TABLE,
+                              stream=None):
+    """Quantize bf16 x [L][K] to packed E2M1 b [L][K/2] and E4M3 block scales sfb [L][K/16]."""
+    K, L = int(K), int(L)
+    ok = K > 0 and L > 0 and K % 16 == 0
+    with _on_device([x, b, sfb]):
+        px = _bf16_ptr("x", x, 2 * K * L if ok else 0)
+        pb = _ptr("b", b, K * L // 2 if ok else 0)
+        ps = _ptr("sfb", sfb, K * L // 16 if ok else 0)
+        h = _stream_handle(stream, [x, b, sfb])
+        _check(load_library().nvfp4_quantize_activation(px, ctypes.c_float(global_scale),
+                                                        int(rounding), pb, ps, K, L, h))
+
+
+def nvfp4_gemv_batched_bf16(A, sfa, g_a, x, x_global_scale, b_out, sfb_out, c, M, K, L,
+                            rounding=ROUND_HALF_STEP_TABLE, stream=None, plan=None):
+    """The GEMV with a bf16 vector x [L][K]: quantizes it (global scale x_global_scale, which is
+    g_b) into b_out / sfb_out and computes c from A and that vector."""
+    pl = None
+    if plan is not None:
+        pl = Plan(**plan) if isinstance(plan, dict) else plan
+    M, K, L = int(M), int(K), int(L)
+    ok = M > 0 and K > 0 and L > 0 and K % 16 == 0
+    with _on_device([A, sfa, x, b_out, sfb_out, c]):
+        (pA, pSA, pB, pSB, pC), ga, gb, M, K, L, h = _marshal(A, sfa, g_a, b_out, sfb_out,
+                                                              x_global_scale, c, M, K, L, stream)
+        px = _bf16_ptr("x", x, 2 * K * L if ok else 0)
+        _check(load_library().nvfp4_gemv_batched_bf16(
+            pA, pSA, ga, px, gb, int(rounding), pB, pSB, pC, M, K, L, h,
+            ctypes.byref(pl) if pl is not None else None))

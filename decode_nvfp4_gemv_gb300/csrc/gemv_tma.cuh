@@ -49,6 +49,7 @@
 
 #include "gemv_kernels.cuh"
 #include "nvfp4_device.cuh"
+#include "quantize.cuh"
 
 namespace nvfp4 {
 
@@ -73,6 +74,14 @@ struct TmaArgs {
   uint32_t stage_bytes;  // bytes per ring stage (A rows, then sfa rows at sfa_off)
   uint32_t sfa_off;      // offset of the sfa rows inside a stage (16-byte aligned)
   uint32_t b_off, sb_off, part_off, ring_off;  // shared-memory layout (bytes); b/sb unused by rv
+  // fused activation quantization (rv kernel with QX): the vector arrives as bf16 x [L][K] with
+  // global scale x_gs and is quantized in the staging step; the first CTA of each batch writes the
+  // packed bytes and scale bytes to b_out / sfb_out ([L][K/2], [L][K/16])
+  const uint16_t* x;
+  float x_gs;
+  int32_t rounding;
+  uint8_t* b_out;
+  uint8_t* sfb_out;
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -133,7 +142,7 @@ __device__ __forceinline__ void tma_flush(float (&acc)[4], int lane, int row0, i
 
 // Shared prologue: CTA geometry, barrier initialisation, dependent-launch trigger.
 struct TmaCta {
-  int64_t l, m0;
+  int64_t l, pi, m0;
   int n, NT, Wc;
 };
 
@@ -141,9 +150,9 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
                                             volatile int* abort_flag) {
   TmaCta g;
   g.l = blockIdx.x / p.P;
-  const int64_t pi = blockIdx.x - g.l * p.P;
-  g.m0 = (p.M * pi) / p.P;
-  const int64_t m1 = (p.M * (pi + 1)) / p.P;
+  g.pi = blockIdx.x - g.l * p.P;
+  g.m0 = (p.M * g.pi) / p.P;
+  const int64_t m1 = (p.M * (g.pi + 1)) / p.P;
   g.n = (int)(m1 - g.m0);
   g.NT = (g.n + p.tile_rows - 1) / p.tile_rows;
   g.Wc = (blockDim.x >> 5) - 1;
@@ -338,8 +347,10 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
 
 // ------------------------------------------------------------------------------------------------
 // Vector slice in registers (W_c divides the segment count, or the segment count divides W_c).
+// QX: the vector is bf16 and is quantized to NVFP4 here (see quantize.cuh); its bytes feed the same
+// decode as packed input would.
 // ------------------------------------------------------------------------------------------------
-template <int NSW>
+template <int NSW, bool QX>
 __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -373,12 +384,37 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
     const int64_t k = (int64_t)seg[j] * kStep + 32 * lane;
     live[j] = k < K;
     const int64_t kk = live[j] ? k : 0;  // lanes past K read element 0 and never use it
-    const uint4 v = ld_ro_v4(p.b + g.l * K2 + (kk >> 1));
+    uint4 v;
+    uint16_t s2;
+    if constexpr (QX) {
+      const uint16_t* xs = p.x + g.l * K + kk;
+      uint32_t xv[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 t = ld_ro_v4(xs + 8 * q);
+        xv[4 * q] = t.x;
+        xv[4 * q + 1] = t.y;
+        xv[4 * q + 2] = t.z;
+        xv[4 * q + 3] = t.w;
+      }
+      uint32_t pk[4];
+      quantize_blocks2(xv, p.x_gs, p.rounding, pk, s2);
+      v = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      // one writer per segment: the first CTA of the batch, and (when several warps share a
+      // segment) the warps of the first row-group round
+      if (live[j] && g.pi == 0 && rg_first == 0) {
+        *reinterpret_cast<uint4*>(p.b_out + g.l * K2 + (kk >> 1)) = v;
+        *reinterpret_cast<uint16_t*>(p.sfb_out + g.l * K16 + (kk >> 4)) = s2;
+      }
+    } else {
+      v = ld_ro_v4(p.b + g.l * K2 + (kk >> 1));
+      s2 = ld_ro_u16(p.sfb + g.l * K16 + (kk >> 4));
+    }
     e2m1x8_to_f16x2x4(v.x, bw[j][0], bw[j][1], bw[j][2], bw[j][3]);
     e2m1x8_to_f16x2x4(v.y, bw[j][4], bw[j][5], bw[j][6], bw[j][7]);
     e2m1x8_to_f16x2x4(v.z, bw[j][8], bw[j][9], bw[j][10], bw[j][11]);
     e2m1x8_to_f16x2x4(v.w, bw[j][12], bw[j][13], bw[j][14], bw[j][15]);
-    sb[j] = f16x2_to_f32x2(e4m3x2_to_f16x2(ld_ro_u16(p.sfb + g.l * K16 + (kk >> 4))));
+    sb[j] = f16x2_to_f32x2(e4m3x2_to_f16x2(s2));
   }
   for (int i = threadIdx.x; i < p.rows_cap * p.slots; i += cthreads) part[i] = 0.f;
   named_barrier(1, (uint32_t)cthreads);

@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "../../include/nvfp4_gemv.h"
@@ -78,8 +79,10 @@ void init_device(int dev) {
       (e = prepare_stream_kernel<2>(d.max_smem_optin)) ||
       (e = prepare_stream_kernel<4>(d.max_smem_optin)) ||
       (e = prepare_tma_kernel(nvfp4::gemv_tma_kernel, d.max_smem_optin)) ||
-      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1>, d.max_smem_optin)) ||
-      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2>, d.max_smem_optin))) {
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, false>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, true>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, true>, d.max_smem_optin))) {
     d.err = e;
     return;
   }
@@ -432,9 +435,18 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
   return st;
 }
 
+// The fused-quantization inputs of a TMA_RV launch (NULL: the vector arrives packed).
+struct FusedVector {
+  const uint16_t* x;
+  float gs;
+  int rounding;
+  uint8_t* b_out;
+  uint8_t* sfb_out;
+};
+
 int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const uint8_t* sfa,
            float g_a, const uint8_t* b, const uint8_t* sfb, float g_b, uint16_t* c, int64_t M,
-           int64_t K, int64_t L, cudaStream_t stream) {
+           int64_t K, int64_t L, cudaStream_t stream, const FusedVector* fx = nullptr) {
   (void)d;
   const int threads = pl.warps_per_cta * 32;
   if (pl.kernel == NVFP4_KERNEL_SIMPLE) {
@@ -479,7 +491,25 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     a.part_off = (uint32_t)t.part_off;
     a.ring_off = (uint32_t)t.ring_off;
     void (*kern)(const nvfp4::TmaArgs) = nvfp4::gemv_tma_kernel;
-    if (rv) kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2> : nvfp4::gemv_tma_rv_kernel<1>;
+    a.x = nullptr;
+    a.x_gs = 1.f;
+    a.rounding = 0;
+    a.b_out = a.sfb_out = nullptr;
+    if (fx) {
+      a.x = fx->x;
+      a.x_gs = fx->gs;
+      a.rounding = fx->rounding;
+      a.b_out = fx->b_out;
+      a.sfb_out = fx->sfb_out;
+    }
+    if (rv) {
+      if (fx)
+        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, true>
+                               : nvfp4::gemv_tma_rv_kernel<1, true>;
+      else
+        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false>
+                               : nvfp4::gemv_tma_rv_kernel<1, false>;
+    }
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = dim3((unsigned)(pl.ctas_per_batch * L));
@@ -515,6 +545,100 @@ int gemv_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
   nvfp4_plan pl;
   if ((st = make_plan(*d, M, K, L, forced, &pl)) != NVFP4_OK) return st;
   return launch(*d, pl, A, sfa, g_a, b, sfb, g_b, c, M, K, L, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------- activation quantization
+int check_quant_args(const uint16_t* x, float gs, const uint8_t* b, const uint8_t* sfb,
+                     int64_t K, int64_t L, int rounding, bool* noop) {
+  *noop = false;
+  if (K <= 0 || L < 0 || K % 16)
+    return fail(NVFP4_ERR_INVALID_VALUE, "need K > 0, K %% 16 == 0, L >= 0 (K=%lld L=%lld)",
+                (long long)K, (long long)L);
+  if (rounding != NVFP4_ROUND_HALF_STEP_TABLE && rounding != NVFP4_ROUND_NEAREST_EVEN)
+    return fail(NVFP4_ERR_INVALID_VALUE, "unknown rounding %d", rounding);
+  if (!(gs > 0.f) || !std::isfinite(gs))
+    return fail(NVFP4_ERR_INVALID_VALUE, "the global scale must be finite and > 0 (%g)", (double)gs);
+  const int64_t kMax = (int64_t(1) << 31) - 1;
+  if (L > kMax || K > kMax) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "L and K must be below 2^31");
+  if (L == 0) {
+    *noop = true;
+    return NVFP4_OK;
+  }
+  if (!x || !b || !sfb) return fail(NVFP4_ERR_INVALID_VALUE, "NULL pointer");
+  if (((uintptr_t)x | (uintptr_t)b | (uintptr_t)sfb) & 15u)
+    return fail(NVFP4_ERR_MISALIGNED, "x, b and sfb must be 16-byte aligned");
+  const int64_t nx = 2 * L * K, nb = L * K / 2, ns = L * K / 16;
+  if (overlaps(x, nx, b, nb) || overlaps(x, nx, sfb, ns) || overlaps(b, nb, sfb, ns))
+    return fail(NVFP4_ERR_INVALID_VALUE, "x, b and sfb must not overlap");
+  return NVFP4_OK;
+}
+
+int launch_quantize(const uint16_t* x, float gs, int rounding, uint8_t* b, uint8_t* sfb,
+                    int64_t K, int64_t L, cudaStream_t stream) {
+  const int64_t n_blocks = L * K / 16;
+  const int64_t grid = ceil_div(n_blocks, 256);
+  if (grid > (int64_t(1) << 31) - 1) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, nvfp4::quantize_activation_kernel, x, gs, rounding, b, sfb, n_blocks);
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return NVFP4_OK;
+}
+
+int quantize_impl(const uint16_t* x, float gs, int rounding, uint8_t* b, uint8_t* sfb, int64_t K,
+                  int64_t L, void* stream) {
+  g_last_error[0] = '\0';
+  bool noop = false;
+  int st = check_quant_args(x, gs, b, sfb, K, L, rounding, &noop);
+  if (st != NVFP4_OK || noop) return st;
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if ((st = check_access(*d, x, "x")) || (st = check_access(*d, b, "b")) ||
+      (st = check_access(*d, sfb, "sfb")))
+    return st;
+  return launch_quantize(x, gs, rounding, b, sfb, K, L, (cudaStream_t)stream);
+}
+
+int gemv_bf16_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16_t* x, float x_gs,
+                   int rounding, uint8_t* b_out, uint8_t* sfb_out, uint16_t* c, int64_t M,
+                   int64_t K, int64_t L, void* stream, const nvfp4_plan* forced) {
+  g_last_error[0] = '\0';
+  bool noop = false;
+  int st = check_args(A, sfa, b_out, sfb_out, c, M, K, L, &noop);
+  if (st != NVFP4_OK || noop) return st;
+  if ((st = check_quant_args(x, x_gs, b_out, sfb_out, K, L, rounding, &noop)) != NVFP4_OK)
+    return st;
+  const int64_t nx = 2 * L * K, nA = M * L * (K / 2), nSA = M * L * (K / 16), nC = 2 * M * L,
+                nb = L * K / 2, ns = L * K / 16;
+  if (overlaps(c, nC, x, nx) || overlaps(A, nA, b_out, nb) || overlaps(A, nA, sfb_out, ns) ||
+      overlaps(sfa, nSA, b_out, nb) || overlaps(sfa, nSA, sfb_out, ns))
+    return fail(NVFP4_ERR_INVALID_VALUE, "outputs overlap inputs");
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if ((st = check_access(*d, A, "A")) || (st = check_access(*d, sfa, "sfa")) ||
+      (st = check_access(*d, x, "x")) || (st = check_access(*d, b_out, "b_out")) ||
+      (st = check_access(*d, sfb_out, "sfb_out")) || (st = check_access(*d, c, "c")))
+    return st;
+  nvfp4_plan pl;
+  if ((st = make_plan(*d, M, K, L, forced, &pl)) != NVFP4_OK) return st;
+  if (pl.kernel == NVFP4_KERNEL_TMA_RV) {  // quantize inside the GEMV's vector staging
+    const FusedVector fx{x, x_gs, rounding, b_out, sfb_out};
+    return launch(*d, pl, A, sfa, g_a, nullptr, nullptr, x_gs, c, M, K, L, (cudaStream_t)stream,
+                  &fx);
+  }
+  // other kernels: quantize first (same stream, ordered), then the GEMV on the packed vector
+  if ((st = launch_quantize(x, x_gs, rounding, b_out, sfb_out, K, L, (cudaStream_t)stream)))
+    return st;
+  return launch(*d, pl, A, sfa, g_a, b_out, sfb_out, x_gs, c, M, K, L, (cudaStream_t)stream);
 }
 
 }  // namespace
@@ -563,6 +687,19 @@ const char* nvfp4_status_string(int status) {
 }
 
 const char* nvfp4_last_error(void) { return g_last_error; }
+
+int nvfp4_quantize_activation(const uint16_t* x, float global_scale, int rounding, uint8_t* b,
+                              uint8_t* sfb, int64_t K, int64_t L, void* stream) {
+  return quantize_impl(x, global_scale, rounding, b, sfb, K, L, stream);
+}
+
+int nvfp4_gemv_batched_bf16(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16_t* x,
+                            float x_global_scale, int rounding, uint8_t* b_out, uint8_t* sfb_out,
+                            uint16_t* c, int64_t M, int64_t K, int64_t L, void* stream,
+                            const nvfp4_plan* plan) {
+  return gemv_bf16_impl(A, sfa, g_a, x, x_global_scale, rounding, b_out, sfb_out, c, M, K, L,
+                        stream, plan);
+}
 
 int nvfp4_abi_version(void) { return NVFP4_ABI_VERSION; }
 

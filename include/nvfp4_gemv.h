@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define NVFP4_ABI_VERSION 1
+#define NVFP4_ABI_VERSION 2
 
 typedef enum nvfp4_status {
   NVFP4_OK = 0,
@@ -145,6 +145,39 @@ const char* nvfp4_status_string(int status);
 /* Detail text of the last non-OK status returned to the calling thread ("" if none).  The pointer
  * stays valid until that thread's next call into the library. */
 const char* nvfp4_last_error(void);
+
+/* ------------------------------------------------------------------------------------------
+ * Activation quantization (cutedsl/bridge.py, "Quantization", quantize_activation_nvfp4): bf16
+ * x [L][K] -> packed E2M1 b [L][K/2] and E4M3FN block scales sfb [L][K/16], with a fixed fp32
+ * global scale (x ~= global_scale * e4m3(sfb) * e2m1(b)).  Per 16-element block, in fp32 with IEEE
+ * round-to-nearest divisions: x_norm = x / global_scale; scale = e4m3(max(max|x_norm|, 1e-8) / 6)
+ * rounded to nearest even and saturating at 448; x_scaled = x_norm / max(scale, 1e-8); magnitude
+ * min(|x_scaled|, 6) rounded to E2M1 by `rounding`; the sign of x_scaled.  Each block is
+ * independent, so the step needs no reduction and no workspace.  x must hold finite values.
+ * ------------------------------------------------------------------------------------------ */
+enum {
+  NVFP4_ROUND_HALF_STEP_TABLE = 0,  /* the page's rule: table[rint(2 * magnitude)], table =
+                                       0,1,2,3,4,4,5,5,6,6,6,7,7 (codes) */
+  NVFP4_ROUND_NEAREST_EVEN = 1      /* nearest E2M1 value, ties to the even code */
+};
+
+/* Quantizes x (uint16 bf16 bits, [L][K], 16-byte aligned) into b and sfb (16-byte aligned, caller
+ * owned, not overlapping x).  K % 16 == 0; global_scale finite and > 0 (else INVALID_VALUE).
+ * L == 0 enqueues nothing.  Enqueued on `stream`; returns an nvfp4_status. */
+int nvfp4_quantize_activation(const uint16_t* x, float global_scale, int rounding, uint8_t* b,
+                              uint8_t* sfb, int64_t K, int64_t L, void* stream);
+
+/* The GEMV with a bf16 vector: quantizes x as nvfp4_quantize_activation does (global scale
+ * x_global_scale, which becomes g_b) and computes c as nvfp4_gemv_batched with that vector.  The
+ * quantized vector is also written to b_out [L][K/2] and sfb_out [L][K/16] (caller owned, 16-byte
+ * aligned, required: they hold the vector whichever kernel runs).  With the register-vector TMA
+ * kernel the quantization happens inside the GEMV (one launch); other plans run the quantizer
+ * first on the same stream.  plan: as for nvfp4_gemv_batched_ex (NULL = automatic).  Checks are
+ * those of both calls; M == 0 or L == 0 enqueues nothing (b_out and sfb_out are not written). */
+int nvfp4_gemv_batched_bf16(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16_t* x,
+                            float x_global_scale, int rounding, uint8_t* b_out, uint8_t* sfb_out,
+                            uint16_t* c, int64_t M, int64_t K, int64_t L, void* stream,
+                            const nvfp4_plan* plan);
 
 /* NVFP4_ABI_VERSION of the built library. */
 int nvfp4_abi_version(void);

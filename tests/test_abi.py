@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_status_strings(lib):
     import decode_nvfp4_gemv_gb300 as pkg
 
-    assert pkg.nvfp4_abi_version() == 1
+    assert pkg.nvfp4_abi_version() == 2
     assert pkg.nvfp4_status_string(0) == "ok"
     assert pkg.nvfp4_status_string(2) == "misaligned pointer"
     assert pkg.nvfp4_status_string(99) == "unknown status"
@@ -96,3 +96,46 @@ def test_plan_query_without_gpu(lib):
     with pytest.raises(pkg.NVFP4Error) as e:
         pkg.nvfp4_gemv_plan(128, 256, 1)
     assert e.value.status == 5          # CUDA error: no device
+
+
+def _quant(lib, x=0x1000, gs=1.0, rounding=0, b=0x100000, sfb=0x200000, K=256, L=1):
+    vp = ctypes.c_void_p
+    return lib.nvfp4_quantize_activation(vp(x), ctypes.c_float(gs), rounding, vp(b), vp(sfb),
+                                         K, L, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=24), 1), (dict(K=0), 1), (dict(L=-1), 1), (dict(rounding=2), 1),
+    (dict(gs=0.0), 1), (dict(gs=-1.0), 1), (dict(gs=float("inf")), 1), (dict(gs=float("nan")), 1),
+    (dict(x=0), 1), (dict(b=0), 1), (dict(sfb=0), 1),
+    (dict(x=0x1002), 2), (dict(b=0x100008), 2), (dict(sfb=0x200001), 2),
+    (dict(b=0x1100), 1),                        # b overlaps x (x holds 512 bytes)
+    (dict(K=1 << 33), 3),
+])
+def test_quantize_rejected_before_device_work(lib, kw, status):
+    assert _quant(lib, **kw) == status
+
+
+def test_quantize_empty_batch_is_a_noop(lib):
+    assert _quant(lib, L=0, x=0, b=0, sfb=0) == 0
+
+
+def _gemv_bf16(lib, A=0x1000, sfa=0x2000, x=0x3000, b=0x100000, sfb=0x200000, c=0x5000, gs=1.0,
+               M=4, K=256, L=1):
+    vp = ctypes.c_void_p
+    return lib.nvfp4_gemv_batched_bf16(vp(A), vp(sfa), ctypes.c_float(1.0), vp(x),
+                                       ctypes.c_float(gs), 0, vp(b), vp(sfb), vp(c), M, K, L,
+                                       None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(K=24), 1), (dict(gs=0.0), 1), (dict(x=0), 1), (dict(b=0), 1), (dict(x=0x3002), 2),
+    (dict(c=0x3000), 1),                        # c overlaps x
+    (dict(b=0x1000 + 64), 1),                   # b_out overlaps A
+])
+def test_gemv_bf16_rejected_before_device_work(lib, kw, status):
+    assert _gemv_bf16(lib, **kw) == status
+
+
+def test_gemv_bf16_empty_is_a_noop(lib):
+    assert _gemv_bf16(lib, M=0, A=0, sfa=0, c=0) == 0
