@@ -259,6 +259,72 @@ def time_device(pkg, w, sets, outs, plan, steps, warmup, stream):
     return g_full, g_rem, chunk, rem
 
 
+def time_bf16_vector(pkg, w, sets, outs, stream, steps, warmup, dist, early):
+    """The GEMV with a bf16 activation vector: fused (quantized inside the GEMV kernel when the plan
+    is the register-vector TMA kernel) and as two launches (quantizer, then the packed GEMV).
+    Algorithmic bytes add the bf16 vector read and the quantized vector written."""
+    import torch
+
+    n = len(sets)
+    dev = sets[0]["A"].device
+    x32 = workloads.normal_bf16(12, "x", w.K * w.L)
+    bits = (x32.view(np.uint32) >> 16).astype(np.uint16).view(np.int16).reshape(w.L, w.K)
+    gs = float(np.abs(x32).max() / (448.0 * 6.0))
+    xs = [torch.from_numpy(bits).to(dev) for _ in range(n)]
+    bo = [torch.empty(w.L * w.K // 2, dtype=torch.uint8, device=dev) for _ in range(n)]
+    so = [torch.empty(w.L * w.K // 16, dtype=torch.uint8, device=dev) for _ in range(n)]
+    plan = {"flags": FLAG_EARLY_WEIGHTS} if early else {"flags": 0}
+
+    def fused(i):
+        s = sets[i % n]
+        pkg.nvfp4_gemv_batched_bf16(s["A"], s["sfa"], w.g_a, xs[i % n], gs, bo[i % n], so[i % n],
+                                    outs[i % n], w.M, w.K, w.L, stream=stream, plan=plan)
+
+    def two(i):
+        s = sets[i % n]
+        pkg.nvfp4_quantize_activation(xs[i % n], gs, bo[i % n], so[i % n], w.K, w.L, stream=stream)
+        pkg.nvfp4_gemv_batched_ex(s["A"], s["sfa"], w.g_a, bo[i % n], so[i % n], gs, outs[i % n],
+                                  w.M, w.K, w.L, stream=stream, plan=plan)
+
+    out = {}
+    for name, fn in (("fused", fused), ("two_launches", two)):
+        with torch.cuda.stream(stream):
+            for i in range(max(warmup, 1)):
+                fn(i)
+        stream.synchronize()
+        chunk = min(GRAPH_CHUNK, steps)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(chunk):
+                fn(i)
+        reps = max(1, steps // chunk)
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            barrier(dist)
+            torch.cuda.synchronize(dev)
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize(dev)
+            barrier(dist)
+        sec = ev0.elapsed_time(ev1) / 1e3
+        calls = reps * chunk
+        out[name] = {"us_per_call": round(sec / calls * 1e6, 3), "calls": calls}
+        del g
+    # the packed vector is written instead of read (same bytes), plus the bf16 vector read
+    bytes_call = w.algorithmic_bytes + 2 * w.K * w.L
+    for v in out.values():
+        v["GB/s"] = round(bytes_call / (v["us_per_call"] * 1e-6) / 1e9, 2)
+    out["bytes_per_call"] = bytes_call
+    out["bytes"] = "A + sfa + bf16 x read + packed x and its scales written + c"
+    out["plan_kernel"] = KERNEL_NAMES.get(pkg.nvfp4_gemv_plan(w.M, w.K, w.L).kernel, "?")
+    out["flags"] = "early weights" if early else "none"
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -337,6 +403,11 @@ def run_ours(args):
                   "flags": "none (every thread waits for the preceding call before any read)"}
         del gs_full, gs_rem
 
+    bf16 = None
+    if not args.plan and not args.no_bf16:
+        bf16 = time_bf16_vector(pkg, w, sets, outs, stream, min(args.steps, 20000), args.warmup,
+                                dist, early=True)
+
     e2e = None
     if not args.no_e2e:
         # host buffers are copied in before every call, so A is written by preceding work: no flag
@@ -387,6 +458,8 @@ def run_ours(args):
         }
         if strict is not None:
             line["strict_order"] = strict
+        if bf16 is not None:
+            line["bf16_vector"] = bf16
         if e2e is not None:
             line["e2e"] = e2e
         if cpu is not None:
@@ -512,6 +585,8 @@ def main():
     ap.add_argument("--no-strict", action="store_true",
                     help="skip the second timing without the early-weights flag")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-bf16", action="store_true",
+                    help="skip the bf16-vector (activation quantization) timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
