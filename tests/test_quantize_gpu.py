@@ -55,7 +55,7 @@ def dev_bf16(x32):
 def special_blocks(gs):
     """16-element blocks of edge values for global scale gs (bf16-rounded)."""
     up, down = np.float32(1 + 2.0 ** -7), np.float32(1 - 2.0 ** -8)   # bf16 neighbours of 1
-    mids = np.concatenate([MIDS, -MIDS[:-1]]).astype(np.float32)
+    mids = np.concatenate([MIDS, -MIDS, [0.3]]).astype(np.float32)      # 15 values
     rows = [
         np.zeros(16, np.float32),
         np.array([0.0, -0.0] * 8, np.float32),
@@ -68,7 +68,7 @@ def special_blocks(gs):
         np.linspace(-1e5, 1e5, 16, dtype=np.float32) * gs,       # far beyond: clamped magnitudes
         np.full(16, 1e-12, np.float32),                          # scale 0 (floor 1e-8)
         np.array([1e-40, -1e-39, 3e-38, 0.0] * 4, np.float32),   # subnormal and tiny
-        np.concatenate([[6.0], GRID[1:], -GRID[1:]]) * gs * 2.0 ** -9,   # smallest scale
+        np.concatenate([[6.0, 0.0], GRID[1:], -GRID[1:]]) * gs * 2.0 ** -9,   # smallest scale
         np.concatenate([[6.0], mids]) * gs * 2.0 ** -7,
         np.linspace(0.01, 7.0, 16, dtype=np.float32) * gs,
     ]

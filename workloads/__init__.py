@@ -38,7 +38,7 @@ _M1 = 0xBF58476D1CE4E5B9
 _M2 = 0x94D049BB133111EB
 _U64 = np.uint64
 
-TENSOR_IDS = {"A": 0, "sfa": 1, "b": 2, "sfb": 3}
+TENSOR_IDS = {"A": 0, "sfa": 1, "b": 2, "sfb": 3, "x": 4}   # x: a bf16 activation vector
 
 
 _CHUNK = 1 << 20  # draws per chunk: temporaries stay cache-resident
