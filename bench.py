@@ -48,6 +48,7 @@ import workloads  # noqa: E402
 METRIC = "NVFP4 batched GEMV achieved HBM GB/s (% of GB300 peak) and us/call per MxKxL"
 GRAPH_CHUNK = 1000
 FLAG_EARLY_WEIGHTS = 1      # nvfp4_plan.flags: A and sfa are not written by preceding work
+FLAG_QUANTIZE_IN_GEMV = 4   # nvfp4_plan.flags: quantize the bf16 vector inside the GEMV kernel
 KERNEL_NAMES = {1: "gemv_simple_kernel", 2: "gemv_stream_kernel", 3: "gemv_tma_kernel",
                 4: "gemv_tma_rv_kernel"}
 DEFAULT_PEAK_GBS = 6800.0   # only if MEASURED_PEAKS.json is absent
@@ -259,10 +260,12 @@ def time_device(pkg, w, sets, outs, plan, steps, warmup, stream):
     return g_full, g_rem, chunk, rem
 
 
-def time_bf16_vector(pkg, w, sets, outs, stream, steps, warmup, dist, early):
-    """The GEMV with a bf16 activation vector: fused (quantized inside the GEMV kernel when the plan
-    is the register-vector TMA kernel) and as two launches (quantizer, then the packed GEMV).
-    Algorithmic bytes add the bf16 vector read and the quantized vector written."""
+def time_bf16_vector(pkg, w, sets, outs, stream, steps, warmup, dist):
+    """The GEMV with a bf16 activation vector through nvfp4_gemv_batched_bf16, in its two forms:
+    the quantizer launched ahead of the GEMV (the default) and the quantization inside the
+    register-vector TMA kernel (NVFP4_FLAG_QUANTIZE_IN_GEMV).  Static weights (early-weights flag),
+    as in the main timing.  Algorithmic bytes add the bf16 vector read; the packed vector is
+    written instead of read (the same bytes)."""
     import torch
 
     n = len(sets)
@@ -273,21 +276,18 @@ def time_bf16_vector(pkg, w, sets, outs, stream, steps, warmup, dist, early):
     xs = [torch.from_numpy(bits).to(dev) for _ in range(n)]
     bo = [torch.empty(w.L * w.K // 2, dtype=torch.uint8, device=dev) for _ in range(n)]
     so = [torch.empty(w.L * w.K // 16, dtype=torch.uint8, device=dev) for _ in range(n)]
-    plan = {"flags": FLAG_EARLY_WEIGHTS} if early else {"flags": 0}
-
-    def fused(i):
-        s = sets[i % n]
-        pkg.nvfp4_gemv_batched_bf16(s["A"], s["sfa"], w.g_a, xs[i % n], gs, bo[i % n], so[i % n],
-                                    outs[i % n], w.M, w.K, w.L, stream=stream, plan=plan)
-
-    def two(i):
-        s = sets[i % n]
-        pkg.nvfp4_quantize_activation(xs[i % n], gs, bo[i % n], so[i % n], w.K, w.L, stream=stream)
-        pkg.nvfp4_gemv_batched_ex(s["A"], s["sfa"], w.g_a, bo[i % n], so[i % n], gs, outs[i % n],
-                                  w.M, w.K, w.L, stream=stream, plan=plan)
-
+    bytes_call = w.algorithmic_bytes + 2 * w.K * w.L
     out = {}
-    for name, fn in (("fused", fused), ("two_launches", two)):
+    for name, flags in (("quantizer_then_gemv", FLAG_EARLY_WEIGHTS),
+                        ("in_gemv", FLAG_EARLY_WEIGHTS | FLAG_QUANTIZE_IN_GEMV)):
+        plan = {"flags": flags}
+
+        def fn(i):
+            s = sets[i % n]
+            pkg.nvfp4_gemv_batched_bf16(s["A"], s["sfa"], w.g_a, xs[i % n], gs, bo[i % n],
+                                        so[i % n], outs[i % n], w.M, w.K, w.L, stream=stream,
+                                        plan=plan)
+
         with torch.cuda.stream(stream):
             for i in range(max(warmup, 1)):
                 fn(i)
@@ -312,16 +312,14 @@ def time_bf16_vector(pkg, w, sets, outs, stream, steps, warmup, dist, early):
             barrier(dist)
         sec = ev0.elapsed_time(ev1) / 1e3
         calls = reps * chunk
-        out[name] = {"us_per_call": round(sec / calls * 1e6, 3), "calls": calls}
+        tot, slow = aggregate(dist, bytes_call * calls, sec)
+        out[name] = {"us_per_call": round(sec / calls * 1e6, 3), "calls": calls,
+                     "GB/s": round(tot / slow / 1e9, 2),
+                     "launches_per_call": 1 if flags & FLAG_QUANTIZE_IN_GEMV else 2}
         del g
-    # the packed vector is written instead of read (same bytes), plus the bf16 vector read
-    bytes_call = w.algorithmic_bytes + 2 * w.K * w.L
-    for v in out.values():
-        v["GB/s"] = round(bytes_call / (v["us_per_call"] * 1e-6) / 1e9, 2)
     out["bytes_per_call"] = bytes_call
     out["bytes"] = "A + sfa + bf16 x read + packed x and its scales written + c"
-    out["plan_kernel"] = KERNEL_NAMES.get(pkg.nvfp4_gemv_plan(w.M, w.K, w.L).kernel, "?")
-    out["flags"] = "early weights" if early else "none"
+    out["gemv_kernel"] = KERNEL_NAMES.get(pkg.nvfp4_gemv_plan(w.M, w.K, w.L).kernel, "?")
     return out
 
 
@@ -406,7 +404,7 @@ def run_ours(args):
     bf16 = None
     if not args.plan and not args.no_bf16:
         bf16 = time_bf16_vector(pkg, w, sets, outs, stream, min(args.steps, 20000), args.warmup,
-                                dist, early=True)
+                                dist)
 
     e2e = None
     if not args.no_e2e:

@@ -24,14 +24,15 @@ from .build import LIB_PATH
 
 __all__ = [
     "NVFP4Error", "Plan", "KERNEL_AUTO", "KERNEL_SIMPLE", "KERNEL_STREAM", "KERNEL_TMA",
-    "KERNEL_TMA_RV", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "ROUND_HALF_STEP_TABLE",
+    "KERNEL_TMA_RV", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "FLAG_QUANTIZE_IN_GEMV",
+    "ROUND_HALF_STEP_TABLE",
     "ROUND_NEAREST_EVEN", "nvfp4_quantize_activation", "nvfp4_gemv_batched_bf16", "library_path",
     "load_library", "nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_plan",
     "nvfp4_max_stream_k", "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version", "gemv",
 ]
 
 KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV = 0, 1, 2, 3, 4
-FLAG_EARLY_WEIGHTS, FLAG_NO_PDL = 1, 2
+FLAG_EARLY_WEIGHTS, FLAG_NO_PDL, FLAG_QUANTIZE_IN_GEMV = 1, 2, 4
 ROUND_HALF_STEP_TABLE, ROUND_NEAREST_EVEN = 0, 1
 
 OK, ERR_INVALID_VALUE, ERR_MISALIGNED, ERR_UNSUPPORTED_SHAPE, ERR_ARCH, ERR_CUDA = range(6)

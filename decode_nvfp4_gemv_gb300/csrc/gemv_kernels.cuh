@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(512) gemv_stream_kernel(const StreamArgs p) {
   // as four swizzled chunks; the block scales as fp32.
   const uint8_t* b_l = p.b + l * K2;
   for (int64_t i = tid; i < K2 / 16; i += blockDim.x) {
-    const uint4 v = ld_ro_v4(b_l + 16 * i);
+    const uint4 v = ld_l2_v4(b_l + 16 * i);
     uint4 w0, w1, w2, w3;
     e2m1x8_to_f16x2x4(v.x, w0.x, w0.y, w0.z, w0.w);
     e2m1x8_to_f16x2x4(v.y, w1.x, w1.y, w1.z, w1.w);
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(512) gemv_stream_kernel(const StreamArgs p) {
   }
   const uint8_t* sfb_l = p.sfb + l * K16;
   for (int64_t i = tid; i < K16 / 2; i += blockDim.x) {
-    const float2 sc = f16x2_to_f32x2(e4m3x2_to_f16x2(ld_ro_u16(sfb_l + 2 * i)));
+    const float2 sc = f16x2_to_f32x2(e4m3x2_to_f16x2(ld_l2_u16(sfb_l + 2 * i)));
     sbf[2 * i] = sc.x;
     sbf[2 * i + 1] = sc.y;
   }

@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
   const int Wc = g.Wc, cw = warp, cthreads = 32 * Wc;
   const uint8_t* b_l = p.b + g.l * K2;
   for (int64_t i = threadIdx.x; i < K2 / 16; i += cthreads) {
-    const uint4 v = ld_ro_v4(b_l + 16 * i);
+    const uint4 v = ld_l2_v4(b_l + 16 * i);
     uint4 w0, w1, w2, w3;
     e2m1x8_to_f16x2x4(v.x, w0.x, w0.y, w0.z, w0.w);
     e2m1x8_to_f16x2x4(v.y, w1.x, w1.y, w1.z, w1.w);
@@ -275,7 +275,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
   }
   const uint8_t* sfb_l = p.sfb + g.l * K16;
   for (int64_t i = threadIdx.x; i < K16 / 2; i += cthreads) {
-    const float2 sc = f16x2_to_f32x2(e4m3x2_to_f16x2(ld_ro_u16(sfb_l + 2 * i)));
+    const float2 sc = f16x2_to_f32x2(e4m3x2_to_f16x2(ld_l2_u16(sfb_l + 2 * i)));
     sbf[2 * i] = sc.x;
     sbf[2 * i + 1] = sc.y;
   }
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
       uint32_t xv[16];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint4 t = ld_ro_v4(xs + 8 * q);
+        const uint4 t = ld_l2_v4(xs + 8 * q);
         xv[4 * q] = t.x;
         xv[4 * q + 1] = t.y;
         xv[4 * q + 2] = t.z;
@@ -407,8 +407,8 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
         *reinterpret_cast<uint16_t*>(p.sfb_out + g.l * K16 + (kk >> 4)) = s2;
       }
     } else {
-      v = ld_ro_v4(p.b + g.l * K2 + (kk >> 1));
-      s2 = ld_ro_u16(p.sfb + g.l * K16 + (kk >> 4));
+      v = ld_l2_v4(p.b + g.l * K2 + (kk >> 1));
+      s2 = ld_l2_u16(p.sfb + g.l * K16 + (kk >> 4));
     }
     e2m1x8_to_f16x2x4(v.x, bw[j][0], bw[j][1], bw[j][2], bw[j][3]);
     e2m1x8_to_f16x2x4(v.y, bw[j][4], bw[j][5], bw[j][6], bw[j][7]);

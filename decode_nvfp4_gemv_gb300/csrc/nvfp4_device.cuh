@@ -89,17 +89,26 @@ __device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ uint4 ld_ro_v4(const void* p) {
+// Loads of the vector (and of the activation) read through L2 only (.cg), never from an L1 line:
+// under programmatic dependent launch the data may have been written by a grid that was still
+// running when this one started, after another grid on this SM had cached the old bytes.
+__device__ __forceinline__ uint4 ld_l2_v4(const void* p) {
   uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
 }
 
-__device__ __forceinline__ uint16_t ld_ro_u16(const void* p) {
+__device__ __forceinline__ uint32_t ld_l2_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ld_l2_u16(const void* p) {
   uint16_t v;
-  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(v) : "l"(p));
   return v;
 }
 

@@ -396,7 +396,7 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
   nvfp4_plan f;
   memset(&f, 0, sizeof f);
   if (forced) f = *forced;
-  if (f.flags & ~(NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_NO_PDL))
+  if (f.flags & ~(NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_NO_PDL | NVFP4_FLAG_QUANTIZE_IN_GEMV))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown plan flags 0x%x", (unsigned)f.flags);
   if (f.warps_per_cta < 0 || f.rows_per_warp < 0 || f.k_split < 0 || f.ctas_per_batch < 0 ||
       f.tile_rows < 0 || f.stages < 0)
@@ -542,6 +542,8 @@ int gemv_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
       (st = check_access(*d, b, "b")) || (st = check_access(*d, sfb, "sfb")) ||
       (st = check_access(*d, c, "c")))
     return st;
+  if (forced && (forced->flags & NVFP4_FLAG_QUANTIZE_IN_GEMV))
+    return fail(NVFP4_ERR_INVALID_VALUE, "NVFP4_FLAG_QUANTIZE_IN_GEMV needs a bf16 vector");
   nvfp4_plan pl;
   if ((st = make_plan(*d, M, K, L, forced, &pl)) != NVFP4_OK) return st;
   return launch(*d, pl, A, sfa, g_a, b, sfb, g_b, c, M, K, L, (cudaStream_t)stream);
@@ -574,9 +576,9 @@ int check_quant_args(const uint16_t* x, float gs, const uint8_t* b, const uint8_
 }
 
 int launch_quantize(const uint16_t* x, float gs, int rounding, uint8_t* b, uint8_t* sfb,
-                    int64_t K, int64_t L, cudaStream_t stream) {
-  const int64_t n_blocks = L * K / 16;
-  const int64_t grid = ceil_div(n_blocks, 256);
+                    int64_t K, int64_t L, cudaStream_t stream, bool pdl) {
+  const int64_t n_pairs = L * K / 2;
+  const int64_t grid = ceil_div(n_pairs, 256);
   if (grid > (int64_t(1) << 31) - 1) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
@@ -587,9 +589,9 @@ int launch_quantize(const uint16_t* x, float gs, int rounding, uint8_t* b, uint8
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, nvfp4::quantize_activation_kernel, x, gs, rounding, b, sfb, n_blocks);
+      cudaLaunchKernelEx(&cfg, nvfp4::quantize_activation_kernel, x, gs, rounding, b, sfb, n_pairs);
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return NVFP4_OK;
 }
@@ -605,7 +607,7 @@ int quantize_impl(const uint16_t* x, float gs, int rounding, uint8_t* b, uint8_t
   if ((st = check_access(*d, x, "x")) || (st = check_access(*d, b, "b")) ||
       (st = check_access(*d, sfb, "sfb")))
     return st;
-  return launch_quantize(x, gs, rounding, b, sfb, K, L, (cudaStream_t)stream);
+  return launch_quantize(x, gs, rounding, b, sfb, K, L, (cudaStream_t)stream, true);
 }
 
 int gemv_bf16_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16_t* x, float x_gs,
@@ -630,13 +632,19 @@ int gemv_bf16_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16
     return st;
   nvfp4_plan pl;
   if ((st = make_plan(*d, M, K, L, forced, &pl)) != NVFP4_OK) return st;
-  if (pl.kernel == NVFP4_KERNEL_TMA_RV) {  // quantize inside the GEMV's vector staging
+  if (pl.flags & NVFP4_FLAG_QUANTIZE_IN_GEMV) {  // quantize inside the GEMV's vector staging
+    if (pl.kernel != NVFP4_KERNEL_TMA_RV)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                  "quantizing inside the GEMV needs the register-vector TMA kernel (plan kernel %d)",
+                  pl.kernel);
     const FusedVector fx{x, x_gs, rounding, b_out, sfb_out};
     return launch(*d, pl, A, sfa, g_a, nullptr, nullptr, x_gs, c, M, K, L, (cudaStream_t)stream,
                   &fx);
   }
-  // other kernels: quantize first (same stream, ordered), then the GEMV on the packed vector
-  if ((st = launch_quantize(x, x_gs, rounding, b_out, sfb_out, K, L, (cudaStream_t)stream)))
+  // the quantizer first (it releases the GEMV at once: the GEMV can stream A meanwhile when the
+  // weights are static), then the GEMV on the packed vector, in stream order
+  if ((st = launch_quantize(x, x_gs, rounding, b_out, sfb_out, K, L, (cudaStream_t)stream,
+                            !(pl.flags & NVFP4_FLAG_NO_PDL))))
     return st;
   return launch(*d, pl, A, sfa, g_a, b_out, sfb_out, x_gs, c, M, K, L, (cudaStream_t)stream);
 }

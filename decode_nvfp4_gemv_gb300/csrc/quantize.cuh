@@ -77,47 +77,36 @@ __device__ __forceinline__ void quantize_blocks2(const uint32_t (&xv)[16], float
   }
 }
 
-// One 16-element block (the standalone kernel's unit; K need only be a multiple of 16).
-__device__ __forceinline__ void quantize_block1(const uint32_t (&xv)[8], float gs, int rounding,
-                                                uint32_t (&packed)[2], uint8_t& sf) {
-  float xn[16];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    xn[2 * i] = __fdiv_rn(bf16_bits_to_f32(xv[i] & 0xFFFFu), gs);
-    xn[2 * i + 1] = __fdiv_rn(bf16_bits_to_f32(xv[i] >> 16), gs);
-  }
-  float a = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(xn[i]));
-  a = fmaxf(a, 1e-8f);
-  const uint16_t s2 = f32x2_to_e4m3x2_sat(__fdiv_rn(a, 6.0f), 0.f);
-  sf = (uint8_t)(s2 & 0xFFu);
-  const float d = fmaxf(f16x2_to_f32x2(e4m3x2_to_f16x2(s2)).x, 1e-8f);
-  packed[0] = packed[1] = 0u;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float xs = __fdiv_rn(xn[i], d);
-    const uint32_t nib = e2m1_code(fminf(fabsf(xs), 6.0f), rounding) | (xs < 0.f ? 8u : 0u);
-    packed[i >> 3] |= nib << (4 * (i & 7));
-  }
-}
-
-// Standalone quantizer: thread t quantizes block t of the [L][K/16] blocks (x 16-byte aligned, K %
-// 16 == 0): 32 bytes of bf16 in, 8 packed bytes and 1 scale byte out (coalesced across the warp).
+// Standalone quantizer: eight consecutive threads own one 16-element block, two elements each
+// (x 16-byte aligned, K % 16 == 0, so a block never straddles two warps).  The block maximum is a
+// shuffle reduction over the eight lanes; each lane then writes the byte of its element pair and
+// the block's first lane the scale byte (a warp writes 32 consecutive packed bytes).  The kernel
+// releases its dependents at once (they only read what it writes after their own grid wait) and
+// waits for the preceding work before touching memory.
 __global__ void __launch_bounds__(256) quantize_activation_kernel(
     const uint16_t* __restrict__ x, float gs, int rounding, uint8_t* __restrict__ b,
-    uint8_t* __restrict__ sfb, int64_t n_blocks) {
+    uint8_t* __restrict__ sfb, int64_t n_pairs) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= n_blocks) return;
-  const uint4 v0 = ld_ro_v4(x + 16 * t);
-  const uint4 v1 = ld_ro_v4(x + 16 * t + 8);
-  const uint32_t xv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-  uint32_t packed[2];
-  uint8_t sf;
-  quantize_block1(xv, gs, rounding, packed, sf);
-  *reinterpret_cast<uint2*>(b + 8 * t) = make_uint2(packed[0], packed[1]);
-  sfb[t] = sf;
+  const bool valid = t < n_pairs;  // n_pairs % 8 == 0: a block's eight lanes agree
+  const uint32_t w = ld_l2_u32(x + 2 * (valid ? t : 0));
+  const float xn0 = __fdiv_rn(bf16_bits_to_f32(w & 0xFFFFu), gs);
+  const float xn1 = __fdiv_rn(bf16_bits_to_f32(w >> 16), gs);
+  float a = fmaxf(fabsf(xn0), fabsf(xn1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+  a = fmaxf(a, 1e-8f);
+  const uint16_t s2 = f32x2_to_e4m3x2_sat(__fdiv_rn(a, 6.0f), 0.f);
+  const float d = fmaxf(f16x2_to_f32x2(e4m3x2_to_f16x2(s2)).x, 1e-8f);
+  const float xs0 = __fdiv_rn(xn0, d), xs1 = __fdiv_rn(xn1, d);
+  const uint32_t nib0 = e2m1_code(fminf(fabsf(xs0), 6.0f), rounding) | (xs0 < 0.f ? 8u : 0u);
+  const uint32_t nib1 = e2m1_code(fminf(fabsf(xs1), 6.0f), rounding) | (xs1 < 0.f ? 8u : 0u);
+  if (valid) {
+    b[t] = (uint8_t)(nib0 | (nib1 << 4));
+    if ((t & 7) == 0) sfb[t >> 3] = (uint8_t)(s2 & 0xFFu);
+  }
 }
 
 }  // namespace nvfp4

@@ -93,7 +93,11 @@ enum {
      starts streaming A and sfa before it waits for that work to finish. */
   NVFP4_FLAG_EARLY_WEIGHTS = 1,
   /* Launch without programmatic dependent launch (plain stream order). */
-  NVFP4_FLAG_NO_PDL = 2
+  NVFP4_FLAG_NO_PDL = 2,
+  /* nvfp4_gemv_batched_bf16 only (INVALID_VALUE elsewhere): quantize the bf16 vector inside the
+     register-vector TMA kernel (one launch; every CTA quantizes the part of the vector it reads)
+     instead of a quantizer launch ahead of the GEMV.  The plan's kernel must be TMA_RV. */
+  NVFP4_FLAG_QUANTIZE_IN_GEMV = 4
 };
 
 /*
@@ -170,9 +174,11 @@ int nvfp4_quantize_activation(const uint16_t* x, float global_scale, int roundin
 /* The GEMV with a bf16 vector: quantizes x as nvfp4_quantize_activation does (global scale
  * x_global_scale, which becomes g_b) and computes c as nvfp4_gemv_batched with that vector.  The
  * quantized vector is also written to b_out [L][K/2] and sfb_out [L][K/16] (caller owned, 16-byte
- * aligned, required: they hold the vector whichever kernel runs).  With the register-vector TMA
- * kernel the quantization happens inside the GEMV (one launch); other plans run the quantizer
- * first on the same stream.  plan: as for nvfp4_gemv_batched_ex (NULL = automatic).  Checks are
+ * aligned, required: they hold the vector whichever kernel runs).  The quantizer runs first on
+ * the same stream and releases the GEMV at once (programmatic dependent launch; the GEMV waits for
+ * it before reading the vector), or, with NVFP4_FLAG_QUANTIZE_IN_GEMV, the register-vector TMA
+ * kernel quantizes inside its vector staging.  plan: as for nvfp4_gemv_batched_ex (NULL =
+ * automatic).  Checks are
  * those of both calls; M == 0 or L == 0 enqueues nothing (b_out and sfb_out are not written). */
 int nvfp4_gemv_batched_bf16(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16_t* x,
                             float x_global_scale, int rounding, uint8_t* b_out, uint8_t* sfb_out,

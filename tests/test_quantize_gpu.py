@@ -170,10 +170,13 @@ def tma_plan(TR=0, NS=0, P=0, W=0, rv=False, flags=0):
                 warps_per_cta=W, flags=flags)
 
 
-FUSED_PLANS = [None, tma_plan(rv=True), tma_plan(rv=True, flags=1), tma_plan(rv=True, flags=2),
-               tma_plan(rv=True, TR=3, NS=5, P=2), tma_plan(rv=True, TR=16, NS=2, P=1)]
-UNFUSED_PLANS = [dict(kernel=1), dict(kernel=2), dict(kernel=2, rows_per_warp=4, k_split=2),
-                 tma_plan(), tma_plan(TR=5, NS=3, P=2, W=3, flags=1)]
+IN_GEMV = 4        # NVFP4_FLAG_QUANTIZE_IN_GEMV
+FUSED_PLANS = [tma_plan(rv=True, flags=IN_GEMV), tma_plan(rv=True, flags=IN_GEMV | 1),
+               tma_plan(rv=True, flags=IN_GEMV | 2), tma_plan(rv=True, TR=3, NS=5, P=2, flags=IN_GEMV),
+               tma_plan(rv=True, TR=16, NS=2, P=1, flags=IN_GEMV | 1)]
+UNFUSED_PLANS = [None, dict(kernel=1), dict(kernel=2), dict(kernel=2, rows_per_warp=4, k_split=2),
+                 tma_plan(), tma_plan(TR=5, NS=3, P=2, W=3, flags=1), tma_plan(rv=True),
+                 tma_plan(rv=True, flags=1), tma_plan(rv=True, flags=2)]
 GSHAPES = [(129, 256, 3), (7, 1024, 2), (64, 2048, 1), (33, 3072, 2), (300, 5120, 1),
            (40, 16384, 2)]
 
@@ -225,13 +228,15 @@ def test_gemv_bf16_all_plans(pkg, shape, rounding, name):
         assert_bytes_equal(b, pr, what + " b_out")
         assert not np.isnan(c).any(), what
         assert_parity(c, ref, T, what)
-        c_packed = packed_gemv(pkg, A, sfa, w.g_a, pr, sr, gs, M, K, L, plan)
+        packed_plan = None if plan is None else dict(plan, flags=plan.get("flags", 0) & ~IN_GEMV)
+        c_packed = packed_gemv(pkg, A, sfa, w.g_a, pr, sr, gs, M, K, L, packed_plan)
         assert np.array_equal(c.view(np.uint16), c_packed.view(np.uint16)), what + " vs packed"
 
 
-def test_gemv_bf16_full_decode_shape(pkg, workload):
-    """The decode projection's shape (M=7168, K=16384, L=1) with the automatic plan: a fused
-    launch, b_out / sfb_out bit exact, c within tolerance, deterministic."""
+@pytest.mark.parametrize("flags", [1, 1 | IN_GEMV], ids=["quantizer-then-gemv", "in-gemv"])
+def test_gemv_bf16_full_decode_shape(pkg, workload, flags):
+    """The decode projection's shape (M=7168, K=16384, L=1) with the automatic plan and the flags
+    the bench times: b_out / sfb_out bit exact, c within tolerance, deterministic."""
     w = workload("c2")
     M, K, L = w.M, w.K, w.L
     assert pkg.nvfp4_gemv_plan(M, K, L).kernel == 4
@@ -240,12 +245,49 @@ def test_gemv_bf16_full_decode_shape(pkg, workload):
     pr, sr = Q.quantize_activation(x, gs, "lut")
     ref, T = oracle.gemv(w.A, w.sfa, w.g_a, pr, sr, gs, M, K, L)
     A, sfa = torch.from_numpy(w.A).cuda(), torch.from_numpy(w.sfa).cuda()
-    c, b, s = gemv_bf16(pkg, A, sfa, w.g_a, x, gs, 0, M, None)
+    c, b, s = gemv_bf16(pkg, A, sfa, w.g_a, x, gs, 0, M, {"flags": flags})
     assert_bytes_equal(s, sr, "c2 sfb_out")
     assert_bytes_equal(b, pr, "c2 b_out")
     assert_parity(c, ref, T, "c2 bf16 vector")
-    c2, _, _ = gemv_bf16(pkg, A, sfa, w.g_a, x, gs, 0, M, None)
+    c2, _, _ = gemv_bf16(pkg, A, sfa, w.g_a, x, gs, 0, M, {"flags": flags})
     assert np.array_equal(c.view(np.uint16), c2.view(np.uint16))
+
+
+def test_back_to_back_calls_reuse_the_vector_buffers(pkg):
+    """Decode reuses b_out / sfb_out every step: a chain of calls on one stream with new
+    activations each time (no host sync between them) must give each step's own result."""
+    M, K, L = 4096, 4096, 1
+    assert pkg.nvfp4_gemv_plan(M, K, L).kernel == 4
+    w = workloads.random_workload(M, K, L, seed=5, g_a=0.5, g_b=1.0)
+    A, sfa = torch.from_numpy(w.A).cuda(), torch.from_numpy(w.sfa).cuda()
+    gs = 0.01
+    xs = [activation(K, L, seed=100 + i, gs=gs, plant=False) for i in range(6)]
+    xd = [dev_bf16(x) for x in xs]
+    b = torch.empty(L * K // 2, dtype=torch.uint8, device="cuda")
+    s = torch.empty(L * K // 16, dtype=torch.uint8, device="cuda")
+    for flags in (1, 1 | IN_GEMV):
+        cs = [torch.empty((L, M), dtype=torch.float16, device="cuda") for _ in xs]
+        for x, c in zip(xd, cs):
+            pkg.nvfp4_gemv_batched_bf16(A, sfa, w.g_a, x, gs, b, s, c, M, K, L,
+                                        plan={"flags": flags})
+        torch.cuda.synchronize()
+        for i, (x, c) in enumerate(zip(xs, cs)):
+            pr, sr = Q.quantize_activation(x, gs, "lut")
+            ref, T = oracle.gemv(w.A, w.sfa, w.g_a, pr, sr, gs, M, K, L)
+            assert_parity(c.cpu().numpy(), ref, T, f"step {i} flags {flags}")
+
+
+def test_in_gemv_flag_rules(pkg):
+    M, K, L = 64, 1024, 1
+    w = workloads.random_workload(M, K, L, seed=6)
+    A, sfa = torch.from_numpy(w.A).cuda(), torch.from_numpy(w.sfa).cuda()
+    x = activation(K, L, seed=1, gs=1.0, plant=False)
+    with pytest.raises(pkg.NVFP4Error) as e:          # needs the register-vector kernel
+        gemv_bf16(pkg, A, sfa, 1.0, x, 1.0, 0, M, dict(kernel=2, flags=IN_GEMV))
+    assert e.value.status == 3
+    with pytest.raises(pkg.NVFP4Error) as e:          # meaningless for a packed vector
+        packed_gemv(pkg, A, sfa, 1.0, w.b, w.sfb, 1.0, M, K, L, {"flags": IN_GEMV})
+    assert e.value.status == 1
 
 
 def test_gemv_bf16_empty_and_statuses(pkg):
