@@ -323,6 +323,75 @@ def time_bf16_vector(pkg, w, sets, outs, stream, steps, warmup, dist):
     return out
 
 
+def time_grouped(pkg, device, stream, steps, warmup, dist, name="g1", n_routes=4):
+    """The grouped (mixture-of-experts) decode GEMV on `name`: the experts' weights stay resident
+    and every call takes the next of `n_routes` routings (its own offsets and token vectors), as
+    decode steps do.  Algorithmic bytes count each expert that owns a token once per call."""
+    import torch
+
+    w0 = workloads.make_grouped(name)
+    ws = [w0] + [workloads.make_grouped(name, route=r, with_weights=w0) for r in range(1, n_routes)]
+    A = torch.from_numpy(w0.A).to(device)
+    sfa = torch.from_numpy(w0.sfa).to(device)
+    g_a = torch.from_numpy(np.ascontiguousarray(w0.g_a, np.float32)).to(device)
+    g_b = torch.from_numpy(np.ascontiguousarray(w0.g_b, np.float32)).to(device)
+    per = []
+    for w in ws:
+        offs = np.cumsum(np.bincount(w.expert_of, minlength=w.E)).astype(np.int32)
+        per.append(dict(b=torch.from_numpy(w.b).to(device), sfb=torch.from_numpy(w.sfb).to(device),
+                        offs=torch.from_numpy(offs).to(device),
+                        c=torch.empty((w.T, w.M), dtype=torch.float16, device=device)))
+    M, K, E, T = w0.M, w0.K, w0.E, w0.T
+
+    def call(i):
+        r = per[i % n_routes]
+        pkg.nvfp4_gemv_grouped(A, sfa, g_a, r["b"], r["sfb"], g_b, r["c"], M, K, E, T,
+                               expert_offsets=r["offs"], stream=stream)
+
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 1)):
+            call(i)
+    stream.synchronize()
+    chunk = min(GRAPH_CHUNK, steps)
+    chunk -= chunk % n_routes
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(chunk):
+            call(i)
+    reps = max(1, steps // chunk)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        barrier(dist)
+        torch.cuda.synchronize(device)
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(dist)
+    sec = ev0.elapsed_time(ev1) / 1e3
+    calls = reps * chunk
+    bytes_call = sum(w.algorithmic_bytes for w in ws) / n_routes
+    tot, slow = aggregate(dist, bytes_call * calls, sec)
+    peak, peak_kind = measured_peak_gbs()
+    gbs = tot / slow / 1e9
+    del g
+    return {
+        "workload": f"grouped decode GEMV {name}: E={E} experts of M={M} K={K}, "
+                    f"{workloads.GROUPED[name]['tokens']} tokens x top-"
+                    f"{workloads.GROUPED[name]['top_k']} = {T} rows, {n_routes} routings rotated",
+        "us_per_call": round(sec / calls * 1e6, 3), "calls": calls, "GB/s": round(gbs, 2),
+        "frac": round(gbs / peak, 4), "peak_kind": f"{peak_kind} HBM copy bandwidth (burst)",
+        "active_experts": [w.active_experts for w in ws],
+        "bytes_per_call": int(bytes_call),
+        "kernel": KERNEL_NAMES.get(pkg.nvfp4_gemv_plan(M, K, T).kernel, "?"),
+        "weights_resident_mb": round((w0.A.nbytes + w0.sfa.nbytes) / 1e6, 1),
+    }
+
+
 def run_ours(args):
     import torch
 
@@ -406,6 +475,10 @@ def run_ours(args):
         bf16 = time_bf16_vector(pkg, w, sets, outs, stream, min(args.steps, 20000), args.warmup,
                                 dist)
 
+    grouped = None
+    if not args.plan and not args.no_grouped:
+        grouped = time_grouped(pkg, device, stream, min(args.steps, 20000), args.warmup, dist)
+
     e2e = None
     if not args.no_e2e:
         # host buffers are copied in before every call, so A is written by preceding work: no flag
@@ -458,6 +531,8 @@ def run_ours(args):
             line["strict_order"] = strict
         if bf16 is not None:
             line["bf16_vector"] = bf16
+        if grouped is not None:
+            line["grouped"] = grouped
         if e2e is not None:
             line["e2e"] = e2e
         if cpu is not None:
@@ -585,6 +660,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-bf16", action="store_true",
                     help="skip the bf16-vector (activation quantization) timing")
+    ap.add_argument("--no-grouped", action="store_true",
+                    help="skip the grouped (mixture-of-experts) timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)

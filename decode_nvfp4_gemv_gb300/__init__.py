@@ -26,7 +26,8 @@ __all__ = [
     "NVFP4Error", "Plan", "KERNEL_AUTO", "KERNEL_SIMPLE", "KERNEL_STREAM", "KERNEL_TMA",
     "KERNEL_TMA_RV", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "FLAG_QUANTIZE_IN_GEMV",
     "ROUND_HALF_STEP_TABLE",
-    "ROUND_NEAREST_EVEN", "nvfp4_quantize_activation", "nvfp4_gemv_batched_bf16", "library_path",
+    "ROUND_NEAREST_EVEN", "nvfp4_quantize_activation", "nvfp4_gemv_batched_bf16", "OUT_F16",
+    "OUT_BF16", "nvfp4_gemv_grouped", "library_path",
     "load_library", "nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_plan",
     "nvfp4_max_stream_k", "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version", "gemv",
 ]
@@ -34,6 +35,7 @@ __all__ = [
 KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV = 0, 1, 2, 3, 4
 FLAG_EARLY_WEIGHTS, FLAG_NO_PDL, FLAG_QUANTIZE_IN_GEMV = 1, 2, 4
 ROUND_HALF_STEP_TABLE, ROUND_NEAREST_EVEN = 0, 1
+OUT_F16, OUT_BF16 = 0, 1
 
 OK, ERR_INVALID_VALUE, ERR_MISALIGNED, ERR_UNSUPPORTED_SHAPE, ERR_ARCH, ERR_CUDA = range(6)
 
@@ -86,6 +88,9 @@ def load_library():
     lib.nvfp4_gemv_batched_bf16.argtypes = [u8p, u8p, f32, vp, f32, ctypes.c_int, vp, vp, u16p,
                                             i64, i64, i64, vp, ctypes.POINTER(Plan)]
     lib.nvfp4_gemv_batched_bf16.restype = ctypes.c_int
+    lib.nvfp4_gemv_grouped.argtypes = [u8p, u8p, vp, u8p, u8p, vp, vp, vp, u16p, ctypes.c_int,
+                                       i64, i64, i64, i64, vp, ctypes.POINTER(Plan)]
+    lib.nvfp4_gemv_grouped.restype = ctypes.c_int
     lib.nvfp4_gemv_plan.argtypes = [i64, i64, i64, ctypes.POINTER(Plan)]
     lib.nvfp4_gemv_plan.restype = ctypes.c_int
     lib.nvfp4_max_stream_k.argtypes = []
@@ -286,4 +291,49 @@ def nvfp4_gemv_batched_bf16(A, sfa, g_a, x, x_global_scale, b_out, sfb_out, c, M
         px = _bf16_ptr("x", x, 2 * K * L if ok else 0)
         _check(load_library().nvfp4_gemv_batched_bf16(
             pA, pSA, ga, px, gb, int(rounding), pB, pSB, pC, M, K, L, h,
+            ctypes.byref(pl) if pl is not None else None))
+
+
+def _typed_ptr(name, x, dtypes, need_bytes):
+    """Device address of a contiguous CUDA tensor of one of `dtypes` (names), or a raw integer."""
+    if x is None or isinstance(x, int):
+        return x
+    import torch
+
+    if not isinstance(x, torch.Tensor) or str(x.dtype).replace("torch.", "") not in dtypes:
+        raise TypeError(f"{name} must be a tensor of {' or '.join(dtypes)}")
+    if not x.is_contiguous() or not x.is_cuda:
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if x.numel() * x.element_size() < need_bytes:
+        raise ValueError(f"{name} holds {x.numel() * x.element_size()} bytes, needs {need_bytes}")
+    return x.data_ptr()
+
+
+def nvfp4_gemv_grouped(A, sfa, g_a, b, sfb, g_b, c, M, K, E, T, expert_offsets=None,
+                       expert_of_token=None, out_dtype=OUT_F16, stream=None, plan=None):
+    """Grouped (mixture-of-experts) decode GEMV: token t uses expert e(t)'s matrix A[e] and the
+    global scales g_a[e], g_b[e] (fp32 device arrays); e(t) from inclusive cumulative
+    ``expert_offsets`` [E] or from ``expert_of_token`` [T] (int32 device arrays, exactly one).
+    c [T][M] is fp16 or bfloat16 (``out_dtype``); tokens without an expert get zeros."""
+    pl = None
+    if plan is not None:
+        pl = Plan(**plan) if isinstance(plan, dict) else plan
+    M, K, E, T = int(M), int(K), int(E), int(T)
+    ok = M > 0 and K > 0 and T > 0 and E > 0 and K % 16 == 0
+    tensors = [A, sfa, g_a, b, sfb, g_b, c, expert_offsets, expert_of_token]
+    with _on_device([t for t in tensors if t is not None]):
+        pA = _ptr("A", A, E * M * K // 2 if ok else 0)
+        pSA = _ptr("sfa", sfa, E * M * K // 16 if ok else 0)
+        pB = _ptr("b", b, T * K // 2 if ok else 0)
+        pSB = _ptr("sfb", sfb, T * K // 16 if ok else 0)
+        pga = _typed_ptr("g_a", g_a, ("float32",), 4 * E if ok else 0)
+        pgb = _typed_ptr("g_b", g_b, ("float32",), 4 * E if ok else 0)
+        po = _typed_ptr("expert_offsets", expert_offsets, ("int32",), 4 * E if ok else 0)
+        pm = _typed_ptr("expert_of_token", expert_of_token, ("int32",), 4 * T if ok else 0)
+        out_types = ("bfloat16", "int16", "uint16") if out_dtype == OUT_BF16 else \
+            ("float16", "int16", "uint16")
+        pC = _typed_ptr("c", c, out_types, 2 * M * T if ok else 0)
+        h = _stream_handle(stream, [t for t in tensors if t is not None])
+        _check(load_library().nvfp4_gemv_grouped(
+            pA, pSA, pga, pB, pSB, pgb, po, pm, pC, int(out_dtype), M, K, E, T, h,
             ctypes.byref(pl) if pl is not None else None))

@@ -20,6 +20,36 @@ namespace nvfp4 {
 constexpr unsigned kFullMask = 0xffffffffu;
 
 // ------------------------------------------------------------------------------------------------
+// Grouped (mixture-of-experts) form.  A and sfa hold E expert matrices ([E][M][K/2], [E][M][K/16]);
+// batch l is a token (b[l], c[l]) that uses expert e(l) and the global scales g_a[e], g_b[e]
+// (cutedsl/bridge.py, "Kernel Launch": per-expert global scales; "compute_expert_offsets": tokens
+// sorted by expert, offsets[e] = tokens of experts 0..e).  e(l) comes from the inclusive offsets
+// (e(l) = the first e with l < offsets[e], which for non-decreasing offsets is the number of
+// offsets <= l) or from a per-token expert index.  A token with no expert (past the last offset,
+// or an index outside [0, E)) gets an output row of zeros.  E == 0 is the plain batched form.
+// ------------------------------------------------------------------------------------------------
+struct Groups {
+  const int32_t* offsets;    // [E], or null
+  const int32_t* expert_of;  // [L], or null
+  const float* g_a;          // [E]
+  const float* g_b;          // [E]
+  int32_t E;
+};
+
+// Expert of batch l, or -1; called by all 32 lanes of a warp (the counts are a warp reduction).
+// Every index read is in range whatever the offsets hold.
+__device__ __forceinline__ int group_of_batch(const Groups& G, int64_t l, int lane) {
+  if (G.expert_of) {
+    const int e = __ldcg(G.expert_of + l);
+    return (e >= 0 && e < G.E) ? e : -1;
+  }
+  int cnt = 0;
+  for (int e = lane; e < G.E; e += 32) cnt += (int64_t)__ldcg(G.offsets + e) <= l ? 1 : 0;
+  const int e = __reduce_add_sync(0xffffffffu, cnt);
+  return e < G.E ? e : -1;
+}
+
+// ------------------------------------------------------------------------------------------------
 // SIMPLE: one warp per output row (l, m), lane j handles whole 16-element blocks j, j+32, ...
 // All arithmetic in fp32, byte loads, so any K % 16 == 0 and any byte alignment works.  Used when
 // the streaming kernel's shape or alignment conditions do not hold, and as a cross-check.
@@ -27,7 +57,7 @@ constexpr unsigned kFullMask = 0xffffffffu;
 __global__ void __launch_bounds__(256) gemv_simple_kernel(
     const uint8_t* __restrict__ A, const uint8_t* __restrict__ sfa,
     const uint8_t* __restrict__ b, const uint8_t* __restrict__ sfb, float g_a, float g_b,
-    uint16_t* __restrict__ c, int64_t M, int64_t K, int64_t L) {
+    uint16_t* __restrict__ c, int64_t M, int64_t K, int64_t L, const Groups G, int out_bf16) {
   const int lane = threadIdx.x & 31;
   const int64_t warps_per_cta = blockDim.x >> 5;
   const int64_t n_rows = M * L;
@@ -35,8 +65,20 @@ __global__ void __launch_bounds__(256) gemv_simple_kernel(
   for (int64_t row = blockIdx.x * warps_per_cta + (threadIdx.x >> 5); row < n_rows;
        row += (int64_t)gridDim.x * warps_per_cta) {
     const int64_t l = row / M;
-    const uint8_t* a_row = A + row * K2;
-    const uint8_t* sa_row = sfa + row * K16;
+    int64_t a_index = row;  // row of A (and of sfa) this output row reads
+    float ga = g_a, gb = g_b;
+    if (G.E > 0) {
+      const int e = group_of_batch(G, l, lane);
+      if (e < 0) {
+        if (lane == 0) c[row] = 0;
+        continue;
+      }
+      a_index = (int64_t)e * M + (row - l * M);
+      ga = __ldcg(G.g_a + e);
+      gb = __ldcg(G.g_b + e);
+    }
+    const uint8_t* a_row = A + a_index * K2;
+    const uint8_t* sa_row = sfa + a_index * K16;
     const uint8_t* b_l = b + l * K2;
     const uint8_t* sb_l = sfb + l * K16;
     float acc = 0.f;
@@ -55,7 +97,7 @@ __global__ void __launch_bounds__(256) gemv_simple_kernel(
     }
 #pragma unroll
     for (int w = 16; w >= 1; w >>= 1) acc += __shfl_xor_sync(kFullMask, acc, w);
-    if (lane == 0) c[row] = f32_to_f16_bits((acc * g_a) * g_b);
+    if (lane == 0) c[row] = f32_to_out_bits((acc * ga) * gb, out_bf16 != 0);
   }
 }
 
@@ -98,6 +140,8 @@ struct StreamArgs {
   int32_t S;            // K slices per row
   int32_t slice_steps;  // 1024-element steps per slice (the last slice may be shorter)
   int32_t rows_cap;     // ceil(M / P): row capacity of the shared partial array
+  Groups G;             // grouped form (G.E > 0)
+  int32_t out_bf16;     // 1: bfloat16 output instead of fp16
 };
 
 constexpr int kStep = 1024;  // elements one warp covers per step (32 lanes x 32)
@@ -194,8 +238,20 @@ __global__ void __launch_bounds__(512) gemv_stream_kernel(const StreamArgs p) {
   const int64_t pi = blockIdx.x - l * p.P;
   const int64_t m0 = (p.M * pi) / p.P, m1 = (p.M * (pi + 1)) / p.P;
   const int n = (int)(m1 - m0);
-  const uint8_t* A_c = p.A + (l * p.M + m0) * K2;
-  const uint8_t* sfa_c = p.sfa + (l * p.M + m0) * K16;
+  int64_t ea = l;  // which matrix of A this CTA reads
+  float ga = p.g_a, gb = p.g_b;
+  if (p.G.E > 0) {  // grouped: every warp finds the same expert (the offsets do not change)
+    const int e = group_of_batch(p.G, l, lane);
+    if (e < 0) {
+      for (int t = tid; t < n; t += blockDim.x) p.c[l * p.M + m0 + t] = 0;
+      return;
+    }
+    ea = e;
+    ga = __ldcg(p.G.g_a + e);
+    gb = __ldcg(p.G.g_b + e);
+  }
+  const uint8_t* A_c = p.A + (ea * p.M + m0) * K2;
+  const uint8_t* sfa_c = p.sfa + (ea * p.M + m0) * K16;
   const int G = (n + R - 1) / R;
   const int U = G * p.S;
   const int64_t slice_elems = (int64_t)p.slice_steps * kStep;
@@ -290,7 +346,7 @@ __global__ void __launch_bounds__(512) gemv_stream_kernel(const StreamArgs p) {
   for (int t = tid; t < n; t += blockDim.x) {
     float v = part[t];
     for (int s = 1; s < p.S; ++s) v += part[s * p.rows_cap + t];
-    c_c[t] = f32_to_f16_bits((v * p.g_a) * p.g_b);
+    c_c[t] = f32_to_out_bits((v * ga) * gb, p.out_bf16 != 0);
   }
 }
 

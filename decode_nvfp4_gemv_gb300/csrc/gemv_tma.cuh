@@ -82,6 +82,9 @@ struct TmaArgs {
   int32_t rounding;
   uint8_t* b_out;
   uint8_t* sfb_out;
+  Groups G;              // grouped form (G.E > 0; never with early_weights: e(l) is read after
+                         // the programmatic-launch wait)
+  int32_t out_bf16;      // 1: bfloat16 output instead of fp16
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -144,6 +147,9 @@ __device__ __forceinline__ void tma_flush(float (&acc)[4], int lane, int row0, i
 struct TmaCta {
   int64_t l, pi, m0;
   int n, NT, Wc;
+  int64_t ea;     // the matrix of A this CTA streams: l, or the expert of token l
+  float ga, gb;   // global scales
+  bool skip;      // grouped form: token l has no expert, its outputs are zeros
 };
 
 __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
@@ -156,6 +162,10 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
   g.n = (int)(m1 - g.m0);
   g.NT = (g.n + p.tile_rows - 1) / p.tile_rows;
   g.Wc = (blockDim.x >> 5) - 1;
+  g.ea = g.l;
+  g.ga = p.g_a;
+  g.gb = p.g_b;
+  g.skip = false;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(smem_addr(&bars[s]), 1);                          // producer's arrive + bytes
@@ -169,14 +179,29 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
   return g;
 }
 
+// Grouped form, after the programmatic-launch wait: each warp finds token l's expert itself (all
+// warps read the same offsets, so they agree).  A token without an expert gets zero outputs.
+__device__ __forceinline__ void tma_resolve_group(const TmaArgs& p, TmaCta& g, int lane) {
+  if (p.G.E <= 0) return;
+  const int e = group_of_batch(p.G, g.l, lane);
+  g.skip = e < 0;
+  if (g.skip) {
+    for (int t = threadIdx.x; t < g.n; t += blockDim.x) p.c[g.l * p.M + g.m0 + t] = 0;
+    return;
+  }
+  g.ea = e;
+  g.ga = __ldcg(p.G.g_a + e);
+  g.gb = __ldcg(p.G.g_b + e);
+}
+
 // The producer lane: streams the CTA's row tiles into the ring.
 __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, uint64_t* bars,
                                             volatile int* abort_flag, uint8_t* ring) {
   const int64_t K2 = p.K >> 1, K16 = p.K >> 4;
   const int NS = p.stages, TR = p.tile_rows;
   const uint64_t pol = l2_evict_first_policy();
-  const uint8_t* A_c = p.A + (g.l * p.M + g.m0) * K2;
-  const uint8_t* S_c = p.sfa + (g.l * p.M + g.m0) * K16;
+  const uint8_t* A_c = p.A + (g.ea * p.M + g.m0) * K2;
+  const uint8_t* S_c = p.sfa + (g.ea * p.M + g.m0) * K16;
   int issued = 0;
   bool ok = true;
   for (int T = 0; T < g.NT; ++T) {
@@ -231,7 +256,8 @@ __device__ __forceinline__ void tma_epilogue(const TmaArgs& p, const TmaCta& g, 
   for (int t = threadIdx.x; t < g.n; t += 32 * g.Wc) {
     float v = 0.f;
     for (int q = 0; q < p.slots; ++q) v += part[t * p.slots + q];
-    c_c[t] = failed ? (uint16_t)0x7E00 : f32_to_f16_bits((v * p.g_a) * p.g_b);
+    const uint16_t nan_bits = p.out_bf16 ? (uint16_t)0x7FC0 : (uint16_t)0x7E00;
+    c_c[t] = failed ? nan_bits : f32_to_out_bits((v * g.ga) * g.gb, p.out_bf16 != 0);
   }
 }
 
@@ -249,8 +275,10 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
   const int64_t K = p.K, K2 = p.K >> 1, K16 = p.K >> 4;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  const TmaCta g = tma_setup(p, bars, abort_flag);
+  TmaCta g = tma_setup(p, bars, abort_flag);
   if (!p.early_weights) pdl_wait();
+  tma_resolve_group(p, g, lane);
+  if (g.skip) return;
   if (warp == g.Wc) {
     if (lane == 0) tma_produce(p, g, bars, abort_flag, ring);
     return;
@@ -360,8 +388,10 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
   const int64_t K = p.K, K2 = p.K >> 1, K16 = p.K >> 4;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  const TmaCta g = tma_setup(p, bars, abort_flag);
+  TmaCta g = tma_setup(p, bars, abort_flag);
   if (!p.early_weights) pdl_wait();
+  tma_resolve_group(p, g, lane);
+  if (g.skip) return;
   if (warp == g.Wc) {
     if (lane == 0) tma_produce(p, g, bars, abort_flag, ring);
     return;

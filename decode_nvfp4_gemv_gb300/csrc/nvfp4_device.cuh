@@ -5,6 +5,7 @@
 // element with even k in its low nibble; an E4M3FN block scale covers 16 consecutive k.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -115,6 +116,15 @@ __device__ __forceinline__ uint16_t ld_l2_u16(const void* p) {
 // fp32 -> IEEE binary16 bits, round-to-nearest-even, overflow to +-inf.
 __device__ __forceinline__ uint16_t f32_to_f16_bits(float x) {
   return __half_as_ushort(__float2half_rn(x));
+}
+
+// fp32 -> bfloat16 bits, round-to-nearest-even.
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ uint16_t f32_to_out_bits(float x, bool bf16) {
+  return bf16 ? f32_to_bf16_bits(x) : f32_to_f16_bits(x);
 }
 
 }  // namespace nvfp4

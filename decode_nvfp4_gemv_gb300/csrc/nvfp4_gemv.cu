@@ -109,8 +109,11 @@ bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
   return x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
 }
 
+// n_mats: matrices in A and sfa (L for the batched form, E for the grouped form).
 int check_args(const uint8_t* A, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
-               const uint16_t* c, int64_t M, int64_t K, int64_t L, bool* noop) {
+               const uint16_t* c, int64_t M, int64_t K, int64_t L, bool* noop,
+               int64_t n_mats = -1) {
+  if (n_mats < 0) n_mats = L;
   *noop = false;
   if (M < 0 || L < 0 || K <= 0)
     return fail(NVFP4_ERR_INVALID_VALUE, "need M >= 0, L >= 0, K > 0 (M=%lld K=%lld L=%lld)",
@@ -129,7 +132,7 @@ int check_args(const uint8_t* A, const uint8_t* sfa, const uint8_t* b, const uin
     return fail(NVFP4_ERR_MISALIGNED, "A, sfa, b and sfb must be 16-byte aligned");
   if ((uintptr_t)c & 1u) return fail(NVFP4_ERR_MISALIGNED, "c must be 2-byte aligned");
   // products fit easily: M, L < 2^31 and K/2 < 2^31 would overflow int64 only beyond 2^62
-  const int64_t nA = M * L * (K / 2), nSA = M * L * (K / 16), nB = L * (K / 2),
+  const int64_t nA = M * n_mats * (K / 2), nSA = M * n_mats * (K / 16), nB = L * (K / 2),
                 nSB = L * (K / 16), nC = 2 * M * L;
   if (overlaps(c, nC, A, nA) || overlaps(c, nC, sfa, nSA) || overlaps(c, nC, b, nB) ||
       overlaps(c, nC, sfb, nSB))
@@ -444,20 +447,36 @@ struct FusedVector {
   uint8_t* sfb_out;
 };
 
+// The grouped-form inputs of a launch (E == 0: the batched form) and the output type.
+struct GroupedOut {
+  nvfp4::Groups G;
+  int out_bf16;
+};
+
 int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const uint8_t* sfa,
            float g_a, const uint8_t* b, const uint8_t* sfb, float g_b, uint16_t* c, int64_t M,
-           int64_t K, int64_t L, cudaStream_t stream, const FusedVector* fx = nullptr) {
+           int64_t K, int64_t L, cudaStream_t stream, const FusedVector* fx = nullptr,
+           const GroupedOut* go = nullptr) {
   (void)d;
   const int threads = pl.warps_per_cta * 32;
+  nvfp4::Groups G;
+  memset(&G, 0, sizeof G);
+  int out_bf16 = 0;
+  if (go) {
+    G = go->G;
+    out_bf16 = go->out_bf16;
+  }
   if (pl.kernel == NVFP4_KERNEL_SIMPLE) {
     const int64_t grid = std::min<int64_t>((int64_t)pl.ctas_per_batch * L, (int64_t(1) << 31) - 1);
     nvfp4::gemv_simple_kernel<<<(unsigned)grid, threads, 0, stream>>>(A, sfa, b, sfb, g_a, g_b, c,
-                                                                      M, K, L);
+                                                                      M, K, L, G, out_bf16);
   } else if (pl.kernel == NVFP4_KERNEL_STREAM) {
     nvfp4::StreamArgs a;
     a.A = A; a.sfa = sfa; a.b = b; a.sfb = sfb; a.c = c;
     a.g_a = g_a; a.g_b = g_b;
     a.M = M; a.K = K; a.L = L;
+    a.G = G;
+    a.out_bf16 = out_bf16;
     a.P = pl.ctas_per_batch;
     const int64_t steps = ceil_div(K, nvfp4::kStep);
     a.slice_steps = (int32_t)ceil_div(steps, pl.k_split);
@@ -476,6 +495,8 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     a.A = A; a.sfa = sfa; a.b = b; a.sfb = sfb; a.c = c;
     a.g_a = g_a; a.g_b = g_b;
     a.M = M; a.K = K; a.L = L;
+    a.G = G;
+    a.out_bf16 = out_bf16;
     a.P = pl.ctas_per_batch;
     a.tile_rows = pl.tile_rows;
     a.stages = pl.stages;
@@ -649,6 +670,55 @@ int gemv_bf16_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16
   return launch(*d, pl, A, sfa, g_a, b_out, sfb_out, x_gs, c, M, K, L, (cudaStream_t)stream);
 }
 
+// ---------------------------------------------------------------- grouped (mixture of experts)
+constexpr int64_t kMaxExperts = 65536;
+
+int grouped_impl(const uint8_t* A, const uint8_t* sfa, const float* g_a, const uint8_t* b,
+                 const uint8_t* sfb, const float* g_b, const int32_t* offsets,
+                 const int32_t* expert_of, uint16_t* c, int out_dtype, int64_t M, int64_t K,
+                 int64_t E, int64_t T, void* stream, const nvfp4_plan* forced) {
+  g_last_error[0] = '\0';
+  if (E < 1 || E > kMaxExperts)
+    return fail(E < 1 ? NVFP4_ERR_INVALID_VALUE : NVFP4_ERR_UNSUPPORTED_SHAPE,
+                "need 1 <= E <= %lld experts (E=%lld)", (long long)kMaxExperts, (long long)E);
+  if ((offsets == nullptr) == (expert_of == nullptr))
+    return fail(NVFP4_ERR_INVALID_VALUE,
+                "give exactly one of expert_offsets and expert_of_token");
+  if (out_dtype != NVFP4_OUT_F16 && out_dtype != NVFP4_OUT_BF16)
+    return fail(NVFP4_ERR_INVALID_VALUE, "unknown output type %d", out_dtype);
+  if (forced && (forced->flags & (NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_QUANTIZE_IN_GEMV)))
+    return fail(NVFP4_ERR_INVALID_VALUE,
+                "the grouped form reads each token's expert after the launch wait: no early "
+                "weights, no in-GEMV quantization");
+  bool noop = false;
+  int st = check_args(A, sfa, b, sfb, c, M, K, T, &noop, E);
+  if (st != NVFP4_OK || noop) return st;
+  if (!g_a || !g_b) return fail(NVFP4_ERR_INVALID_VALUE, "NULL global-scale array");
+  const void* idx = offsets ? (const void*)offsets : (const void*)expert_of;
+  if (((uintptr_t)g_a | (uintptr_t)g_b | (uintptr_t)idx) & 3u)
+    return fail(NVFP4_ERR_MISALIGNED, "g_a, g_b and the expert indices must be 4-byte aligned");
+  const int64_t nC = 2 * M * T, nIdx = 4 * (offsets ? E : T);
+  if (overlaps(c, nC, g_a, 4 * E) || overlaps(c, nC, g_b, 4 * E) || overlaps(c, nC, idx, nIdx))
+    return fail(NVFP4_ERR_INVALID_VALUE, "c overlaps an input");
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if ((st = check_access(*d, A, "A")) || (st = check_access(*d, sfa, "sfa")) ||
+      (st = check_access(*d, b, "b")) || (st = check_access(*d, sfb, "sfb")) ||
+      (st = check_access(*d, c, "c")) || (st = check_access(*d, g_a, "g_a")) ||
+      (st = check_access(*d, g_b, "g_b")) || (st = check_access(*d, idx, "expert indices")))
+    return st;
+  nvfp4_plan pl;
+  if ((st = make_plan(*d, M, K, T, forced, &pl)) != NVFP4_OK) return st;
+  GroupedOut go;
+  go.G.offsets = offsets;
+  go.G.expert_of = expert_of;
+  go.G.g_a = g_a;
+  go.G.g_b = g_b;
+  go.G.E = (int32_t)E;
+  go.out_bf16 = out_dtype == NVFP4_OUT_BF16 ? 1 : 0;
+  return launch(*d, pl, A, sfa, 1.f, b, sfb, 1.f, c, M, K, T, (cudaStream_t)stream, nullptr, &go);
+}
+
 }  // namespace
 
 extern "C" {
@@ -657,6 +727,14 @@ int nvfp4_gemv_batched(const uint8_t* A, const uint8_t* sfa, float g_a, const ui
                        const uint8_t* sfb, float g_b, uint16_t* c, int64_t M, int64_t K, int64_t L,
                        void* stream) {
   return gemv_impl(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream, nullptr);
+}
+
+int nvfp4_gemv_grouped(const uint8_t* A, const uint8_t* sfa, const float* g_a, const uint8_t* b,
+                       const uint8_t* sfb, const float* g_b, const int32_t* expert_offsets,
+                       const int32_t* expert_of_token, uint16_t* c, int out_dtype, int64_t M,
+                       int64_t K, int64_t E, int64_t T, void* stream, const nvfp4_plan* plan) {
+  return grouped_impl(A, sfa, g_a, b, sfb, g_b, expert_offsets, expert_of_token, c, out_dtype, M,
+                      K, E, T, stream, plan);
 }
 
 int nvfp4_gemv_batched_ex(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,

@@ -62,7 +62,7 @@
 extern "C" {
 #endif
 
-#define NVFP4_ABI_VERSION 2
+#define NVFP4_ABI_VERSION 3
 
 typedef enum nvfp4_status {
   NVFP4_OK = 0,
@@ -184,6 +184,38 @@ int nvfp4_gemv_batched_bf16(const uint8_t* A, const uint8_t* sfa, float g_a, con
                             float x_global_scale, int rounding, uint8_t* b_out, uint8_t* sfb_out,
                             uint16_t* c, int64_t M, int64_t K, int64_t L, void* stream,
                             const nvfp4_plan* plan);
+
+/* ------------------------------------------------------------------------------------------
+ * Grouped (mixture-of-experts) decode GEMV.  cutedsl/bridge.py, "Kernel Launch"
+ * (run_nvfp4_grouped_gemm: a 2-D token operand times a 3-D expert operand, per-expert fp32 global
+ * scales, bf16 output) and "compute_expert_offsets" (tokens sorted by expert; offsets[e] = the
+ * number of tokens of experts 0..e); the per-token expert index is the row-to-group map of the
+ * grouped-GEMM API in the flashinfer docs (group_deepgemm_fp8_nt_groupwise, m_indices).
+ *
+ *   c[t][m] = out( g_a[e] * g_b[e] * sum_k e2m1(A[e][m][k]) e2m1(b[t][k]) e4m3(sfa[e][m][k/16])
+ *                                          e4m3(sfb[t][k/16]) ),   e = e(t)
+ *
+ * A [E][M][K/2], sfa [E][M][K/16]: the experts' weights (layout of nvfp4_gemv_batched with L = E).
+ * b [T][K/2], sfb [T][K/16]: one packed vector per token.  c [T][M]: 16-bit outputs, fp16
+ * (NVFP4_OUT_F16) or bfloat16 (NVFP4_OUT_BF16), round to nearest even.  g_a, g_b: [E] fp32 device
+ * arrays.  Exactly one of:
+ *   expert_offsets [E] int32: inclusive cumulative token counts, non-decreasing; token t belongs
+ *     to the first e with t < expert_offsets[e];
+ *   expert_of_token [T] int32: the expert of each token.
+ * A token without an expert (t >= expert_offsets[E-1], or an index outside [0, E)) gets an output
+ * row of zeros.  Offsets that decrease give an unspecified (but in-bounds) assignment.
+ * The expert indices and global scales are read on the device after the preceding work in the
+ * stream, so they may be produced by it (a router); NVFP4_FLAG_EARLY_WEIGHTS and
+ * NVFP4_FLAG_QUANTIZE_IN_GEMV are rejected (INVALID_VALUE).  1 <= E <= 65536.  Other checks,
+ * alignment (16 bytes for A, sfa, b, sfb; 4 for g_a, g_b and the indices), plans and status
+ * codes: as for nvfp4_gemv_batched_ex with L = T; M == 0 or T == 0 enqueues nothing.
+ * ------------------------------------------------------------------------------------------ */
+typedef enum { NVFP4_OUT_F16 = 0, NVFP4_OUT_BF16 = 1 } nvfp4_out_dtype;
+
+int nvfp4_gemv_grouped(const uint8_t* A, const uint8_t* sfa, const float* g_a, const uint8_t* b,
+                       const uint8_t* sfb, const float* g_b, const int32_t* expert_offsets,
+                       const int32_t* expert_of_token, uint16_t* c, int out_dtype, int64_t M,
+                       int64_t K, int64_t E, int64_t T, void* stream, const nvfp4_plan* plan);
 
 /* NVFP4_ABI_VERSION of the built library. */
 int nvfp4_abi_version(void);

@@ -11,6 +11,8 @@ Contents, each written from the pages' definitions (citations in each module):
 * ``codecs``   E2M1 / E4M3FN decoders from their bit layouts, nibble unpacking, fp16 rounding.
 * ``nvfp4_gemv`` the GEMV definition in fp64 (``gemv``, ``gemv_rows``) and an independent exact
                integer formulation (``gemv_exact_units``).
+* ``grouped``  the grouped (mixture-of-experts) decode GEMV: expert ownership from the bridge's
+               cumulative offsets or from a per-token index, then the GEMV definition per token.
 * ``quantize`` the NVFP4 activation quantizer with a fixed global scale (bridge.py,
                ``quantize_activation_nvfp4``): the page's half-step-table rounding and
                round-to-nearest-even, fp32 steps in the page's order.
@@ -30,6 +32,11 @@ Pins (tests that tie the oracle to something other than itself):
 * quantizer: the printed half-step table; its E4M3 encoder against torch's cast; exact grid
   round-trips; brute-force nearest rounding; error bounds; sign symmetry; bit-for-bit agreement
   with the workload generator's independently written quantizer.
+
+* grouped: ownership on a worked offsets example and against a second formulation; identity
+  routing == the batched definition; one expert == the batched definition over a repeated
+  matrix; expert relabelling; per-expert scales; a brute-force loop over tiny inputs; planted
+  mistakes (off-by-one ownership, scales indexed by token) each fail a pin.
 
 No function in this package is "parity unpinned".
 """

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_status_strings(lib):
     import decode_nvfp4_gemv_gb300 as pkg
 
-    assert pkg.nvfp4_abi_version() == 2
+    assert pkg.nvfp4_abi_version() == 3
     assert pkg.nvfp4_status_string(0) == "ok"
     assert pkg.nvfp4_status_string(2) == "misaligned pointer"
     assert pkg.nvfp4_status_string(99) == "unknown status"
@@ -139,3 +139,30 @@ def test_gemv_bf16_rejected_before_device_work(lib, kw, status):
 
 def test_gemv_bf16_empty_is_a_noop(lib):
     assert _gemv_bf16(lib, M=0, A=0, sfa=0, c=0) == 0
+
+
+def _grouped(lib, A=0x100000, sfa=0x200000, ga=0x300000, b=0x400000, sfb=0x500000, gb=0x600000,
+             offs=0x700000, emap=0, c=0x800000, out=0, M=4, K=256, E=2, T=3, flags=None):
+    vp = ctypes.c_void_p
+    import decode_nvfp4_gemv_gb300 as pkg
+
+    plan = ctypes.byref(pkg.Plan(flags=flags)) if flags is not None else None
+    return lib.nvfp4_gemv_grouped(vp(A), vp(sfa), vp(ga), vp(b), vp(sfb), vp(gb),
+                                  vp(offs) if offs else None, vp(emap) if emap else None, vp(c),
+                                  out, M, K, E, T, None, plan)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(E=0), 1), (dict(E=70000), 3), (dict(offs=0), 1), (dict(emap=0x900000), 1),
+    (dict(out=2), 1), (dict(flags=1), 1), (dict(flags=4), 1), (dict(K=24), 1),
+    (dict(ga=0), 1), (dict(gb=0), 1), (dict(ga=0x300002), 2), (dict(offs=0x700001), 2),
+    (dict(A=0x100008), 2), (dict(c=0x700000), 1),   # c overlaps the offsets
+    (dict(c=0x300000), 1),                          # c overlaps g_a
+])
+def test_grouped_rejected_before_device_work(lib, kw, status):
+    assert _grouped(lib, **kw) == status
+
+
+def test_grouped_empty_is_a_noop(lib):
+    assert _grouped(lib, T=0, A=0, sfa=0, b=0, sfb=0, c=0) == 0
+    assert _grouped(lib, M=0, A=0, sfa=0, b=0, sfb=0, c=0) == 0

@@ -38,7 +38,8 @@ _M1 = 0xBF58476D1CE4E5B9
 _M2 = 0x94D049BB133111EB
 _U64 = np.uint64
 
-TENSOR_IDS = {"A": 0, "sfa": 1, "b": 2, "sfb": 3, "x": 4}   # x: a bf16 activation vector
+TENSOR_IDS = {"A": 0, "sfa": 1, "b": 2, "sfb": 3, "x": 4, "route": 5, "g": 6}
+# x: a bf16 activation vector; route: expert choices of the grouped workloads; g: their scales
 
 
 _CHUNK = 1 << 20  # draws per chunk: temporaries stay cache-resident
@@ -277,6 +278,78 @@ def make(name: str, seed: int | None = None) -> Workload:
     else:
         raise KeyError(name)
     return w
+
+
+# ---------------------------------------------------------------------------------------------
+# Grouped (mixture-of-experts) decode workloads.  E experts' weights [E][M][K/2] drawn like c5
+# (M=3584, K=6144 is the expert shape of the bridge's grouped GEMM); each of `tokens` tokens picks
+# `top_k` distinct experts uniformly at random; the (token, expert) rows are sorted by expert
+# (stable) and each row gets its own packed vector.  Per-expert global scales are drawn from small
+# sets of powers of two.  `route` selects an independent routing and vectors over the same
+# weights.  Only draws here: the expert offsets are derived by the caller.
+# ---------------------------------------------------------------------------------------------
+@dataclass
+class GroupedWorkload:
+    name: str
+    M: int
+    K: int
+    E: int
+    T: int
+    A: np.ndarray          # uint8 [E][M][K/2]
+    sfa: np.ndarray        # uint8 [E][M][K/16]
+    g_a: np.ndarray        # float32 [E]
+    g_b: np.ndarray        # float32 [E]
+    b: np.ndarray          # uint8 [T][K/2]
+    sfb: np.ndarray        # uint8 [T][K/16]
+    expert_of: np.ndarray  # int32 [T], non-decreasing
+    seed: int
+    recipe: str = ""
+
+    @property
+    def active_experts(self) -> int:
+        return len(np.unique(self.expert_of[self.expert_of >= 0]))
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Bytes a call must move: the weights and scales of every expert that owns a token, once;
+        the vectors, the outputs (16-bit) and the per-expert scales and offsets."""
+        M, K, E, T = self.M, self.K, self.E, self.T
+        return (self.active_experts * (M * K // 2 + M * K // 16) + T * (K // 2 + K // 16)
+                + 2 * M * T + 12 * E)
+
+
+GROUPED = {
+    "g1": dict(M=3584, K=6144, E=32, tokens=2, top_k=8, seed=11),
+    "g0": dict(M=96, K=512, E=6, tokens=3, top_k=2, seed=12),
+}
+
+
+def grouped_routing(seed: int, route: int, tokens: int, top_k: int, E: int) -> np.ndarray:
+    keys = uniform01(seed * 1009 + route, "route", tokens * E).reshape(tokens, E)
+    chosen = np.argsort(keys, axis=1, kind="stable")[:, :top_k]
+    return np.sort(chosen.ravel(), kind="stable").astype(np.int32)
+
+
+def make_grouped(name: str, route: int = 0, with_weights=None) -> GroupedWorkload:
+    """with_weights: a GroupedWorkload of the same config whose weights are reused."""
+    cfg = GROUPED[name]
+    M, K, E, s = cfg["M"], cfg["K"], cfg["E"], cfg["seed"]
+    expert_of = grouped_routing(s, route, cfg["tokens"], cfg["top_k"], E)
+    T = len(expert_of)
+    if with_weights is not None:
+        A, sfa, g_a, g_b = with_weights.A, with_weights.sfa, with_weights.g_a, with_weights.g_b
+    else:
+        A = uniform_bytes(s, "A", E * M * K // 2).reshape(E, M, K // 2)
+        sfa = choice_bytes(s, "sfa", E * M * K // 16, pow2_scale_bytes(-4, 3)).reshape(E, M, K // 16)
+        gi = choice_bytes(s, "g", 2 * E, (0, 1, 2, 3))
+        g_a = np.float32([0.25, 0.5, 1.0, 2.0])[gi[:E]]
+        g_b = np.float32([0.5, 1.0, 2.0, 0.25])[gi[E:]]
+    vs = s * 1009 + route
+    b = uniform_bytes(vs, "b", T * K // 2).reshape(T, K // 2)
+    sfb = choice_bytes(vs, "sfb", T * K // 16, pow2_scale_bytes(-4, 3)).reshape(T, K // 16)
+    return GroupedWorkload(name, M, K, E, T, A, sfa, g_a, g_b, b, sfb, expert_of, s,
+                           recipe=f"{E} experts, {cfg['tokens']} tokens x top-{cfg['top_k']}, "
+                                  "uniform bytes, scales 2^-4..2^3, per-expert g in powers of two")
 
 
 def describe(name: str) -> str:
