@@ -392,6 +392,63 @@ def time_grouped(pkg, device, stream, steps, warmup, dist, name="g1", n_routes=4
     }
 
 
+def time_general(pkg, w, stream, steps, warmup, dist, n_copies):
+    """The general path: the same workload with every input 1 byte past a 16-byte boundary, which
+    the planner sends to the byte-load kernel (any alignment, any K % 16 == 0)."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    sets, keep = [], []
+    for _ in range(n_copies):
+        s = {}
+        for k in ("A", "sfa", "b", "sfb"):
+            x = np.ascontiguousarray(getattr(w, k)).ravel()
+            raw = torch.empty(x.size + 32, dtype=torch.uint8, device=dev)
+            v = raw[1:1 + x.size]
+            v.copy_(torch.from_numpy(x))
+            keep.append(raw)
+            s[k] = v
+        sets.append(s)
+    outs = [torch.empty((w.L, w.M), dtype=torch.float16, device=dev) for _ in range(n_copies)]
+
+    def call(i):
+        s = sets[i % n_copies]
+        pkg.nvfp4_gemv_batched(s["A"], s["sfa"], w.g_a, s["b"], s["sfb"], w.g_b, outs[i % n_copies],
+                               w.M, w.K, w.L, stream=stream)
+
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 1)):
+            call(i)
+    stream.synchronize()
+    chunk = min(GRAPH_CHUNK, steps)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(chunk):
+            call(i)
+    reps = max(1, steps // chunk)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+    sec = ev0.elapsed_time(ev1) / 1e3
+    calls = reps * chunk
+    tot, slow = aggregate(dist, w.algorithmic_bytes * calls, sec)
+    peak, _ = measured_peak_gbs()
+    del g
+    return {"inputs": "A, sfa, b, sfb each 1 byte past a 16-byte boundary",
+            "kernel": KERNEL_NAMES.get(1), "us_per_call": round(sec / calls * 1e6, 3),
+            "calls": calls, "GB/s": round(tot / slow / 1e9, 2), "frac": round(tot / slow / 1e9 / peak, 4)}
+
+
 def run_ours(args):
     import torch
 
@@ -475,6 +532,10 @@ def run_ours(args):
         bf16 = time_bf16_vector(pkg, w, sets, outs, stream, min(args.steps, 20000), args.warmup,
                                 dist)
 
+    general = None
+    if not args.plan and not args.no_general:
+        general = time_general(pkg, w, stream, min(args.steps, 2000), args.warmup, dist, n_copies)
+
     grouped = None
     if not args.plan and not args.no_grouped:
         grouped = time_grouped(pkg, device, stream, min(args.steps, 20000), args.warmup, dist)
@@ -533,6 +594,8 @@ def run_ours(args):
             line["bf16_vector"] = bf16
         if grouped is not None:
             line["grouped"] = grouped
+        if general is not None:
+            line["general_unaligned"] = general
         if e2e is not None:
             line["e2e"] = e2e
         if cpu is not None:
@@ -662,6 +725,8 @@ def main():
                     help="skip the bf16-vector (activation quantization) timing")
     ap.add_argument("--no-grouped", action="store_true",
                     help="skip the grouped (mixture-of-experts) timing")
+    ap.add_argument("--no-general", action="store_true",
+                    help="skip the unaligned-input (byte-load kernel) timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)

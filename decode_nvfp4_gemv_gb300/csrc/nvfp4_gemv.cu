@@ -110,11 +110,14 @@ bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
 }
 
 // n_mats: matrices in A and sfa (L for the batched form, E for the grouped form).
+// *aligned16: A, sfa, b and sfb all 16-byte aligned (the vector-load and TMA kernels need it; the
+// simple kernel's byte loads take any alignment).
 int check_args(const uint8_t* A, const uint8_t* sfa, const uint8_t* b, const uint8_t* sfb,
                const uint16_t* c, int64_t M, int64_t K, int64_t L, bool* noop,
-               int64_t n_mats = -1) {
+               bool* aligned16, int64_t n_mats = -1) {
   if (n_mats < 0) n_mats = L;
   *noop = false;
+  *aligned16 = true;
   if (M < 0 || L < 0 || K <= 0)
     return fail(NVFP4_ERR_INVALID_VALUE, "need M >= 0, L >= 0, K > 0 (M=%lld K=%lld L=%lld)",
                 (long long)M, (long long)K, (long long)L);
@@ -128,8 +131,7 @@ int check_args(const uint8_t* A, const uint8_t* sfa, const uint8_t* b, const uin
     return NVFP4_OK;
   }
   if (!A || !sfa || !b || !sfb || !c) return fail(NVFP4_ERR_INVALID_VALUE, "NULL pointer");
-  if (((uintptr_t)A | (uintptr_t)sfa | (uintptr_t)b | (uintptr_t)sfb) & 15u)
-    return fail(NVFP4_ERR_MISALIGNED, "A, sfa, b and sfb must be 16-byte aligned");
+  *aligned16 = (((uintptr_t)A | (uintptr_t)sfa | (uintptr_t)b | (uintptr_t)sfb) & 15u) == 0;
   if ((uintptr_t)c & 1u) return fail(NVFP4_ERR_MISALIGNED, "c must be 2-byte aligned");
   // products fit easily: M, L < 2^31 and K/2 < 2^31 would overflow int64 only beyond 2^62
   const int64_t nA = M * n_mats * (K / 2), nSA = M * n_mats * (K / 16), nB = L * (K / 2),
@@ -395,10 +397,15 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
 
 // Fills every field of *pl for (M, K, L); `forced` fields (non-zero) are honoured or rejected.
 int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan* forced,
-              nvfp4_plan* pl) {
+              nvfp4_plan* pl, bool aligned16 = true) {
   nvfp4_plan f;
   memset(&f, 0, sizeof f);
   if (forced) f = *forced;
+  if (!aligned16 && f.kernel != NVFP4_KERNEL_AUTO && f.kernel != NVFP4_KERNEL_SIMPLE)
+    return fail(NVFP4_ERR_MISALIGNED,
+                "kernel %d needs 16-byte aligned A, sfa, b and sfb (the simple kernel takes any)",
+                f.kernel);
+  if (!aligned16) f.kernel = NVFP4_KERNEL_SIMPLE;
   if (f.flags & ~(NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_NO_PDL | NVFP4_FLAG_QUANTIZE_IN_GEMV))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown plan flags 0x%x", (unsigned)f.flags);
   if (f.warps_per_cta < 0 || f.rows_per_warp < 0 || f.k_split < 0 || f.ctas_per_batch < 0 ||
@@ -554,8 +561,8 @@ int gemv_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
               const uint8_t* sfb, float g_b, uint16_t* c, int64_t M, int64_t K, int64_t L,
               void* stream, const nvfp4_plan* forced) {
   g_last_error[0] = '\0';
-  bool noop = false;
-  int st = check_args(A, sfa, b, sfb, c, M, K, L, &noop);
+  bool noop = false, aligned16 = true;
+  int st = check_args(A, sfa, b, sfb, c, M, K, L, &noop, &aligned16);
   if (st != NVFP4_OK || noop) return st;
   const DeviceInfo* d = nullptr;
   if ((st = current_device(&d)) != NVFP4_OK) return st;
@@ -566,7 +573,7 @@ int gemv_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
   if (forced && (forced->flags & NVFP4_FLAG_QUANTIZE_IN_GEMV))
     return fail(NVFP4_ERR_INVALID_VALUE, "NVFP4_FLAG_QUANTIZE_IN_GEMV needs a bf16 vector");
   nvfp4_plan pl;
-  if ((st = make_plan(*d, M, K, L, forced, &pl)) != NVFP4_OK) return st;
+  if ((st = make_plan(*d, M, K, L, forced, &pl, aligned16)) != NVFP4_OK) return st;
   return launch(*d, pl, A, sfa, g_a, b, sfb, g_b, c, M, K, L, (cudaStream_t)stream);
 }
 
@@ -635,8 +642,8 @@ int gemv_bf16_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16
                    int rounding, uint8_t* b_out, uint8_t* sfb_out, uint16_t* c, int64_t M,
                    int64_t K, int64_t L, void* stream, const nvfp4_plan* forced) {
   g_last_error[0] = '\0';
-  bool noop = false;
-  int st = check_args(A, sfa, b_out, sfb_out, c, M, K, L, &noop);
+  bool noop = false, aligned16 = true;
+  int st = check_args(A, sfa, b_out, sfb_out, c, M, K, L, &noop, &aligned16);
   if (st != NVFP4_OK || noop) return st;
   if ((st = check_quant_args(x, x_gs, b_out, sfb_out, K, L, rounding, &noop)) != NVFP4_OK)
     return st;
@@ -652,7 +659,7 @@ int gemv_bf16_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16
       (st = check_access(*d, sfb_out, "sfb_out")) || (st = check_access(*d, c, "c")))
     return st;
   nvfp4_plan pl;
-  if ((st = make_plan(*d, M, K, L, forced, &pl)) != NVFP4_OK) return st;
+  if ((st = make_plan(*d, M, K, L, forced, &pl, aligned16)) != NVFP4_OK) return st;
   if (pl.flags & NVFP4_FLAG_QUANTIZE_IN_GEMV) {  // quantize inside the GEMV's vector staging
     if (pl.kernel != NVFP4_KERNEL_TMA_RV)
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
@@ -690,8 +697,8 @@ int grouped_impl(const uint8_t* A, const uint8_t* sfa, const float* g_a, const u
     return fail(NVFP4_ERR_INVALID_VALUE,
                 "the grouped form reads each token's expert after the launch wait: no early "
                 "weights, no in-GEMV quantization");
-  bool noop = false;
-  int st = check_args(A, sfa, b, sfb, c, M, K, T, &noop, E);
+  bool noop = false, aligned16 = true;
+  int st = check_args(A, sfa, b, sfb, c, M, K, T, &noop, &aligned16, E);
   if (st != NVFP4_OK || noop) return st;
   if (!g_a || !g_b) return fail(NVFP4_ERR_INVALID_VALUE, "NULL global-scale array");
   const void* idx = offsets ? (const void*)offsets : (const void*)expert_of;
@@ -708,7 +715,7 @@ int grouped_impl(const uint8_t* A, const uint8_t* sfa, const float* g_a, const u
       (st = check_access(*d, g_b, "g_b")) || (st = check_access(*d, idx, "expert indices")))
     return st;
   nvfp4_plan pl;
-  if ((st = make_plan(*d, M, K, T, forced, &pl)) != NVFP4_OK) return st;
+  if ((st = make_plan(*d, M, K, T, forced, &pl, aligned16)) != NVFP4_OK) return st;
   GroupedOut go;
   go.G.offsets = offsets;
   go.G.expert_of = expert_of;

@@ -47,7 +47,11 @@
  *   NVFP4_ERR_INVALID_VALUE   M < 0, L < 0, K <= 0, K % 16 != 0, a NULL pointer when M*L > 0,
  *                             c overlapping an input, or an inaccessible pointer
  *   NVFP4_ERR_UNSUPPORTED_SHAPE  M, L or K/2 above 2^31 - 1, or an invalid forced plan
- *   NVFP4_ERR_MISALIGNED      A, sfa, b or sfb not 16-byte aligned, or c not 2-byte aligned
+ *   NVFP4_ERR_MISALIGNED      c not 2-byte aligned, or a forced plan other than SIMPLE while A,
+ *                             sfa, b or sfb is not 16-byte aligned
+ *   Any alignment of A, sfa, b and sfb is accepted: when one of them is not 16-byte aligned the
+ *   automatic plan is the simple kernel (byte loads), the general path for any alignment and any
+ *   K % 16 == 0.
  *   NVFP4_ERR_ARCH            the current device is not compute capability 10.3 (GB300)
  *   NVFP4_ERR_CUDA            a CUDA runtime call or the launch failed (nvfp4_last_error() has
  *                             the runtime's message)

@@ -61,7 +61,7 @@ def _call(lib, A=0x1000, sfa=0x2000, b=0x3000, sfb=0x4000, c=0x5000, M=4, K=256,
 @pytest.mark.parametrize("kw,status", [
     (dict(M=-1), 1), (dict(L=-2), 1), (dict(K=0), 1), (dict(K=24), 1), (dict(K=-16), 1),
     (dict(A=0), 1), (dict(sfb=0), 1), (dict(c=0), 1),
-    (dict(A=0x1008), 2), (dict(sfa=0x2001), 2), (dict(b=0x3004), 2), (dict(c=0x5001), 2),
+    (dict(c=0x5001), 2),
     (dict(c=0x1000), 1),                        # c overlaps A
     (dict(M=1 << 31), 3), (dict(K=1 << 33), 3),
 ])
@@ -156,7 +156,7 @@ def _grouped(lib, A=0x100000, sfa=0x200000, ga=0x300000, b=0x400000, sfb=0x50000
     (dict(E=0), 1), (dict(E=70000), 3), (dict(offs=0), 1), (dict(emap=0x900000), 1),
     (dict(out=2), 1), (dict(flags=1), 1), (dict(flags=4), 1), (dict(K=24), 1),
     (dict(ga=0), 1), (dict(gb=0), 1), (dict(ga=0x300002), 2), (dict(offs=0x700001), 2),
-    (dict(A=0x100008), 2), (dict(c=0x700000), 1),   # c overlaps the offsets
+    (dict(c=0x800001), 2), (dict(c=0x700000), 1),   # c overlaps the offsets
     (dict(c=0x300000), 1),                          # c overlaps g_a
 ])
 def test_grouped_rejected_before_device_work(lib, kw, status):

@@ -342,7 +342,11 @@ def test_error_statuses_with_real_buffers(pkg):
             return e.status
 
     assert status() == 0
-    assert status(A=raw[1:]) == 2                           # misaligned A
+    assert status(A=raw[1:]) == 0                           # any alignment: the simple kernel
+    with pytest.raises(pkg.NVFP4Error) as e:                # ... but no vector-load kernel
+        pkg.nvfp4_gemv_batched_ex(raw[1:], t["sfa"], 1.0, t["b"], t["sfb"], 1.0, c, 8, 256, 1,
+                                  plan=dict(kernel=2))
+    assert e.value.status == 2
     assert status(c=c.data_ptr() + 1) == 2                  # misaligned c (raw address)
     assert status(c=raw[2:].view(torch.int16)[:8]) == 0     # 2-byte aligned c is fine
     assert status(K=24) == 1
