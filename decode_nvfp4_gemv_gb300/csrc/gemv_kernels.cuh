@@ -188,7 +188,7 @@ template <int R>
 __device__ __forceinline__ void stream_compute(const uint32_t* __restrict__ bq,
                                                const float* __restrict__ sbf, int64_t k,
                                                const uint4 (&av)[R], const uint16_t (&sv)[R],
-                                               float (&acc)[R]) {
+                                               float2 (&acc)[R]) {
   // vector words for bytes k/2 .. k/2 + 15 (chunks q .. q+3, swizzled) and the two block scales
   const uint32_t q = (uint32_t)(k >> 3);
   uint4 bw[4];
@@ -219,9 +219,7 @@ __device__ __forceinline__ void stream_compute(const uint32_t* __restrict__ bq,
     hfma2(p1, h[13], bw[3].y);
     hfma2(p1, h[14], bw[3].z);
     hfma2(p1, h[15], bw[3].w);
-    const float2 sa = f16x2_to_f32x2(e4m3x2_to_f16x2(sv[i]));
-    acc[i] = fmaf(f16x2_hsum_f32(p0), sa.x * sb.x, acc[i]);
-    acc[i] = fmaf(f16x2_hsum_f32(p1), sa.y * sb.y, acc[i]);
+    ffma2(acc[i], scaled_block_pair(p0, p1, e4m3x2_to_f16x2(sv[i])), sb);
   }
 }
 
@@ -301,9 +299,9 @@ __global__ void __launch_bounds__(512) gemv_stream_kernel(const StreamArgs p) {
   }
   __syncthreads();
 
-  float acc[R];
+  float2 acc[R];  // per row: running sums of the lane's first and second blocks of a step
 #pragma unroll
-  for (int i = 0; i < R; ++i) acc[i] = 0.f;
+  for (int i = 0; i < R; ++i) acc[i] = make_float2(0.f, 0.f);
   while (u < U) {
     // the next position and, when it starts a new unit, that unit's geometry
     int un = u, jn = j + 1, gn = g, nsn = nsteps;
@@ -321,12 +319,15 @@ __global__ void __launch_bounds__(512) gemv_stream_kernel(const StreamArgs p) {
     const int64_t k = kb + (int64_t)j * kStep + 32 * lane;
     if (k < ke) stream_compute<R>(bq, sbf, k, av, sv, acc);
     if (un != u) {
-      const float row_sum = warp_reduce_rows<R>(acc, lane);
+      float r[R];
+#pragma unroll
+      for (int i = 0; i < R; ++i) r[i] = acc[i].x + acc[i].y;
+      const float row_sum = warp_reduce_rows<R>(r, lane);
       const int s = u - g * p.S;
       const int jr = lane / (32 / R);
       if ((lane & (32 / R - 1)) == 0 && g * R + jr < n) part[s * p.rows_cap + g * R + jr] = row_sum;
 #pragma unroll
-      for (int i = 0; i < R; ++i) acc[i] = 0.f;
+      for (int i = 0; i < R; ++i) acc[i] = make_float2(0.f, 0.f);
     }
 #pragma unroll
     for (int i = 0; i < R; ++i) {

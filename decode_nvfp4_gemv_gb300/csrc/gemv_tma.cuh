@@ -111,10 +111,11 @@ __device__ __forceinline__ float2 lds_f2(uint32_t a) {
 }
 
 // One row group (4 rows) times one 32-element lane slice: decode, exact block partials, scale.
-// bw: the 16 vector words for this lane's 32 elements; sb: the two vector block scales.
+// bw: the 16 vector words for this lane's 32 elements; sb: the two vector block scales.  acc[i]
+// holds row i's running sums of the lane's first and second blocks (added at the flush).
 __device__ __forceinline__ void item_compute4(const uint4 (&av)[4], const uint16_t (&sv)[4],
                                               const uint32_t (&bw)[16], float2 sb,
-                                              float (&acc)[4]) {
+                                              float2 (&acc)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t h[16];
@@ -127,20 +128,21 @@ __device__ __forceinline__ void item_compute4(const uint4 (&av)[4], const uint16
     for (int q = 0; q < 8; ++q) hfma2(p0, h[q], bw[q]);
 #pragma unroll
     for (int q = 8; q < 16; ++q) hfma2(p1, h[q], bw[q]);
-    const float2 sa = f16x2_to_f32x2(e4m3x2_to_f16x2(sv[i]));
-    acc[i] = fmaf(f16x2_hsum_f32(p0), sa.x * sb.x, acc[i]);
-    acc[i] = fmaf(f16x2_hsum_f32(p1), sa.y * sb.y, acc[i]);
+    ffma2(acc[i], scaled_block_pair(p0, p1, e4m3x2_to_f16x2(sv[i])), sb);
   }
 }
 
 // Reduces the 4 row sums of a group across the warp and stores them to partial[row][slot].
-__device__ __forceinline__ void tma_flush(float (&acc)[4], int lane, int row0, int rows_t,
+__device__ __forceinline__ void tma_flush(float2 (&acc)[4], int lane, int row0, int rows_t,
                                           float* part_tile, int slots, int slot) {
-  const float v = warp_reduce_rows<4>(acc, lane);
+  float r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r[i] = acc[i].x + acc[i].y;
+  const float v = warp_reduce_rows<4>(r, lane);
   const int j = lane >> 3;  // lanes 8j .. 8j+7 hold row j of the group
   if ((lane & 7) == 0 && row0 + j < rows_t) part_tile[(row0 + j) * slots + slot] = v;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) acc[i] = 0.f;
+  for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 }
 
 // Shared prologue: CTA geometry, barrier initialisation, dependent-launch trigger.
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
   const uint32_t x = ((uint32_t)lane >> 1) & 3u;
   const uint32_t bsw[4] = {16u * (0u ^ x), 16u * (1u ^ x), 16u * (2u ^ x), 16u * (3u ^ x)};
   const int rg0 = cw / nseg, sg0 = cw - rg0 * nseg;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
   for (int T = 0; T < g.NT; ++T) {
     if (!tma_consume_wait(p, bars, abort_flag, T, lane)) break;
     const int rows_t = min(p.tile_rows, g.n - T * p.tile_rows);
@@ -466,7 +468,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
         aoff[i] = stA + r * K2u + 16u * lane;
         soff[i] = stS + r * K16u + 2u * lane;
       }
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
       for (int j = 0; j < NSW; ++j) {
         if (live[j]) {

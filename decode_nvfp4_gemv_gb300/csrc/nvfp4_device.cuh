@@ -63,6 +63,38 @@ __device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h) {
   return make_float2(lo, hi);
 }
 
+// Two exact block partials scaled by their block scales, in fp32: for p0 (block A) and p1 (block
+// B) as f16x2 half sums and sa2 = (scale A, scale B) as f16x2, returns
+// ((p0.lo + p0.hi) * sa.A, (p1.lo + p1.hi) * sa.B) by four mixed-precision FMAs (f16 operands,
+// f32 accumulation).  Exact: each half sum is a multiple of 1/4 below 2^9 and a scale has 4
+// significant bits, so every product and both sums fit fp32's 24 bits.
+__device__ __forceinline__ float2 scaled_block_pair(uint32_t p0, uint32_t p1, uint32_t sa2) {
+  float a, b;
+  asm("{\n\t.reg .b16 a0, a1, b0, b1, s0, s1;\n\t"
+      "mov.b32 {a0, a1}, %2;\n\t"
+      "mov.b32 {b0, b1}, %3;\n\t"
+      "mov.b32 {s0, s1}, %4;\n\t"
+      "fma.rn.f32.f16 %0, a0, s0, 0f00000000;\n\t"
+      "fma.rn.f32.f16 %0, a1, s0, %0;\n\t"
+      "fma.rn.f32.f16 %1, b0, s1, 0f00000000;\n\t"
+      "fma.rn.f32.f16 %1, b1, s1, %1;\n\t}"
+      : "=f"(a), "=f"(b)
+      : "r"(p0), "r"(p1), "r"(sa2));
+  return make_float2(a, b);
+}
+
+// acc += a * b on both lanes of an fp32 pair (one packed fp32x2 FMA, round-to-nearest each).
+__device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%0, %1};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+}
+
 // low half + high half, in f32 (one widening and one mixed-precision add).
 __device__ __forceinline__ float f16x2_hsum_f32(uint32_t h) {
   float r;
