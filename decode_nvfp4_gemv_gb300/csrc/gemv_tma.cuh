@@ -196,6 +196,19 @@ __device__ __forceinline__ void tma_resolve_group(const TmaArgs& p, TmaCta& g, i
   g.gb = __ldcg(p.G.g_b + e);
 }
 
+// Ring position of tile T: stage T mod NS and the parity (T / NS) mod 2 of that stage's use,
+// advanced one tile at a time (no division in the loops).
+struct RingPos {
+  int s = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void advance(int stages) {
+    if (++s == stages) {
+      s = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // The producer lane: streams the CTA's row tiles into the ring.
 __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, uint64_t* bars,
                                             volatile int* abort_flag, uint8_t* ring) {
@@ -206,10 +219,11 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
   const uint8_t* S_c = p.sfa + (g.ea * p.M + g.m0) * K16;
   int issued = 0;
   bool ok = true;
-  for (int T = 0; T < g.NT; ++T) {
-    const int s = T % NS;
-    if (T >= NS &&
-        !mbar_wait_bounded(smem_addr(&bars[NS + s]), ((T / NS) - 1) & 1, kWaitLimitNs)) {
+  RingPos rp;
+  for (int T = 0; T < g.NT; ++T, rp.advance(NS)) {
+    const int s = rp.s;
+    // stage s was last filled in the previous round: wait until its consumers released it
+    if (T >= NS && !mbar_wait_bounded(smem_addr(&bars[NS + s]), rp.phase ^ 1u, kWaitLimitNs)) {
       ok = false;
       break;
     }
@@ -234,11 +248,12 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
   }
 }
 
-// Consumer wait for tile T; the verdict is voted so the whole warp leaves together.
+// Consumer wait for the tile at ring position r; the verdict is voted so the whole warp leaves
+// together.
 __device__ __forceinline__ bool tma_consume_wait(const TmaArgs& p, uint64_t* bars,
-                                                 volatile int* abort_flag, int T, int lane) {
-  const bool ready =
-      mbar_wait_bounded(smem_addr(&bars[T % p.stages]), (T / p.stages) & 1, kWaitLimitNs);
+                                                 volatile int* abort_flag, const RingPos& r,
+                                                 int lane) {
+  const bool ready = mbar_wait_bounded(smem_addr(&bars[r.s]), r.phase, kWaitLimitNs);
   if (!__all_sync(kFullMask, ready && *abort_flag == 0)) {
     if (lane == 0) *abort_flag = 1;
     return false;
@@ -246,9 +261,10 @@ __device__ __forceinline__ bool tma_consume_wait(const TmaArgs& p, uint64_t* bar
   return true;
 }
 
-__device__ __forceinline__ void tma_release(const TmaArgs& p, uint64_t* bars, int T, int lane) {
+__device__ __forceinline__ void tma_release(const TmaArgs& p, uint64_t* bars, const RingPos& r,
+                                            int lane) {
   __syncwarp();
-  if (lane == 0) mbar_arrive(smem_addr(&bars[p.stages + T % p.stages]));
+  if (lane == 0) mbar_arrive(smem_addr(&bars[p.stages + r.s]));
 }
 
 __device__ __forceinline__ void tma_epilogue(const TmaArgs& p, const TmaCta& g, const float* part,
@@ -320,10 +336,11 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
   const uint32_t bsw[4] = {16u * (0u ^ x), 16u * (1u ^ x), 16u * (2u ^ x), 16u * (3u ^ x)};
   const int rg0 = cw / nseg, sg0 = cw - rg0 * nseg;
   float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-  for (int T = 0; T < g.NT; ++T) {
-    if (!tma_consume_wait(p, bars, abort_flag, T, lane)) break;
+  RingPos rp;
+  for (int T = 0; T < g.NT; ++T, rp.advance(p.stages)) {
+    if (!tma_consume_wait(p, bars, abort_flag, rp, lane)) break;
     const int rows_t = min(p.tile_rows, g.n - T * p.tile_rows);
-    const uint32_t stA = ring32 + (uint32_t)(T % p.stages) * p.stage_bytes;
+    const uint32_t stA = ring32 + (uint32_t)rp.s * p.stage_bytes;
     const uint32_t stS = stA + p.sfa_off;
     float* part_tile = part + (size_t)T * p.tile_rows * p.slots;
     const int rgs = (rows_t + 3) >> 2;
@@ -369,7 +386,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
       }
     }
     if (cur >= 0) tma_flush(acc, lane, 4 * cur, rows_t, part_tile, p.slots, cw);
-    tma_release(p, bars, T, lane);
+    tma_release(p, bars, rp, lane);
   }
   named_barrier(1, (uint32_t)cthreads);
   tma_epilogue(p, g, part, abort_flag);
@@ -453,11 +470,18 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
 
   const uint32_t ring32 = smem_addr(ring);
   const uint32_t K2u = (uint32_t)K2, K16u = (uint32_t)K16;
-  for (int T = 0; T < g.NT; ++T) {
-    if (!tma_consume_wait(p, bars, abort_flag, T, lane)) break;
+  uint32_t lane_a[NSW], lane_s[NSW];  // this lane's byte offsets inside a row, per segment
+#pragma unroll
+  for (int j = 0; j < NSW; ++j) {
+    lane_a[j] = (uint32_t)seg[j] * 512u + 16u * lane;
+    lane_s[j] = (uint32_t)seg[j] * 64u + 2u * lane;
+  }
+  RingPos rp;
+  for (int T = 0; T < g.NT; ++T, rp.advance(p.stages)) {
+    if (!tma_consume_wait(p, bars, abort_flag, rp, lane)) break;
     const int rows_t = min(p.tile_rows, g.n - T * p.tile_rows);
     const int rgs = (rows_t + 3) >> 2;
-    const uint32_t stA = ring32 + (uint32_t)(T % p.stages) * p.stage_bytes;
+    const uint32_t stA = ring32 + (uint32_t)rp.s * p.stage_bytes;
     const uint32_t stS = stA + p.sfa_off;
     float* part_tile = part + (size_t)T * p.tile_rows * p.slots;
     for (int rg = rg_first; rg < rgs; rg += rg_step) {
@@ -465,27 +489,26 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t r = (uint32_t)min(4 * rg + i, rows_t - 1);  // re-read the last row
-        aoff[i] = stA + r * K2u + 16u * lane;
-        soff[i] = stS + r * K16u + 2u * lane;
+        aoff[i] = stA + r * K2u;
+        soff[i] = stS + r * K16u;
       }
       float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
       for (int j = 0; j < NSW; ++j) {
         if (live[j]) {
-          const uint32_t so = (uint32_t)seg[j];
           uint4 av[4];
           uint16_t sv[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            av[i] = lds_v4(aoff[i] + so * 512u);
-            sv[i] = lds_u16(soff[i] + so * 64u);
+            av[i] = lds_v4(aoff[i] + lane_a[j]);
+            sv[i] = lds_u16(soff[i] + lane_s[j]);
           }
           item_compute4(av, sv, bw[j], sb[j], acc);
         }
       }
       tma_flush(acc, lane, 4 * rg, rows_t, part_tile, p.slots, slot);
     }
-    tma_release(p, bars, T, lane);
+    tma_release(p, bars, rp, lane);
   }
   named_barrier(1, (uint32_t)cthreads);
   tma_epilogue(p, g, part, abort_flag);
