@@ -24,7 +24,7 @@ from .build import LIB_PATH
 
 __all__ = [
     "NVFP4Error", "Plan", "KERNEL_AUTO", "KERNEL_SIMPLE", "KERNEL_STREAM", "KERNEL_TMA",
-    "KERNEL_TMA_RV", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "FLAG_QUANTIZE_IN_GEMV",
+    "KERNEL_TMA_RV", "KERNEL_TC", "nvfp4_gemm_small_n", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "FLAG_QUANTIZE_IN_GEMV",
     "ROUND_HALF_STEP_TABLE",
     "ROUND_NEAREST_EVEN", "nvfp4_quantize_activation", "nvfp4_gemv_batched_bf16", "OUT_F16",
     "OUT_BF16", "nvfp4_gemv_grouped", "library_path",
@@ -32,7 +32,7 @@ __all__ = [
     "nvfp4_max_stream_k", "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version", "gemv",
 ]
 
-KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV = 0, 1, 2, 3, 4
+KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV, KERNEL_TC = 0, 1, 2, 3, 4, 5
 FLAG_EARLY_WEIGHTS, FLAG_NO_PDL, FLAG_QUANTIZE_IN_GEMV = 1, 2, 4
 ROUND_HALF_STEP_TABLE, ROUND_NEAREST_EVEN = 0, 1
 OUT_F16, OUT_BF16 = 0, 1
@@ -91,6 +91,9 @@ def load_library():
     lib.nvfp4_gemv_grouped.argtypes = [u8p, u8p, vp, u8p, u8p, vp, vp, vp, u16p, ctypes.c_int,
                                        i64, i64, i64, i64, vp, ctypes.POINTER(Plan)]
     lib.nvfp4_gemv_grouped.restype = ctypes.c_int
+    lib.nvfp4_gemm_small_n.argtypes = [u8p, u8p, f32, u8p, u8p, f32, u16p, i64, i64, i64, vp,
+                                       ctypes.POINTER(Plan)]
+    lib.nvfp4_gemm_small_n.restype = ctypes.c_int
     lib.nvfp4_gemv_plan.argtypes = [i64, i64, i64, ctypes.POINTER(Plan)]
     lib.nvfp4_gemv_plan.restype = ctypes.c_int
     lib.nvfp4_max_stream_k.argtypes = []
@@ -337,3 +340,23 @@ def nvfp4_gemv_grouped(A, sfa, g_a, b, sfb, g_b, c, M, K, E, T, expert_offsets=N
         _check(load_library().nvfp4_gemv_grouped(
             pA, pSA, pga, pB, pSB, pgb, po, pm, pC, int(out_dtype), M, K, E, T, h,
             ctypes.byref(pl) if pl is not None else None))
+
+
+def nvfp4_gemm_small_n(A, sfa, g_a, b, sfb, g_b, c, M, K, N, stream=None, plan=None):
+    """c[n][m] for N vectors b [N][K/2] sharing one matrix A [M][K/2] (tensor cores when they
+    can take the shape)."""
+    pl = None
+    if plan is not None:
+        pl = Plan(**plan) if isinstance(plan, dict) else plan
+    M, K, N = int(M), int(K), int(N)
+    ok = M > 0 and K > 0 and N > 0 and K % 16 == 0
+    with _on_device([A, sfa, b, sfb, c]):
+        pA = _ptr("A", A, M * K // 2 if ok else 0)
+        pSA = _ptr("sfa", sfa, M * K // 16 if ok else 0)
+        pB = _ptr("b", b, N * K // 2 if ok else 0)
+        pSB = _ptr("sfb", sfb, N * K // 16 if ok else 0)
+        pC = _ptr("c", c, 2 * M * N if ok else 0)
+        h = _stream_handle(stream, [A, sfa, b, sfb, c])
+        _check(load_library().nvfp4_gemm_small_n(pA, pSA, ctypes.c_float(g_a), pB, pSB,
+                                                 ctypes.c_float(g_b), pC, M, K, N, h,
+                                                 ctypes.byref(pl) if pl is not None else None))

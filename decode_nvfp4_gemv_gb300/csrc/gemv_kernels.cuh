@@ -34,6 +34,8 @@ struct Groups {
   const float* g_a;          // [E]
   const float* g_b;          // [E]
   int32_t E;
+  int32_t shared_a;          // 1: every batch reads the one matrix A (the batches are N tokens
+                             // sharing the weights), with the call's g_a and g_b
 };
 
 // Expert of batch l, or -1; called by all 32 lanes of a warp (the counts are a warp reduction).
@@ -65,7 +67,7 @@ __global__ void __launch_bounds__(256) gemv_simple_kernel(
   for (int64_t row = blockIdx.x * warps_per_cta + (threadIdx.x >> 5); row < n_rows;
        row += (int64_t)gridDim.x * warps_per_cta) {
     const int64_t l = row / M;
-    int64_t a_index = row;  // row of A (and of sfa) this output row reads
+    int64_t a_index = G.shared_a ? row - l * M : row;  // row of A (and of sfa) this row reads
     float ga = g_a, gb = g_b;
     if (G.E > 0) {
       const int e = group_of_batch(G, l, lane);
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(512) gemv_stream_kernel(const StreamArgs p) {
   const int64_t pi = blockIdx.x - l * p.P;
   const int64_t m0 = (p.M * pi) / p.P, m1 = (p.M * (pi + 1)) / p.P;
   const int n = (int)(m1 - m0);
-  int64_t ea = l;  // which matrix of A this CTA reads
+  int64_t ea = p.G.shared_a ? 0 : l;  // which matrix of A this CTA reads
   float ga = p.g_a, gb = p.g_b;
   if (p.G.E > 0) {  // grouped: every warp finds the same expert (the offsets do not change)
     const int e = group_of_batch(p.G, l, lane);

@@ -1,0 +1,385 @@
+// Small-N NVFP4 GEMM / GEMV on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+//   c[l][n][m] = fp16(g_a * g_b * sum_k e2m1(A_l[m][k]) e2m1(b_l[n][k]) e4m3(sfa_l[m][k/16]) e4m3(sfb_l[n][k/16]))
+//
+// "nvFP4 Batch GEMV算子系列(下)", sections on torch._scaled_mm and the Blackwell tensor memory:
+// the tensor cores take E2M1 operands with one E4M3 scale per 16 elements (block_scale,
+// scale_vec::4X) and apply the scales inside the MMA, accumulating in fp32 in tensor memory
+// (TMEM).  Here one instruction multiplies a 128-row x 64-element tile of A by a 16-column x 64-
+// element tile of tokens; the tokens are the N <= 16 vectors that share A (a decode batch), or a
+// single vector per batch (the batched GEMV, N = 1, columns 1..15 are zeros).
+//
+// Decomposition.  Output tiles of 128 rows; K is cut into S slices (a cluster of S CTAs along K)
+// so that tiles x S CTAs fill the GPU.  CTA (l, tile, s) streams its rows' K slice in chunks of
+// 256 elements (128 bytes per row) through an NS-stage shared-memory ring:
+//   warp 0      producer: per chunk, four TMA tensor copies (A rows 128 B wide with the 128-byte
+//               swizzle the MMA reads, the tokens' 128 B, and both tiles' 16 scale bytes per row)
+//               completing the stage's `full` mbarrier;
+//   warp 1      allocates TMEM and issues, per chunk, four tcgen05.mma (K = 64 each) whose
+//               completion (tcgen05.commit) frees the stage;
+//   warps 2..5  copy each stage's scale bytes from shared memory into TMEM (tcgen05.st; each warp
+//               owns its TMEM lane quadrant), then read the accumulator for the epilogue.
+// With S > 1 the CTAs of a cluster leave their fp32 partial tiles in their own shared memory and
+// CTA s sums the slice of rows it owns over all S partials in rank order (distributed shared
+// memory), so the result is deterministic and no global workspace is used.
+//
+// Tensor memory layout (32-bit columns; row m of a tile lives in TMEM lane m):
+//   columns 0..15                 accumulator D[m][n]
+//   columns 32 + 32 s + 4 j + q   stage s, MMA step j: A's four block scales (one byte each) of
+//                                 row 32 q + r at lane r of quadrant 0, of the lane's own row at
+//                                 q = 0 and at q = the lane's quadrant elsewhere (the arrangement
+//                                 that the blocked 32 x 4 scale layout and a lane-per-row reading
+//                                 both describe)
+//   columns 48 + 32 s + 4 j + q   stage s, step j: the tokens' block scales, token r at lane r of
+//                                 every quadrant, all four q
+//
+// Bounded waits: every mbarrier wait gives up after one second; a CTA that gives up writes NaN for
+// its outputs (its partial, under split K).  Programmatic dependent launch as in the TMA kernels.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "gemv_tma.cuh"
+#include "nvfp4_device.cuh"
+
+namespace nvfp4 {
+
+constexpr int kTcRows = 128;          // MMA M
+constexpr int kTcCols = 16;           // MMA N (tokens, zero-padded)
+constexpr int kTcChunkBytes = 128;    // bytes of a row per ring stage (256 elements)
+constexpr int kTcMaxStages = 6;
+constexpr int kTcThreads = 192;       // producer, MMA, 4 scale / epilogue warps
+constexpr uint32_t kTcTmemCols = 256;
+// stage layout (bytes, every part 1024-aligned): A 128 x 128, tokens 16 x 128, sfa 128 x 16,
+// sfb 16 x 16
+constexpr uint32_t kTcOffB = 16384, kTcOffSA = 18432, kTcOffSB = 20480, kTcStageBytes = 21504;
+constexpr uint32_t kTcHeaderBytes = 1024;  // barriers, TMEM address, abort flag
+
+struct TcArgs {
+  uint16_t* c;
+  float g_a, g_b;
+  int64_t M;          // rows per batch
+  int32_t K;          // elements (K % 256 == 0)
+  int32_t L;          // batches
+  int32_t N;          // tokens per batch (1 .. 16)
+  int32_t tiles;      // ceil(M / 128)
+  int32_t S;          // K slices = cluster size
+  int32_t chunks;     // K / 256
+  int32_t stages;     // NS
+  int32_t a_rows_per_batch;   // M for the batched GEMV (A_l = rows l*M ..), 0 when A is shared
+  int32_t early_weights;
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored with the 128-byte swizzle
+// (rows of 128 bytes, 8-row atoms 1024 bytes apart; tcgen05 descriptor version 1).
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024u >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor: E2M1 x E2M1, E4M3 scales, K-major operands, N = 16, M = 128.
+constexpr uint32_t kTcIdesc =
+    (1u << 7) | (1u << 10) | ((uint32_t)(kTcCols >> 3) << 17) | ((uint32_t)(kTcRows >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa,
+                                       uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+      " [%0], %1, %2, %6, [%3], [%4], p;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(sfa), "r"(sfb), "r"(accumulate), "r"(kTcIdesc)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};"
+      ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+        "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+        "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// ---------------------------------------------------------------- the kernel
+// Header (shared memory, first kTcHeaderBytes of the 1024-aligned window): full[NS], ready[NS],
+// empty[NS], done (8 bytes each), then the TMEM base address and the abort flag.
+struct TcHeader {
+  uint64_t full[kTcMaxStages];
+  uint64_t ready[kTcMaxStages];
+  uint64_t empty[kTcMaxStages];
+  uint64_t done;
+  uint32_t tmem;
+  int32_t abort;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
+    const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
+    const __grid_constant__ CUtensorMap mSA, const __grid_constant__ CUtensorMap mSB,
+    const TcArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-aligned window (the 128-byte swizzle atoms and the MMA descriptors assume it)
+  const uint32_t raw32 = smem_addr(smem_raw);
+  const uint32_t base32 = (raw32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base32 - raw32);
+  TcHeader* h = reinterpret_cast<TcHeader*>(base);
+  const uint32_t ring32 = base32 + kTcHeaderBytes;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int NS = p.stages;
+
+  // CTA coordinates: blockIdx.x = (l * tiles + tile) * S + slice
+  const int slice = (int)(blockIdx.x % p.S);
+  const int lt = (int)(blockIdx.x / p.S);
+  const int l = lt / p.tiles, tile = lt - l * p.tiles;
+  const int per = (p.chunks + p.S - 1) / p.S;
+  const int c0 = slice * per, nloc = max(0, min(p.chunks, c0 + per) - c0);
+  const int a_row0 = l * p.a_rows_per_batch + tile * kTcRows;
+  const int b_row0 = l * p.N;
+
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_addr(&h->tmem)), "n"(kTcTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_addr(&h->full[s]), 1);
+      mbar_init(smem_addr(&h->ready[s]), 128);
+      mbar_init(smem_addr(&h->empty[s]), 1);
+    }
+    mbar_init(smem_addr(&h->done), 1);
+    h->abort = 0;
+    mbar_init_fence();
+  }
+  // token rows N .. 15 of every stage are never written by the copies: zero them once
+  for (int i = tid; i < NS * (kTcCols - p.N) * 32; i += kTcThreads) {
+    const int s = i / ((kTcCols - p.N) * 32), rem = i - s * (kTcCols - p.N) * 32;
+    reinterpret_cast<uint32_t*>(base + kTcHeaderBytes + s * kTcStageBytes + kTcOffB +
+                                p.N * kTcChunkBytes)[rem] = 0u;
+  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_launch_dependents();
+  const uint32_t tmem = h->tmem;
+  volatile int32_t* abort_flag = &h->abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint32_t bytes = kTcRows * kTcChunkBytes + (uint32_t)p.N * kTcChunkBytes +
+                             kTcRows * 16u + (uint32_t)p.N * 16u;
+      const int pre = p.early_weights ? min(NS, nloc) : 0;
+      // with static weights the first stages' A and sfa copies start before the launch wait
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t st = ring32 + i * kTcStageBytes, full = smem_addr(&h->full[i]);
+        mbar_arrive_expect_tx(full, bytes);
+        tma_load_2d(st, &mA, (c0 + i) * kTcChunkBytes, a_row0, full);
+        tma_load_2d(st + kTcOffSA, &mSA, (c0 + i) * 16, a_row0, full);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t st = ring32 + i * kTcStageBytes, full = smem_addr(&h->full[i]);
+        tma_load_2d(st + kTcOffB, &mB, (c0 + i) * kTcChunkBytes, b_row0, full);
+        tma_load_2d(st + kTcOffSB, &mSB, (c0 + i) * 16, b_row0, full);
+      }
+      RingPos rp;
+      int issued = 0;
+      for (int i = 0; i < nloc; ++i, rp.advance(NS)) {
+        if (i < pre) {
+          issued = i + 1;
+          continue;
+        }
+        if (i >= NS &&
+            !mbar_wait_bounded(smem_addr(&h->empty[rp.s]), rp.phase ^ 1u, kWaitLimitNs)) {
+          *abort_flag = 1;
+          break;
+        }
+        if (*abort_flag) break;
+        const uint32_t st = ring32 + rp.s * kTcStageBytes, full = smem_addr(&h->full[rp.s]);
+        const int x = (c0 + i) * kTcChunkBytes, xs = (c0 + i) * 16;
+        mbar_arrive_expect_tx(full, bytes);
+        tma_load_2d(st, &mA, x, a_row0, full);
+        tma_load_2d(st + kTcOffB, &mB, x, b_row0, full);
+        tma_load_2d(st + kTcOffSA, &mSA, xs, a_row0, full);
+        tma_load_2d(st + kTcOffSB, &mSB, xs, b_row0, full);
+        issued = i + 1;
+      }
+      // every copy issued lands before the CTA may exit
+      for (int i = max(0, issued - NS); i < issued; ++i)
+        mbar_wait_bounded(smem_addr(&h->full[i % NS]), (uint32_t)(i / NS) & 1u, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      RingPos rp;
+      for (int i = 0; i < nloc; ++i, rp.advance(NS)) {
+        if (!mbar_wait_bounded(smem_addr(&h->ready[rp.s]), rp.phase, kWaitLimitNs) ||
+            *abort_flag) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = ring32 + rp.s * kTcStageBytes;
+        const uint32_t sfa_col = tmem + 32u + 32u * rp.s, sfb_col = sfa_col + 16u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tc_mma(tmem, tc_desc_sw128(st + 32u * j), tc_desc_sw128(st + kTcOffB + 32u * j),
+                 sfa_col + 4u * j, sfb_col + 4u * j, (i > 0 || j > 0) ? 1u : 0u);
+        tc_commit(smem_addr(&h->empty[rp.s]));
+      }
+      tc_commit(smem_addr(&h->done));
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ scales into TMEM
+    const uint32_t q = (uint32_t)warp & 3u;            // this warp's TMEM lane quadrant
+    const uint32_t lane_addr = (32u * q) << 16;
+    RingPos rp;
+    for (int i = 0; i < nloc; ++i, rp.advance(NS)) {
+      const bool ok = mbar_wait_bounded(smem_addr(&h->full[rp.s]), rp.phase, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, ok && *abort_flag == 0)) {
+        if (lane == 0) *abort_flag = 1;
+        break;
+      }
+      const uint8_t* st = base + kTcHeaderBytes + rp.s * kTcStageBytes;
+      uint4 rows[4];  // the 16 scale bytes of rows 32 c + lane, c = 0..3 (word j = MMA step j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        rows[c] = *reinterpret_cast<const uint4*>(st + kTcOffSA + (32 * c + lane) * 16);
+      const uint4 own = q == 0 ? rows[0] : q == 1 ? rows[1] : q == 2 ? rows[2] : rows[3];
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t ow = j == 0 ? own.x : j == 1 ? own.y : j == 2 ? own.z : own.w;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 r = rows[c];
+          const uint32_t rw = j == 0 ? r.x : j == 1 ? r.y : j == 2 ? r.z : r.w;
+          v[4 * j + c] = c == 0 ? ow : rw;
+        }
+      }
+      tc_st16(tmem + lane_addr + 32u + 32u * rp.s, v);
+      uint4 tb = make_uint4(0u, 0u, 0u, 0u);
+      if (lane < p.N) tb = *reinterpret_cast<const uint4*>(st + kTcOffSB + lane * 16);
+      uint32_t u[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w = j == 0 ? tb.x : j == 1 ? tb.y : j == 2 ? tb.z : tb.w;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) u[4 * j + c] = w;
+      }
+      tc_st16(tmem + lane_addr + 48u + 32u * rp.s, u);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      mbar_arrive(smem_addr(&h->ready[rp.s]));
+    }
+  }
+
+  // ------------------------------------------------------------ epilogue
+  pdl_wait();  // every thread that may write c waits for the preceding work
+  if (warp >= 2) {
+    const uint32_t q = (uint32_t)warp & 3u;
+    const bool fin = mbar_wait_bounded(smem_addr(&h->done), 0u, kWaitLimitNs);
+    tc_fence_after();
+    uint32_t d[16];
+    tc_ld16(tmem + ((32u * q) << 16), d);
+    const bool failed = !__all_sync(0xffffffffu, fin) || *abort_flag != 0;
+    const int rr = (int)(32u * q) + lane;  // row of the tile (TMEM lane)
+    if (p.S == 1) {
+      const int64_t m = (int64_t)tile * kTcRows + rr;
+      if (m < p.M) {
+#pragma unroll
+        for (int n = 0; n < kTcCols; ++n)
+          if (n < p.N)
+            p.c[(int64_t)(l * p.N + n) * p.M + m] =
+                failed ? (uint16_t)0x7E00
+                       : f32_to_f16_bits((__uint_as_float(d[n]) * p.g_a) * p.g_b);
+      }
+    } else {
+      // this CTA's fp32 partial, row-major [128][16], in the (now idle) first ring stage
+      float* red = reinterpret_cast<float*>(base + kTcHeaderBytes);
+#pragma unroll
+      for (int n = 0; n < 16; ++n)
+        red[rr * 16 + n] = failed ? __int_as_float(0x7fc00000) : __uint_as_float(d[n]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (p.S > 1) {
+    cluster_sync_all();  // every partial of the cluster is in place
+    const int r0 = slice * kTcRows / p.S, r1 = (slice + 1) * kTcRows / p.S;
+    for (int idx = tid; idx < (r1 - r0) * p.N; idx += kTcThreads) {
+      const int rr = r0 + idx / p.N, n = idx - (idx / p.N) * p.N;
+      const int64_t m = (int64_t)tile * kTcRows + rr;
+      float v = 0.f;
+      for (int r = 0; r < p.S; ++r) v += ld_cluster_f32(ring32 + (uint32_t)(rr * 16 + n) * 4u, r);
+      if (m < p.M) p.c[(int64_t)(l * p.N + n) * p.M + m] = f32_to_f16_bits((v * p.g_a) * p.g_b);
+    }
+    cluster_sync_all();  // no CTA leaves while its partial may still be read
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(kTcTmemCols) : "memory");
+  }
+}
+
+}  // namespace nvfp4

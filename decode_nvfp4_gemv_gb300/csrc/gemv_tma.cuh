@@ -164,7 +164,7 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
   g.n = (int)(m1 - g.m0);
   g.NT = (g.n + p.tile_rows - 1) / p.tile_rows;
   g.Wc = (blockDim.x >> 5) - 1;
-  g.ea = g.l;
+  g.ea = p.G.shared_a ? 0 : g.l;
   g.ga = p.g_a;
   g.gb = p.g_b;
   g.skip = false;

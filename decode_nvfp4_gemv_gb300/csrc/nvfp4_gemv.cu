@@ -1,5 +1,7 @@
 // C ABI of the NVFP4 batched GEMV (declared in include/nvfp4_gemv.h): argument validation, the
 // launch planner and the launches.  Nothing here allocates, synchronizes or reads device memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <stdarg.h>
@@ -12,6 +14,7 @@
 
 #include "../../include/nvfp4_gemv.h"
 #include "gemv_kernels.cuh"
+#include "gemv_tc.cuh"
 #include "gemv_tma.cuh"
 
 namespace {
@@ -41,6 +44,7 @@ struct DeviceInfo {
   int max_smem_optin = 0;   // bytes of shared memory one CTA may opt into
   int max_smem_sm = 0;      // bytes of shared memory per SM
   int pageable_access = 0;  // the device can read pageable host memory
+  PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;  // driver's tensor-map encoder
 };
 
 std::once_flag g_dev_once[kMaxDevices];
@@ -82,10 +86,20 @@ void init_device(int dev) {
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, false>, d.max_smem_optin)) ||
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false>, d.max_smem_optin)) ||
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, true>, d.max_smem_optin)) ||
-      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, true>, d.max_smem_optin))) {
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, true>, d.max_smem_optin)) ||
+      (e = cudaFuncSetAttribute(nvfp4::gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                d.max_smem_optin))) {
     d.err = e;
     return;
   }
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    d.encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  else
+    cudaGetLastError();
 }
 
 int current_device(const DeviceInfo** out) {
@@ -396,8 +410,57 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
 }
 
 // Fills every field of *pl for (M, K, L); `forced` fields (non-zero) are honoured or rejected.
+// Tensor-core kernel: 128-row output tiles, K cut into S slices (a cluster of S CTAs) so that
+// groups x tiles x S CTAs fill the GPU at two CTAs per SM; NS ring stages of 256 K elements.
+constexpr int kTcDefaultStages = 5;
+
+// At least 80 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM: a third
+// would wait in its TMEM allocation.
+int64_t tc_smem_bytes(int64_t NS) {
+  return std::max<int64_t>(80 * 1024,
+                           1024 + nvfp4::kTcHeaderBytes + NS * nvfp4::kTcStageBytes);  // + 1024
+}                                                                                    // alignment
+
+int plan_tc(const DeviceInfo& d, int64_t M, int64_t K, int64_t groups, const nvfp4_plan& f,
+            nvfp4_plan* pl) {
+  if (K % 256 != 0)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tensor-core kernel needs K %% 256 == 0 (K=%lld)",
+                (long long)K);
+  if ((f.warps_per_cta && f.warps_per_cta != 4) || (f.tile_rows && f.tile_rows != 128))
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                "tensor-core kernel: 4 epilogue warps and 128-row tiles are fixed");
+  const int64_t NS = f.stages ? f.stages : kTcDefaultStages;
+  if (NS < 2 || NS > nvfp4::kTcMaxStages || tc_smem_bytes(NS) > d.max_smem_optin)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tensor-core kernel: stages must be 2..%d",
+                nvfp4::kTcMaxStages);
+  const int64_t tiles = ceil_div(M, (int64_t)nvfp4::kTcRows), chunks = K / 256;
+  int64_t S = f.k_split;
+  if (S == 0)
+    S = std::min<int64_t>(std::min<int64_t>(8, chunks),
+                          std::max<int64_t>(1, (2 * (int64_t)d.sms) /
+                                                   std::max<int64_t>(1, groups * tiles)));
+  if (S > 8 || S > chunks)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                "tensor-core kernel: K slices must be at most 8 and at most K/256 (S=%lld)",
+                (long long)S);
+  S = std::min<int64_t>(S, 8);
+  const int64_t per = ceil_div(chunks, S);
+  S = ceil_div(chunks, per);  // every slice gets at least one chunk
+  if (groups * tiles * S > (int64_t(1) << 31) - 1 || tiles > (int64_t(1) << 24))
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
+  pl->kernel = NVFP4_KERNEL_TC;
+  pl->rows_per_warp = 0;
+  pl->k_split = (int32_t)S;
+  pl->ctas_per_batch = (int32_t)(tiles * S);
+  pl->warps_per_cta = 4;
+  pl->tile_rows = nvfp4::kTcRows;
+  pl->stages = (int32_t)NS;
+  return NVFP4_OK;
+}
+
 int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan* forced,
-              nvfp4_plan* pl, bool aligned16 = true) {
+              nvfp4_plan* pl, bool aligned16 = true, int64_t tc_groups = -1) {
+  if (tc_groups < 0) tc_groups = L;
   nvfp4_plan f;
   memset(&f, 0, sizeof f);
   if (forced) f = *forced;
@@ -418,6 +481,7 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
     case NVFP4_KERNEL_STREAM: st = plan_stream(d, M, K, L, f, pl); break;
     case NVFP4_KERNEL_TMA: st = plan_tma(d, M, K, L, f, false, pl); break;
     case NVFP4_KERNEL_TMA_RV: st = plan_tma(d, M, K, L, f, true, pl); break;
+    case NVFP4_KERNEL_TC: st = plan_tc(d, M, K, tc_groups, f, pl); break;
     case NVFP4_KERNEL_AUTO: {
       // the TMA ring (vector in registers if the warp mapping allows) when every CTA gets at least
       // 8 rows, else the stream kernel, else the simple kernel
@@ -454,6 +518,84 @@ struct FusedVector {
   uint8_t* sfb_out;
 };
 
+// ---------------------------------------------------------------- tensor-core launch
+int encode_map(const DeviceInfo& d, CUtensorMap* m, const void* base, uint64_t row_bytes,
+               uint64_t rows, uint32_t box_bytes, uint32_t box_rows, bool swizzle128) {
+  cuuint64_t dims[2] = {row_bytes, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_bytes, box_rows};
+  cuuint32_t elem[2] = {1, 1};
+  const CUresult r = d.encode_tiled(
+      m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, elem,
+      CU_TENSOR_MAP_INTERLEAVE_NONE,
+      swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(NVFP4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return NVFP4_OK;
+}
+
+// groups: independent (A, vectors) problems in one launch, each with N vectors; A is [groups][M]
+// rows when a_rows_per_batch == M (the batched GEMV), else one shared [M] matrix.
+int launch_tc(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const uint8_t* sfa,
+              float g_a, const uint8_t* b, const uint8_t* sfb, float g_b, uint16_t* c, int64_t M,
+              int64_t K, int64_t groups, int64_t N, int64_t a_rows_per_batch,
+              cudaStream_t stream) {
+  if (!d.encode_tiled)
+    return fail(NVFP4_ERR_CUDA, "the driver's tensor-map encoder is not available");
+  if (N < 1 || N > nvfp4::kTcCols)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tensor-core kernel: 1..16 vectors per launch");
+  const int64_t rowsA = a_rows_per_batch ? groups * M : M;
+  const int64_t kI32 = (int64_t(1) << 31) - 1;
+  if (rowsA > kI32 || groups * N > kI32 || K / 2 > kI32)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tensor-core kernel: coordinates exceed 2^31");
+  CUtensorMap mA, mB, mSA, mSB;
+  int st;
+  if ((st = encode_map(d, &mA, A, K / 2, rowsA, 128, nvfp4::kTcRows, true)) ||
+      (st = encode_map(d, &mSA, sfa, K / 16, rowsA, 16, nvfp4::kTcRows, false)) ||
+      (st = encode_map(d, &mB, b, K / 2, groups * N, 128, (uint32_t)N, true)) ||
+      (st = encode_map(d, &mSB, sfb, K / 16, groups * N, 16, (uint32_t)N, false)))
+    return st;
+  nvfp4::TcArgs a;
+  a.c = c;
+  a.g_a = g_a;
+  a.g_b = g_b;
+  a.M = M;
+  a.K = (int32_t)K;
+  a.L = (int32_t)groups;
+  a.N = (int32_t)N;
+  a.tiles = (int32_t)ceil_div(M, (int64_t)nvfp4::kTcRows);
+  a.S = pl.k_split;
+  a.chunks = (int32_t)(K / 256);
+  a.stages = pl.stages;
+  a.a_rows_per_batch = (int32_t)a_rows_per_batch;
+  a.early_weights = (pl.flags & NVFP4_FLAG_EARLY_WEIGHTS) ? 1 : 0;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3((unsigned)(groups * a.tiles * a.S));
+  cfg.blockDim = dim3(nvfp4::kTcThreads);
+  cfg.dynamicSmemBytes = (size_t)tc_smem_bytes(pl.stages);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (!(pl.flags & NVFP4_FLAG_NO_PDL)) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (a.S > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)a.S;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, nvfp4::gemv_tc_kernel, mA, mB, mSA, mSB, a);
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core kernel launch");
+  return NVFP4_OK;
+}
+
 // The grouped-form inputs of a launch (E == 0: the batched form) and the output type.
 struct GroupedOut {
   nvfp4::Groups G;
@@ -464,7 +606,6 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
            float g_a, const uint8_t* b, const uint8_t* sfb, float g_b, uint16_t* c, int64_t M,
            int64_t K, int64_t L, cudaStream_t stream, const FusedVector* fx = nullptr,
            const GroupedOut* go = nullptr) {
-  (void)d;
   const int threads = pl.warps_per_cta * 32;
   nvfp4::Groups G;
   memset(&G, 0, sizeof G);
@@ -472,6 +613,12 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
   if (go) {
     G = go->G;
     out_bf16 = go->out_bf16;
+  }
+  if (pl.kernel == NVFP4_KERNEL_TC) {
+    if (fx || G.E > 0 || G.shared_a || out_bf16)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                  "the tensor-core kernel takes packed vectors and fp16 output only");
+    return launch_tc(d, pl, A, sfa, g_a, b, sfb, g_b, c, M, K, L, 1, M, stream);
   }
   if (pl.kernel == NVFP4_KERNEL_SIMPLE) {
     const int64_t grid = std::min<int64_t>((int64_t)pl.ctas_per_batch * L, (int64_t(1) << 31) - 1);
@@ -726,9 +873,64 @@ int grouped_impl(const uint8_t* A, const uint8_t* sfa, const float* g_a, const u
   return launch(*d, pl, A, sfa, 1.f, b, sfb, 1.f, c, M, K, T, (cudaStream_t)stream, nullptr, &go);
 }
 
+// ---------------------------------------------------------------- small N (vectors share A)
+int small_n_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
+                 const uint8_t* sfb, float g_b, uint16_t* c, int64_t M, int64_t K, int64_t N,
+                 void* stream, const nvfp4_plan* forced) {
+  g_last_error[0] = '\0';
+  bool noop = false, aligned16 = true;
+  int st = check_args(A, sfa, b, sfb, c, M, K, N, &noop, &aligned16, 1);
+  if (st != NVFP4_OK || noop) return st;
+  if (forced && (forced->flags & NVFP4_FLAG_QUANTIZE_IN_GEMV))
+    return fail(NVFP4_ERR_INVALID_VALUE, "NVFP4_FLAG_QUANTIZE_IN_GEMV needs a bf16 vector");
+  const DeviceInfo* d = nullptr;
+  if ((st = current_device(&d)) != NVFP4_OK) return st;
+  if ((st = check_access(*d, A, "A")) || (st = check_access(*d, sfa, "sfa")) ||
+      (st = check_access(*d, b, "b")) || (st = check_access(*d, sfb, "sfb")) ||
+      (st = check_access(*d, c, "c")))
+    return st;
+  nvfp4_plan pl;
+  memset(&pl, 0, sizeof pl);
+  const bool automatic = !forced || forced->kernel == NVFP4_KERNEL_AUTO;
+  bool tc = false;
+  if (automatic && aligned16 && K % 256 == 0) {  // the tensor cores when they can take it
+    nvfp4_plan f;
+    memset(&f, 0, sizeof f);
+    if (forced) f = *forced;
+    f.kernel = NVFP4_KERNEL_TC;
+    char saved[sizeof g_last_error];
+    memcpy(saved, g_last_error, sizeof saved);
+    tc = make_plan(*d, M, K, std::min<int64_t>(N, nvfp4::kTcCols), &f, &pl, true, 1) == NVFP4_OK;
+    memcpy(g_last_error, saved, sizeof saved);
+  }
+  if (!tc) {
+    if ((st = make_plan(*d, M, K, N, forced, &pl, aligned16, 1)) != NVFP4_OK) return st;
+    tc = pl.kernel == NVFP4_KERNEL_TC;
+  }
+  if (tc) {  // groups of up to 16 vectors, one launch each
+    for (int64_t n0 = 0; n0 < N; n0 += nvfp4::kTcCols) {
+      const int64_t n = std::min<int64_t>(nvfp4::kTcCols, N - n0);
+      if ((st = launch_tc(*d, pl, A, sfa, g_a, b + n0 * (K / 2), sfb + n0 * (K / 16), g_b,
+                          c + n0 * M, M, K, 1, n, 0, (cudaStream_t)stream)))
+        return st;
+    }
+    return NVFP4_OK;
+  }
+  GroupedOut go;
+  memset(&go, 0, sizeof go);
+  go.G.shared_a = 1;
+  return launch(*d, pl, A, sfa, g_a, b, sfb, g_b, c, M, K, N, (cudaStream_t)stream, nullptr, &go);
+}
+
 }  // namespace
 
 extern "C" {
+
+int nvfp4_gemm_small_n(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
+                       const uint8_t* sfb, float g_b, uint16_t* c, int64_t M, int64_t K, int64_t N,
+                       void* stream, const nvfp4_plan* plan) {
+  return small_n_impl(A, sfa, g_a, b, sfb, g_b, c, M, K, N, stream, plan);
+}
 
 int nvfp4_gemv_batched(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
                        const uint8_t* sfb, float g_b, uint16_t* c, int64_t M, int64_t K, int64_t L,

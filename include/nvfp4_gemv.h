@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define NVFP4_ABI_VERSION 3
+#define NVFP4_ABI_VERSION 4
 
 typedef enum nvfp4_status {
   NVFP4_OK = 0,
@@ -85,9 +85,14 @@ typedef enum nvfp4_kernel {
                                split-K; needs K % 32 == 0 and K <= nvfp4_max_stream_k() */
   NVFP4_KERNEL_TMA = 3,     /* row tiles streamed into a shared-memory ring by bulk async copies
                                (TMA) and mbarriers, vector in shared memory; needs K % 256 == 0 */
-  NVFP4_KERNEL_TMA_RV = 4   /* as TMA with each consumer warp's vector slice held in registers;
+  NVFP4_KERNEL_TMA_RV = 4,  /* as TMA with each consumer warp's vector slice held in registers;
                                needs K % 256 == 0 and the warp count to divide the number of
                                1024-element K segments (or be a multiple of it) */
+  NVFP4_KERNEL_TC = 5       /* tensor cores (tcgen05.mma kind::mxf4nvf4, block scales applied by
+                               the MMA, fp32 accumulator in tensor memory): 128-row tiles x up to
+                               16 vectors, K split over a cluster of k_split (<= 8) CTAs with a
+                               deterministic on-chip reduction; needs K % 256 == 0 and
+                               non-negative block scales (the MMA reads them as unsigned E4M3) */
 } nvfp4_kernel;
 
 /* Plan flags. */
@@ -220,6 +225,25 @@ int nvfp4_gemv_grouped(const uint8_t* A, const uint8_t* sfa, const float* g_a, c
                        const uint8_t* sfb, const float* g_b, const int32_t* expert_offsets,
                        const int32_t* expert_of_token, uint16_t* c, int out_dtype, int64_t M,
                        int64_t K, int64_t E, int64_t T, void* stream, const nvfp4_plan* plan);
+
+/* ------------------------------------------------------------------------------------------
+ * Small-N GEMM: N vectors (a decode batch of tokens) that share one weight matrix.
+ * "nvFP4 Batch GEMV算子系列(下)", section pytorch实现: (m, k) @ (n, k)^T -> (m, n) with block
+ * scales, here for small n and without padding n to 128.
+ *
+ *   c[n][m] = fp16( g_a * g_b * sum_k e2m1(A[m][k]) e2m1(b[n][k]) e4m3(sfa[m][k/16]) e4m3(sfb[n][k/16]) )
+ *
+ * A [M][K/2], sfa [M][K/16] (one matrix), b [N][K/2], sfb [N][K/16], c [N][M] (fp16 bits).
+ * The automatic plan is the tensor-core kernel (NVFP4_KERNEL_TC, groups of up to 16 vectors per
+ * launch) when K % 256 == 0 and A, sfa, b, sfb are 16-byte aligned; otherwise, or with a forced
+ * CUDA-core plan, the batched kernels run one vector per batch, all batches reading A (L2 serves
+ * the repeats).  The TC kernel reads block scales as unsigned E4M3: they must be finite and
+ * non-negative.  Checks, statuses and ownership as for nvfp4_gemv_batched_ex with L = N (A holds
+ * one matrix); M == 0 or N == 0 enqueues nothing.
+ * ------------------------------------------------------------------------------------------ */
+int nvfp4_gemm_small_n(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
+                       const uint8_t* sfb, float g_b, uint16_t* c, int64_t M, int64_t K, int64_t N,
+                       void* stream, const nvfp4_plan* plan);
 
 /* NVFP4_ABI_VERSION of the built library. */
 int nvfp4_abi_version(void);

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_status_strings(lib):
     import decode_nvfp4_gemv_gb300 as pkg
 
-    assert pkg.nvfp4_abi_version() == 3
+    assert pkg.nvfp4_abi_version() == 4
     assert pkg.nvfp4_status_string(0) == "ok"
     assert pkg.nvfp4_status_string(2) == "misaligned pointer"
     assert pkg.nvfp4_status_string(99) == "unknown status"
