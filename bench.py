@@ -449,6 +449,89 @@ def time_general(pkg, w, stream, steps, warmup, dist, n_copies):
             "calls": calls, "GB/s": round(tot / slow / 1e9, 2), "frac": round(tot / slow / 1e9 / peak, 4)}
 
 
+def _graph_time(fn, stream, steps, warmup, dist, dev):
+    """Seconds and calls for `steps` calls of fn(i) replayed from CUDA graphs on `stream`."""
+    import torch
+
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 1)):
+            fn(i)
+    stream.synchronize()
+    chunk = min(GRAPH_CHUNK, steps)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(chunk):
+            fn(i)
+    reps = max(1, steps // chunk)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        barrier(dist)
+        torch.cuda.synchronize(dev)
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+    del g
+    return ev0.elapsed_time(ev1) / 1e3, reps * chunk
+
+
+def time_small_n(pkg, device, stream, steps, warmup, dist, M=7168, K=16384, Ns=(2, 8, 16)):
+    """N vectors sharing one weight matrix (a decode batch): the tensor-core kernel (automatic
+    plan) against the register-vector CUDA-core kernel reading A once per vector.  Bytes: A and
+    sfa once, the N vectors, the N output rows.  Weights rotate over copies larger than L2."""
+    import torch
+
+    w = workloads.random_workload(M, K, 1, seed=2, scale_bytes=workloads.pow2_scale_bytes(-3, 2))
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    ncp = max(2, -(-3 * l2 // (M * K * 9 // 16)) + 1)
+    As = [torch.from_numpy(w.A[0]).to(device) for _ in range(ncp)]
+    Ss = [torch.from_numpy(w.sfa[0]).to(device) for _ in range(ncp)]
+    peak, _ = measured_peak_gbs()
+    out = {"workload": f"M={M} K={K}, N vectors sharing A (rotated over {ncp} copies)"}
+    for N in Ns:
+        v = workloads.random_workload(1, K, N, seed=3)
+        b = torch.from_numpy(v.b).to(device)
+        sb = torch.from_numpy(v.sfb).to(device)
+        c = torch.empty((N, M), dtype=torch.float16, device=device)
+        byt = M * K * 9 // 16 + N * K * 9 // 16 + 2 * M * N
+        row = {}
+        for name, plan in (("tensor_cores", {"flags": FLAG_EARLY_WEIGHTS}),
+                           ("cuda_cores_rv", {"kernel": 4, "flags": FLAG_EARLY_WEIGHTS})):
+            def fn(i, plan=plan):
+                pkg.nvfp4_gemm_small_n(As[i % ncp], Ss[i % ncp], w.g_a, b, sb, w.g_b, c, M, K, N,
+                                       stream=stream, plan=plan)
+            sec, calls = _graph_time(fn, stream, steps, warmup, dist, device)
+            gbs = byt * calls / sec / 1e9
+            row[name] = {"us_per_call": round(sec / calls * 1e6, 3), "GB/s": round(gbs, 2),
+                         "frac": round(gbs / peak, 4)}
+        row["speedup"] = round(row["cuda_cores_rv"]["us_per_call"] /
+                               row["tensor_cores"]["us_per_call"], 2)
+        out[f"N={N}"] = row
+    return out
+
+
+def time_tc_n1(pkg, w, sets, outs, stream, steps, warmup, dist, device):
+    """The batched GEMV (N = 1 per batch) forced onto the tensor-core kernel, same inputs."""
+    n = len(sets)
+    plan = {"kernel": 5, "flags": FLAG_EARLY_WEIGHTS}
+
+    def fn(i):
+        s = sets[i % n]
+        pkg.nvfp4_gemv_batched_ex(s["A"], s["sfa"], w.g_a, s["b"], s["sfb"], w.g_b, outs[i % n],
+                                  w.M, w.K, w.L, stream=stream, plan=plan)
+    sec, calls = _graph_time(fn, stream, steps, warmup, dist, device)
+    gbs = w.algorithmic_bytes * calls / sec / 1e9
+    peak, _ = measured_peak_gbs()
+    return {"kernel": "gemv_tc_kernel", "us_per_call": round(sec / calls * 1e6, 3),
+            "GB/s": round(gbs, 2), "frac": round(gbs / peak, 4),
+            "plan": plan}
+
+
 def run_ours(args):
     import torch
 
@@ -532,6 +615,15 @@ def run_ours(args):
         bf16 = time_bf16_vector(pkg, w, sets, outs, stream, min(args.steps, 20000), args.warmup,
                                 dist)
 
+    tc_n1 = None
+    if not args.plan and not args.no_tc:
+        tc_n1 = time_tc_n1(pkg, w, sets, outs, stream, min(args.steps, 20000), args.warmup, dist,
+                           device)
+
+    small = None
+    if not args.plan and not args.no_tc:
+        small = time_small_n(pkg, device, stream, min(args.steps, 5000), args.warmup, dist)
+
     general = None
     if not args.plan and not args.no_general:
         general = time_general(pkg, w, stream, min(args.steps, 2000), args.warmup, dist, n_copies)
@@ -596,6 +688,10 @@ def run_ours(args):
             line["grouped"] = grouped
         if general is not None:
             line["general_unaligned"] = general
+        if tc_n1 is not None:
+            line["tensor_cores_n1"] = tc_n1
+        if small is not None:
+            line["small_n"] = small
         if e2e is not None:
             line["e2e"] = e2e
         if cpu is not None:
@@ -727,6 +823,8 @@ def main():
                     help="skip the grouped (mixture-of-experts) timing")
     ap.add_argument("--no-general", action="store_true",
                     help="skip the unaligned-input (byte-load kernel) timing")
+    ap.add_argument("--no-tc", action="store_true",
+                    help="skip the tensor-core timings (N = 1 and small N)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
