@@ -18,13 +18,17 @@
 //   warp 1      allocates TMEM and issues, per chunk, four tcgen05.mma (K = 64 each) whose
 //               completion (tcgen05.commit) frees the stage;
 //   warps 2..5  copy each stage's scale bytes from shared memory into TMEM (tcgen05.st; each warp
-//               owns its TMEM lane quadrant), then read the accumulator for the epilogue.
-// With S > 1 the CTAs of a cluster leave their fp32 partial tiles in their own shared memory and
-// CTA s sums the slice of rows it owns over all S partials in rank order (distributed shared
-// memory), so the result is deterministic and no global workspace is used.
+//               owns its TMEM lane quadrant);
+//   warps 6..9  epilogue: read the accumulator (tcgen05.ld) and store, while the MMAs of the next
+//               tile go to the other of two accumulator buffers.
+// With S == 1 a CTA is persistent over tiles u = blockIdx.x, blockIdx.x + gridDim.x, ... and its
+// ring streams across tile boundaries.  With S > 1 (one tile per cluster) every CTA sends each
+// row's fp32 partial to the CTA of the cluster that owns the row (distributed shared memory);
+// after one cluster barrier the owner sums the S partials in rank order, so the result is
+// deterministic and no global workspace is used.
 //
 // Tensor memory layout (32-bit columns; row m of a tile lives in TMEM lane m):
-//   columns 0..15                 accumulator D[m][n]
+//   columns 16 b .. 16 b + 15     accumulator buffer b (b = tile index mod 2), D[m][n]
 //   columns 32 + 32 s + 4 j + q   stage s, MMA step j: A's four block scales (one byte each) of
 //                                 row 32 q + r at lane r of quadrant 0, of the lane's own row at
 //                                 q = 0 and at q = the lane's quadrant elsewhere (the arrangement
@@ -49,12 +53,13 @@ constexpr int kTcRows = 128;          // MMA M
 constexpr int kTcCols = 16;           // MMA N (tokens, zero-padded)
 constexpr int kTcChunkBytes = 128;    // bytes of a row per ring stage (256 elements)
 constexpr int kTcMaxStages = 6;
-constexpr int kTcThreads = 192;       // producer, MMA, 4 scale / epilogue warps
+constexpr int kTcThreads = 320;       // producer, MMA, 4 scale warps, 4 epilogue warps
 constexpr uint32_t kTcTmemCols = 256;
 // stage layout (bytes, every part 1024-aligned): A 128 x 128, tokens 16 x 128, sfa 128 x 16,
 // sfb 16 x 16
 constexpr uint32_t kTcOffB = 16384, kTcOffSA = 18432, kTcOffSB = 20480, kTcStageBytes = 21504;
 constexpr uint32_t kTcHeaderBytes = 1024;  // barriers, TMEM address, abort flag
+constexpr uint32_t kTcRedBytes = 9216;     // split-K partials: S x ceil(128 / S) rows x 16 fp32
 
 struct TcArgs {
   uint16_t* c;
@@ -69,6 +74,8 @@ struct TcArgs {
   int32_t stages;     // NS
   int32_t a_rows_per_batch;   // M for the batched GEMV (A_l = rows l*M ..), 0 when A is shared
   int32_t early_weights;
+  int32_t total_tiles;        // L * tiles
+  uint32_t red_off;           // split-K partial buffer (bytes from the aligned window), S > 1
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -148,25 +155,62 @@ __device__ __forceinline__ void cluster_sync_all() {
                ::: "memory");
 }
 
-__device__ __forceinline__ float ld_cluster_f32(uint32_t local_addr, uint32_t rank) {
+// Stores four floats into the shared memory of cluster CTA `rank` at the offset of local_addr.
+__device__ __forceinline__ void st_cluster_v4(uint32_t local_addr, uint32_t rank, float a, float b,
+                                              float c, float d) {
   uint32_t remote;
-  float v;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- the kernel
-// Header (shared memory, first kTcHeaderBytes of the 1024-aligned window): full[NS], ready[NS],
-// empty[NS], done (8 bytes each), then the TMEM base address and the abort flag.
+// Header (start of the 1024-aligned window): per stage full / ready / empty, the two accumulator
+// buffers' full / empty, the TMEM base address and the abort flag.
 struct TcHeader {
   uint64_t full[kTcMaxStages];
   uint64_t ready[kTcMaxStages];
   uint64_t empty[kTcMaxStages];
-  uint64_t done;
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
   uint32_t tmem;
   int32_t abort;
 };
+
+// Work of one CTA: with S == 1 the tiles blockIdx.x, blockIdx.x + gridDim.x, ... (persistent,
+// the ring streams across tile boundaries and the accumulator is double-buffered); with S > 1
+// one tile, K slice blockIdx.x mod S.
+struct TcWork {
+  int slice, c0, nloc, u0, ustep, ntiles;
+};
+
+__device__ __forceinline__ TcWork tc_work(const TcArgs& p) {
+  TcWork w;
+  w.slice = p.S > 1 ? (int)(blockIdx.x % p.S) : 0;
+  const int per = (p.chunks + p.S - 1) / p.S;
+  w.c0 = w.slice * per;
+  w.nloc = min(p.chunks, w.c0 + per) - w.c0;
+  if (p.S > 1) {
+    w.u0 = (int)(blockIdx.x / p.S);
+    w.ustep = p.total_tiles;
+    w.ntiles = 1;
+  } else {
+    w.u0 = (int)blockIdx.x;
+    w.ustep = (int)gridDim.x;
+    w.ntiles = (p.total_tiles - w.u0 + w.ustep - 1) / w.ustep;
+  }
+  return w;
+}
+
+// First rows of tile u in the A and token tensors.
+__device__ __forceinline__ void tc_rows(const TcArgs& p, int u, int& l, int& tile, int& a_row0,
+                                        int& b_row0) {
+  l = u / p.tiles;
+  tile = u - l * p.tiles;
+  a_row0 = l * p.a_rows_per_batch + tile * kTcRows;
+  b_row0 = l * p.N;
+}
 
 __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
     const __grid_constant__ CUtensorMap mA, const __grid_constant__ CUtensorMap mB,
@@ -181,15 +225,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
   const uint32_t ring32 = base32 + kTcHeaderBytes;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NS = p.stages;
-
-  // CTA coordinates: blockIdx.x = (l * tiles + tile) * S + slice
-  const int slice = (int)(blockIdx.x % p.S);
-  const int lt = (int)(blockIdx.x / p.S);
-  const int l = lt / p.tiles, tile = lt - l * p.tiles;
-  const int per = (p.chunks + p.S - 1) / p.S;
-  const int c0 = slice * per, nloc = max(0, min(p.chunks, c0 + per) - c0);
-  const int a_row0 = l * p.a_rows_per_batch + tile * kTcRows;
-  const int b_row0 = l * p.N;
+  const TcWork w = tc_work(p);
+  const int npairs = w.ntiles * w.nloc;  // (tile, chunk) pairs this CTA streams
 
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -202,15 +239,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
       mbar_init(smem_addr(&h->ready[s]), 128);
       mbar_init(smem_addr(&h->empty[s]), 1);
     }
-    mbar_init(smem_addr(&h->done), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&h->acc_full[b]), 1);
+      mbar_init(smem_addr(&h->acc_empty[b]), 128);
+    }
     h->abort = 0;
     mbar_init_fence();
   }
   // token rows N .. 15 of every stage are never written by the copies: zero them once
-  for (int i = tid; i < NS * (kTcCols - p.N) * 32; i += kTcThreads) {
-    const int s = i / ((kTcCols - p.N) * 32), rem = i - s * (kTcCols - p.N) * 32;
+  const int zero_words = (kTcCols - p.N) * 32;
+  for (int i = tid; i < NS * zero_words; i += kTcThreads) {
+    const int s = i / zero_words;
     reinterpret_cast<uint32_t*>(base + kTcHeaderBytes + s * kTcStageBytes + kTcOffB +
-                                p.N * kTcChunkBytes)[rem] = 0u;
+                                p.N * kTcChunkBytes)[i - s * zero_words] = 0u;
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_before();
@@ -225,75 +266,96 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
     if (lane == 0) {
       const uint32_t bytes = kTcRows * kTcChunkBytes + (uint32_t)p.N * kTcChunkBytes +
                              kTcRows * 16u + (uint32_t)p.N * 16u;
-      const int pre = p.early_weights ? min(NS, nloc) : 0;
       // with static weights the first stages' A and sfa copies start before the launch wait
-      for (int i = 0; i < pre; ++i) {
-        const uint32_t st = ring32 + i * kTcStageBytes, full = smem_addr(&h->full[i]);
+      const int pre = p.early_weights ? min(NS, npairs) : 0;
+      for (int g = 0; g < pre; ++g) {
+        const int k = g / w.nloc, i = g - k * w.nloc;
+        int l, tile, ar, br;
+        tc_rows(p, w.u0 + k * w.ustep, l, tile, ar, br);
+        const uint32_t st = ring32 + g * kTcStageBytes, full = smem_addr(&h->full[g]);
         mbar_arrive_expect_tx(full, bytes);
-        tma_load_2d(st, &mA, (c0 + i) * kTcChunkBytes, a_row0, full);
-        tma_load_2d(st + kTcOffSA, &mSA, (c0 + i) * 16, a_row0, full);
+        tma_load_2d(st, &mA, (w.c0 + i) * kTcChunkBytes, ar, full);
+        tma_load_2d(st + kTcOffSA, &mSA, (w.c0 + i) * 16, ar, full);
       }
       pdl_wait();
-      for (int i = 0; i < pre; ++i) {
-        const uint32_t st = ring32 + i * kTcStageBytes, full = smem_addr(&h->full[i]);
-        tma_load_2d(st + kTcOffB, &mB, (c0 + i) * kTcChunkBytes, b_row0, full);
-        tma_load_2d(st + kTcOffSB, &mSB, (c0 + i) * 16, b_row0, full);
+      for (int g = 0; g < pre; ++g) {
+        const int k = g / w.nloc, i = g - k * w.nloc;
+        int l, tile, ar, br;
+        tc_rows(p, w.u0 + k * w.ustep, l, tile, ar, br);
+        const uint32_t st = ring32 + g * kTcStageBytes, full = smem_addr(&h->full[g]);
+        tma_load_2d(st + kTcOffB, &mB, (w.c0 + i) * kTcChunkBytes, br, full);
+        tma_load_2d(st + kTcOffSB, &mSB, (w.c0 + i) * 16, br, full);
       }
       RingPos rp;
       int issued = 0;
-      for (int i = 0; i < nloc; ++i, rp.advance(NS)) {
-        if (i < pre) {
-          issued = i + 1;
-          continue;
+      for (int g = 0, k = 0, i = 0; g < npairs; ++g, rp.advance(NS)) {
+        if (g >= pre) {
+          if (g >= NS &&
+              !mbar_wait_bounded(smem_addr(&h->empty[rp.s]), rp.phase ^ 1u, kWaitLimitNs)) {
+            *abort_flag = 1;
+            break;
+          }
+          if (*abort_flag) break;
+          int l, tile, ar, br;
+          tc_rows(p, w.u0 + k * w.ustep, l, tile, ar, br);
+          const uint32_t st = ring32 + rp.s * kTcStageBytes, full = smem_addr(&h->full[rp.s]);
+          const int x = (w.c0 + i) * kTcChunkBytes, xs = (w.c0 + i) * 16;
+          mbar_arrive_expect_tx(full, bytes);
+          tma_load_2d(st, &mA, x, ar, full);
+          tma_load_2d(st + kTcOffB, &mB, x, br, full);
+          tma_load_2d(st + kTcOffSA, &mSA, xs, ar, full);
+          tma_load_2d(st + kTcOffSB, &mSB, xs, br, full);
         }
-        if (i >= NS &&
-            !mbar_wait_bounded(smem_addr(&h->empty[rp.s]), rp.phase ^ 1u, kWaitLimitNs)) {
-          *abort_flag = 1;
-          break;
+        issued = g + 1;
+        if (++i == w.nloc) {
+          i = 0;
+          ++k;
         }
-        if (*abort_flag) break;
-        const uint32_t st = ring32 + rp.s * kTcStageBytes, full = smem_addr(&h->full[rp.s]);
-        const int x = (c0 + i) * kTcChunkBytes, xs = (c0 + i) * 16;
-        mbar_arrive_expect_tx(full, bytes);
-        tma_load_2d(st, &mA, x, a_row0, full);
-        tma_load_2d(st + kTcOffB, &mB, x, b_row0, full);
-        tma_load_2d(st + kTcOffSA, &mSA, xs, a_row0, full);
-        tma_load_2d(st + kTcOffSB, &mSB, xs, b_row0, full);
-        issued = i + 1;
       }
       // every copy issued lands before the CTA may exit
-      for (int i = max(0, issued - NS); i < issued; ++i)
-        mbar_wait_bounded(smem_addr(&h->full[i % NS]), (uint32_t)(i / NS) & 1u, kWaitLimitNs);
+      for (int g = max(0, issued - NS); g < issued; ++g)
+        mbar_wait_bounded(smem_addr(&h->full[g % NS]), (uint32_t)(g / NS) & 1u, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       RingPos rp;
-      for (int i = 0; i < nloc; ++i, rp.advance(NS)) {
-        if (!mbar_wait_bounded(smem_addr(&h->ready[rp.s]), rp.phase, kWaitLimitNs) ||
-            *abort_flag) {
+      for (int k = 0; k < w.ntiles; ++k) {
+        const uint32_t ab = (uint32_t)k & 1u;
+        bool ok = k < 2 || mbar_wait_bounded(smem_addr(&h->acc_empty[ab]),
+                                              (uint32_t)((k >> 1) - 1) & 1u, kWaitLimitNs);
+        tc_fence_after();
+        for (int i = 0; ok && i < w.nloc; ++i, rp.advance(NS)) {
+          if (!mbar_wait_bounded(smem_addr(&h->ready[rp.s]), rp.phase, kWaitLimitNs) ||
+              *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t st = ring32 + rp.s * kTcStageBytes;
+          const uint32_t sfa_col = tmem + 32u + 32u * rp.s, sfb_col = sfa_col + 16u;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tc_mma(tmem + 16u * ab, tc_desc_sw128(st + 32u * j),
+                   tc_desc_sw128(st + kTcOffB + 32u * j), sfa_col + 4u * j, sfb_col + 4u * j,
+                   (i > 0 || j > 0) ? 1u : 0u);
+          tc_commit(smem_addr(&h->empty[rp.s]));
+        }
+        tc_commit(smem_addr(&h->acc_full[ab]));  // also on failure, so the epilogue goes on
+        if (!ok) {
           *abort_flag = 1;
           break;
         }
-        tc_fence_after();
-        const uint32_t st = ring32 + rp.s * kTcStageBytes;
-        const uint32_t sfa_col = tmem + 32u + 32u * rp.s, sfb_col = sfa_col + 16u;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          tc_mma(tmem, tc_desc_sw128(st + 32u * j), tc_desc_sw128(st + kTcOffB + 32u * j),
-                 sfa_col + 4u * j, sfb_col + 4u * j, (i > 0 || j > 0) ? 1u : 0u);
-        tc_commit(smem_addr(&h->empty[rp.s]));
       }
-      tc_commit(smem_addr(&h->done));
     }
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ scales into TMEM
-    const uint32_t q = (uint32_t)warp & 3u;            // this warp's TMEM lane quadrant
+    const uint32_t q = (uint32_t)warp & 3u;  // this warp's TMEM lane quadrant
     const uint32_t lane_addr = (32u * q) << 16;
     RingPos rp;
-    for (int i = 0; i < nloc; ++i, rp.advance(NS)) {
+    for (int g = 0; g < npairs; ++g, rp.advance(NS)) {
       const bool ok = mbar_wait_bounded(smem_addr(&h->full[rp.s]), rp.phase, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok && *abort_flag == 0)) {
         if (lane == 0) *abort_flag = 1;
@@ -322,58 +384,80 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
       uint32_t u[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t w = j == 0 ? tb.x : j == 1 ? tb.y : j == 2 ? tb.z : tb.w;
+        const uint32_t x = j == 0 ? tb.x : j == 1 ? tb.y : j == 2 ? tb.z : tb.w;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) u[4 * j + c] = w;
+        for (int c = 0; c < 4; ++c) u[4 * j + c] = x;
       }
       tc_st16(tmem + lane_addr + 48u + 32u * rp.s, u);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       mbar_arrive(smem_addr(&h->ready[rp.s]));
     }
-  }
-
-  // ------------------------------------------------------------ epilogue
-  pdl_wait();  // every thread that may write c waits for the preceding work
-  if (warp >= 2) {
+  } else {
+    // ------------------------------------------------------------ epilogue
+    pdl_wait();  // c may be read or written by the preceding work
     const uint32_t q = (uint32_t)warp & 3u;
-    const bool fin = mbar_wait_bounded(smem_addr(&h->done), 0u, kWaitLimitNs);
-    tc_fence_after();
-    uint32_t d[16];
-    tc_ld16(tmem + ((32u * q) << 16), d);
-    const bool failed = !__all_sync(0xffffffffu, fin) || *abort_flag != 0;
     const int rr = (int)(32u * q) + lane;  // row of the tile (TMEM lane)
-    if (p.S == 1) {
-      const int64_t m = (int64_t)tile * kTcRows + rr;
-      if (m < p.M) {
+    const int rmax = (kTcRows + p.S - 1) / p.S;
+    for (int k = 0; k < w.ntiles; ++k) {
+      const uint32_t ab = (uint32_t)k & 1u;
+      bool fin = *abort_flag == 0 &&
+                 mbar_wait_bounded(smem_addr(&h->acc_full[ab]), (uint32_t)(k >> 1) & 1u,
+                                   kWaitLimitNs);
+      fin = __all_sync(0xffffffffu, fin);
+      tc_fence_after();
+      uint32_t d[16];
+      tc_ld16(tmem + ((32u * q) << 16) + 16u * ab, d);
+      tc_fence_before();
+      mbar_arrive(smem_addr(&h->acc_empty[ab]));
+      const bool failed = !fin || *abort_flag != 0;
+      int l, tile, ar, br;
+      tc_rows(p, w.u0 + k * w.ustep, l, tile, ar, br);
+      if (p.S == 1) {
+        const int64_t m = (int64_t)tile * kTcRows + rr;
+        if (m < p.M) {
 #pragma unroll
-        for (int n = 0; n < kTcCols; ++n)
-          if (n < p.N)
-            p.c[(int64_t)(l * p.N + n) * p.M + m] =
-                failed ? (uint16_t)0x7E00
-                       : f32_to_f16_bits((__uint_as_float(d[n]) * p.g_a) * p.g_b);
+          for (int n = 0; n < kTcCols; ++n)
+            if (n < p.N)
+              p.c[(int64_t)(l * p.N + n) * p.M + m] =
+                  failed ? (uint16_t)0x7E00
+                         : f32_to_f16_bits((__uint_as_float(d[n]) * p.g_a) * p.g_b);
+        }
+      } else {
+        // this row's partial goes to the CTA of the cluster that owns the row
+        int o = 0;
+        while (o + 1 < p.S && (o + 1) * kTcRows / p.S <= rr) ++o;
+        const int idx = rr - o * kTcRows / p.S;
+        const uint32_t dst = base32 + p.red_off + (uint32_t)((w.slice * rmax + idx) * 16) * 4u;
+        const float nan = __int_as_float(0x7fc00000);
+#pragma unroll
+        for (int n = 0; n < 16; n += 4)
+          st_cluster_v4(dst + 4u * n, (uint32_t)o,
+                        failed ? nan : __uint_as_float(d[n]), failed ? nan : __uint_as_float(d[n + 1]),
+                        failed ? nan : __uint_as_float(d[n + 2]),
+                        failed ? nan : __uint_as_float(d[n + 3]));
       }
-    } else {
-      // this CTA's fp32 partial, row-major [128][16], in the (now idle) first ring stage
-      float* red = reinterpret_cast<float*>(base + kTcHeaderBytes);
-#pragma unroll
-      for (int n = 0; n < 16; ++n)
-        red[rr * 16 + n] = failed ? __int_as_float(0x7fc00000) : __uint_as_float(d[n]);
     }
   }
+
+  // ------------------------------------------------------------ split-K reduction, teardown
   tc_fence_before();
   __syncthreads();
   if (p.S > 1) {
-    cluster_sync_all();  // every partial of the cluster is in place
-    const int r0 = slice * kTcRows / p.S, r1 = (slice + 1) * kTcRows / p.S;
-    for (int idx = tid; idx < (r1 - r0) * p.N; idx += kTcThreads) {
-      const int rr = r0 + idx / p.N, n = idx - (idx / p.N) * p.N;
-      const int64_t m = (int64_t)tile * kTcRows + rr;
+    cluster_sync_all();  // every partial of the cluster has landed in its owner
+    pdl_wait();
+    const int rmax = (kTcRows + p.S - 1) / p.S;
+    const int r0 = w.slice * kTcRows / p.S, r1 = (w.slice + 1) * kTcRows / p.S;
+    int l, tile, ar, br;
+    tc_rows(p, w.u0, l, tile, ar, br);
+    const float* red = reinterpret_cast<const float*>(base + p.red_off);
+    for (int it = tid; it < (r1 - r0) * p.N; it += kTcThreads) {
+      const int idx = it / p.N, n = it - idx * p.N;
+      const int64_t m = (int64_t)tile * kTcRows + r0 + idx;
       float v = 0.f;
-      for (int r = 0; r < p.S; ++r) v += ld_cluster_f32(ring32 + (uint32_t)(rr * 16 + n) * 4u, r);
+      for (int src = 0; src < p.S; ++src) v += red[(src * rmax + idx) * 16 + n];
       if (m < p.M) p.c[(int64_t)(l * p.N + n) * p.M + m] = f32_to_f16_bits((v * p.g_a) * p.g_b);
     }
-    cluster_sync_all();  // no CTA leaves while its partial may still be read
   }
   if (warp == 1) {
     tc_fence_after();

@@ -414,12 +414,13 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
 // groups x tiles x S CTAs fill the GPU at two CTAs per SM; NS ring stages of 256 K elements.
 constexpr int kTcDefaultStages = 5;
 
-// At least 80 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM: a third
-// would wait in its TMEM allocation.
-int64_t tc_smem_bytes(int64_t NS) {
-  return std::max<int64_t>(80 * 1024,
-                           1024 + nvfp4::kTcHeaderBytes + NS * nvfp4::kTcStageBytes);  // + 1024
-}                                                                                    // alignment
+// Shared memory of a tensor-core CTA: alignment slack, header, NS stages, split-K partials when
+// S > 1; at least 80 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM (a
+// third would wait in its TMEM allocation).
+int64_t tc_smem_bytes(int64_t NS, int64_t S) {
+  return std::max<int64_t>(80 * 1024, 1024 + nvfp4::kTcHeaderBytes + NS * nvfp4::kTcStageBytes +
+                                          (S > 1 ? nvfp4::kTcRedBytes : 0));
+}
 
 int plan_tc(const DeviceInfo& d, int64_t M, int64_t K, int64_t groups, const nvfp4_plan& f,
             nvfp4_plan* pl) {
@@ -429,24 +430,25 @@ int plan_tc(const DeviceInfo& d, int64_t M, int64_t K, int64_t groups, const nvf
   if ((f.warps_per_cta && f.warps_per_cta != 4) || (f.tile_rows && f.tile_rows != 128))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                 "tensor-core kernel: 4 epilogue warps and 128-row tiles are fixed");
-  const int64_t NS = f.stages ? f.stages : kTcDefaultStages;
-  if (NS < 2 || NS > nvfp4::kTcMaxStages || tc_smem_bytes(NS) > d.max_smem_optin)
-    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tensor-core kernel: stages must be 2..%d",
-                nvfp4::kTcMaxStages);
   const int64_t tiles = ceil_div(M, (int64_t)nvfp4::kTcRows), chunks = K / 256;
+  const int64_t total = groups * tiles, slots = 2 * (int64_t)d.sms;
   int64_t S = f.k_split;
-  if (S == 0)
-    S = std::min<int64_t>(std::min<int64_t>(8, chunks),
-                          std::max<int64_t>(1, (2 * (int64_t)d.sms) /
-                                                   std::max<int64_t>(1, groups * tiles)));
-  if (S > 8 || S > chunks)
+  if (S == 0)  // split K only while the tiles leave at least half of the CTA slots empty
+    S = 2 * total >= slots ? 1
+                           : std::min<int64_t>(std::min<int64_t>(8, chunks),
+                                               std::max<int64_t>(1, slots / total));
+  if (S < 1 || S > 8 || S > chunks)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
-                "tensor-core kernel: K slices must be at most 8 and at most K/256 (S=%lld)",
+                "tensor-core kernel: K slices must be 1..8 and at most K/256 (S=%lld)",
                 (long long)S);
-  S = std::min<int64_t>(S, 8);
   const int64_t per = ceil_div(chunks, S);
   S = ceil_div(chunks, per);  // every slice gets at least one chunk
-  if (groups * tiles * S > (int64_t(1) << 31) - 1 || tiles > (int64_t(1) << 24))
+  const int64_t NS = f.stages ? f.stages : (S > 1 ? 4 : kTcDefaultStages);
+  if (NS < 2 || NS > nvfp4::kTcMaxStages || tc_smem_bytes(NS, S) > d.max_smem_optin)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                "tensor-core kernel: stages must be 2..%d within shared memory",
+                nvfp4::kTcMaxStages);
+  if (total * S > (int64_t(1) << 31) - 1 || tiles > (int64_t(1) << 24))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
   pl->kernel = NVFP4_KERNEL_TC;
   pl->rows_per_warp = 0;
@@ -569,11 +571,20 @@ int launch_tc(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const
   a.stages = pl.stages;
   a.a_rows_per_batch = (int32_t)a_rows_per_batch;
   a.early_weights = (pl.flags & NVFP4_FLAG_EARLY_WEIGHTS) ? 1 : 0;
+  a.total_tiles = (int32_t)(groups * a.tiles);
+  a.red_off = nvfp4::kTcHeaderBytes + (uint32_t)pl.stages * nvfp4::kTcStageBytes;
+  const int64_t smem = tc_smem_bytes(pl.stages, a.S);
+  // S == 1: persistent CTAs, as many as fit at once (at most two per SM); S > 1: one per
+  // (tile, slice)
+  const int64_t occ =
+      std::max<int64_t>(1, std::min<int64_t>(2, d.max_smem_sm / (smem + 1024)));
+  const int64_t grid = a.S > 1 ? (int64_t)a.total_tiles * a.S
+                               : std::min<int64_t>(a.total_tiles, occ * d.sms);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3((unsigned)(groups * a.tiles * a.S));
+  cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(nvfp4::kTcThreads);
-  cfg.dynamicSmemBytes = (size_t)tc_smem_bytes(pl.stages);
+  cfg.dynamicSmemBytes = (size_t)smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   int na = 0;
