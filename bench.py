@@ -188,12 +188,17 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- traffic record
 
+# The headers the register-vector TMA kernel (the kernel the roofline line reports) is built from.
+RV_KERNEL_HEADERS = ("gemv_kernels.cuh", "gemv_tma.cuh", "nvfp4_device.cuh", "quantize.cuh")
+
+
 def kernel_source_digest() -> str:
-    """Digest of the device-code headers (the kernels); the host planner is not part of it."""
+    """Digest of the device-code headers of the reported kernel; the host planner and the other
+    kernels' headers are not part of it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_nvfp4_gemv_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith(".cuh"):
+        if f in RV_KERNEL_HEADERS:
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
