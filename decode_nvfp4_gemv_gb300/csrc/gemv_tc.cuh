@@ -234,6 +234,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
+    // fetch the four tensor-map descriptors while the CTA sets up
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mB)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mSA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&mSB)) : "memory");
     for (int s = 0; s < NS; ++s) {
       mbar_init(smem_addr(&h->full[s]), 1);
       mbar_init(smem_addr(&h->ready[s]), 128);
@@ -395,15 +400,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    pdl_wait();  // c may be read or written by the preceding work
     const uint32_t q = (uint32_t)warp & 3u;
     const int rr = (int)(32u * q) + lane;  // row of the tile (TMEM lane)
     const int rmax = (kTcRows + p.S - 1) / p.S;
     for (int k = 0; k < w.ntiles; ++k) {
       const uint32_t ab = (uint32_t)k & 1u;
       bool fin = *abort_flag == 0 &&
-                 mbar_wait_bounded(smem_addr(&h->acc_full[ab]), (uint32_t)(k >> 1) & 1u,
-                                   kWaitLimitNs);
+                 mbar_wait_sleepy(smem_addr(&h->acc_full[ab]), (uint32_t)(k >> 1) & 1u,
+                                  kWaitLimitNs);
       fin = __all_sync(0xffffffffu, fin);
       tc_fence_after();
       uint32_t d[16];
@@ -413,6 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
       const bool failed = !fin || *abort_flag != 0;
       int l, tile, ar, br;
       tc_rows(p, w.u0 + k * w.ustep, l, tile, ar, br);
+      if (k == 0) pdl_wait();  // c may be read or written by the preceding work
       if (p.S == 1) {
         const int64_t m = (int64_t)tile * kTcRows + rr;
         if (m < p.M) {

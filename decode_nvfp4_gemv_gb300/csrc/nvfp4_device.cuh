@@ -216,6 +216,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// As mbar_wait_bounded, for waiters off the critical path (an epilogue waiting for a whole
+// mainloop): they sleep between polls instead of taking issue slots from the warps that work.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity,
+                                                 uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    __nanosleep(200);
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // L2 policy for data read exactly once.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
