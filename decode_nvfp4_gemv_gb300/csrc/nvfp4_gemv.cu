@@ -450,10 +450,14 @@ int plan_tc(const DeviceInfo& d, int64_t M, int64_t K, int64_t groups, const nvf
                 nvfp4::kTcMaxStages);
   if (total * S > (int64_t(1) << 31) - 1 || tiles > (int64_t(1) << 24))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
+  // ctas_per_batch: with S == 1 the number of persistent CTAs for the whole launch (forced, or 0
+  // for as many as fit); with S > 1 one CTA per (tile, slice)
+  int64_t ctas = S > 1 ? total * S : f.ctas_per_batch;
+  if (S == 1 && ctas > total) ctas = total;
   pl->kernel = NVFP4_KERNEL_TC;
   pl->rows_per_warp = 0;
   pl->k_split = (int32_t)S;
-  pl->ctas_per_batch = (int32_t)(tiles * S);
+  pl->ctas_per_batch = (int32_t)ctas;
   pl->warps_per_cta = 4;
   pl->tile_rows = nvfp4::kTcRows;
   pl->stages = (int32_t)NS;
@@ -579,7 +583,8 @@ int launch_tc(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const
   const int64_t occ =
       std::max<int64_t>(1, std::min<int64_t>(2, d.max_smem_sm / (smem + 1024)));
   const int64_t grid = a.S > 1 ? (int64_t)a.total_tiles * a.S
-                               : std::min<int64_t>(a.total_tiles, occ * d.sms);
+                      : pl.ctas_per_batch > 0 ? std::min<int64_t>(a.total_tiles, pl.ctas_per_batch)
+                                              : std::min<int64_t>(a.total_tiles, occ * d.sms);
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3((unsigned)grid);

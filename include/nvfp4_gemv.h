@@ -118,12 +118,15 @@ typedef struct nvfp4_plan {
   int32_t kernel;          /* nvfp4_kernel */
   int32_t rows_per_warp;   /* STREAM: rows a warp processes together (1, 2 or 4); TMA*: 4 */
   int32_t k_split;         /* STREAM: K slices per row inside a CTA (1 .. ceil(K/1024));
-                              TMA_RV: 1024-element segments per warp (filled in by the planner) */
-  int32_t ctas_per_batch;  /* all kernels: CTAs sharing one batch's rows (1 .. M) */
+                              TMA_RV: 1024-element segments per warp (filled in by the planner);
+                              TC: K slices = cluster size (1 .. 8, at most K/256) */
+  int32_t ctas_per_batch;  /* SIMPLE, STREAM, TMA*: CTAs sharing one batch's rows (1 .. M);
+                              TC with k_split 1: persistent CTAs for the whole launch (0 = as many
+                              as fit); TC with k_split > 1: filled in (tiles x k_split) */
   int32_t warps_per_cta;   /* SIMPLE: 1 .. 8; STREAM: 1 .. 16; TMA*: consumer warps 1 .. 16 (one
-                              producer warp is added) */
-  int32_t tile_rows;       /* TMA*: rows per ring stage (1 .. 256) */
-  int32_t stages;          /* TMA*: ring stages (2 .. 8) */
+                              producer warp is added); TC: 4 (fixed) */
+  int32_t tile_rows;       /* TMA*: rows per ring stage (1 .. 256); TC: 128 (fixed) */
+  int32_t stages;          /* TMA*: ring stages (2 .. 8); TC: 2 .. 6 stages of 256 elements */
   int32_t flags;           /* NVFP4_FLAG_* (honoured by the automatic plan too) */
 } nvfp4_plan;
 
