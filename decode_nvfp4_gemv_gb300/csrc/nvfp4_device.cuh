@@ -95,18 +95,6 @@ __device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
 }
 
-// low half + high half, in f32 (one widening and one mixed-precision add).
-__device__ __forceinline__ float f16x2_hsum_f32(uint32_t h) {
-  float r;
-  asm("{\n\t.reg .b16 l, u;\n\t.reg .f32 t;\n\t"
-      "mov.b32 {l, u}, %1;\n\t"
-      "cvt.f32.f16 t, l;\n\t"
-      "add.rn.f32.f16 %0, u, t;\n\t}"
-      : "=f"(r)
-      : "r"(h));
-  return r;
-}
-
 // 16-byte read-only streaming load: not allocated in L1 (each byte of A is read once).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;

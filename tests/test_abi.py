@@ -166,3 +166,27 @@ def test_grouped_rejected_before_device_work(lib, kw, status):
 def test_grouped_empty_is_a_noop(lib):
     assert _grouped(lib, T=0, A=0, sfa=0, b=0, sfb=0, c=0) == 0
     assert _grouped(lib, M=0, A=0, sfa=0, b=0, sfb=0, c=0) == 0
+
+
+def _small_n(lib, A=0x100000, sfa=0x200000, b=0x300000, sfb=0x400000, c=0x500000, M=4, K=256,
+             N=3, flags=None):
+    vp = ctypes.c_void_p
+    import decode_nvfp4_gemv_gb300 as pkg
+
+    plan = ctypes.byref(pkg.Plan(flags=flags)) if flags is not None else None
+    return lib.nvfp4_gemm_small_n(vp(A), vp(sfa), ctypes.c_float(1.0), vp(b), vp(sfb),
+                                  ctypes.c_float(1.0), vp(c), M, K, N, None, plan)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(M=-1), 1), (dict(N=-1), 1), (dict(K=24), 1), (dict(K=0), 1), (dict(A=0), 1),
+    (dict(c=0x500001), 2), (dict(c=0x100000), 1),   # c misaligned; c overlaps A
+    (dict(flags=4), 1), (dict(M=1 << 31), 3),
+])
+def test_small_n_rejected_before_device_work(lib, kw, status):
+    assert _small_n(lib, **kw) == status
+
+
+def test_small_n_empty_is_a_noop(lib):
+    assert _small_n(lib, N=0, A=0, sfa=0, b=0, sfb=0, c=0) == 0
+    assert _small_n(lib, M=0, A=0, sfa=0, b=0, sfb=0, c=0) == 0
