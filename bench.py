@@ -705,44 +705,73 @@ def run_ours(args):
     barrier(dist)
 
 
-def time_e2e(pkg, w, plan, device, stream, steps, dist):
+def time_e2e(pkg, w, plan, device, stream, steps, dist, copy_streams=1):
     """GB/s of algorithmic bytes when every step copies its inputs from pinned host memory, runs
-    the GEMV through the public call and reads c back to pinned host memory."""
+    the GEMV through the public call and reads c back to pinned host memory.  The input copy of a
+    step is split over `copy_streams` streams (the copy engines work in parallel) into one of two
+    device buffers, so step i's copies overlap step i-1's GEMV and read-back; a buffer is reused
+    only after the GEMV that read it has finished."""
     import torch
 
-    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(w, k))).pin_memory()
-            for k in ("A", "sfa", "b", "sfb")}
-    devb = {k: torch.empty_like(v, device=device) for k, v in host.items()}
-    c_dev = torch.empty((w.L, w.M), dtype=torch.float16, device=device)
-    c_host = torch.empty((w.L, w.M), dtype=torch.float16).pin_memory()
+    names = ("A", "sfa", "b", "sfb")
+    host = {k: torch.from_numpy(np.ascontiguousarray(getattr(w, k)).ravel()).pin_memory()
+            for k in names}
+    devb = [{k: torch.empty_like(v, device=device) for k, v in host.items()} for _ in range(2)]
+    c_dev = [torch.empty((w.L, w.M), dtype=torch.float16, device=device) for _ in range(2)]
+    c_host = [torch.empty((w.L, w.M), dtype=torch.float16).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() for v in host.values())
-    d2h = c_host.numel() * 2
+    d2h = c_host[0].numel() * 2
+    cps = [torch.cuda.Stream(device) for _ in range(copy_streams)]
+    nA = host["A"].numel()
+    cuts = [nA * j // copy_streams for j in range(copy_streams + 1)]
+    done = [None, None]  # event after the GEMV that last read buffer 0 / 1
 
-    def step():
-        for k in host:
-            devb[k].copy_(host[k], non_blocking=True)
-        pkg.nvfp4_gemv_batched_ex(devb["A"], devb["sfa"], w.g_a, devb["b"], devb["sfb"], w.g_b,
-                                  c_dev, w.M, w.K, w.L, stream=stream, plan=plan)
-        c_host.copy_(c_dev, non_blocking=True)
+    def step(i, start=None):
+        bi = i % 2
+        evs = []
+        for j, cs in enumerate(cps):
+            if start is not None:
+                cs.wait_event(start)
+            if done[bi] is not None:
+                cs.wait_event(done[bi])
+            with torch.cuda.stream(cs):
+                devb[bi]["A"][cuts[j]:cuts[j + 1]].copy_(host["A"][cuts[j]:cuts[j + 1]],
+                                                         non_blocking=True)
+                if j == copy_streams - 1:
+                    for k in ("sfa", "b", "sfb"):
+                        devb[bi][k].copy_(host[k], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            evs.append(ev)
+        for ev in evs:
+            stream.wait_event(ev)
+        d = devb[bi]
+        with torch.cuda.stream(stream):
+            pkg.nvfp4_gemv_batched_ex(d["A"], d["sfa"], w.g_a, d["b"], d["sfb"], w.g_b,
+                                      c_dev[bi], w.M, w.K, w.L, stream=stream, plan=plan)
+            fin = torch.cuda.Event()
+            fin.record(stream)
+            done[bi] = fin
+            c_host[bi].copy_(c_dev[bi], non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            step()
-        stream.synchronize()
-        barrier(dist)
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(steps):
-            step()
-        ev1.record(stream)
-        stream.synchronize()
-        barrier(dist)
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(steps):
+        step(i, start=ev0 if i == 0 else None)
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist)
     seconds = ev0.elapsed_time(ev1) / 1e3
     total, slowest = aggregate(dist, w.algorithmic_bytes * steps, seconds)
     return {"value": round(total / slowest / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": steps,
-            "us_per_step": round(seconds / steps * 1e6, 2)}
+            "us_per_step": round(seconds / steps * 1e6, 2),
+            "copies": f"{copy_streams} streams, double-buffered inputs"}
 
 
 # ---------------------------------------------------------------------------- the oracle on the CPU
