@@ -118,8 +118,10 @@ __global__ void __launch_bounds__(256) gemv_simple_kernel(
 //
 // Per row and step the lane decodes 16 bytes with cvt.rn.f16x2.e2m1x2, multiplies them by the
 // staged vector words with packed f16 FMAs (two chains of 8, one per block: each half-lane sum is
-// at most 8 * 36 = 288 in quarter units, so exact in f16), widens each block partial to f32, and
-// adds partial * (sfa * sfb) into an fp32 row accumulator.  At the end of a unit the R row sums
+// at most 8 * 36 = 288 in quarter units, so exact in f16), multiplies each half sum by the f16
+// block scale sfa with mixed-precision FMAs (f16 operands, exact f32 result) and adds the block
+// term times sfb into the row's pair of fp32 accumulators (one per block position, one packed
+// fp32x2 FMA for both), which the unit's end adds.  At the end of a unit the R row sums
 // are reduced across the warp (a transposing butterfly: R - 1 exchange shuffles, then
 // 5 - log2(R) plain ones) and stored to a shared array partial[slice][row].  After the CTA
 // barrier, thread t sums partial[0..S)[t] in slice order (deterministic), applies g_a and g_b in

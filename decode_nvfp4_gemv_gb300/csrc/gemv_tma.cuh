@@ -17,7 +17,8 @@
 // Items.  A tile is cut into groups of 4 rows x 1024-element segments.  For an item, lane t takes
 // 16 bytes (32 elements, two scale blocks) of each of the 4 rows at k = 1024 * seg + 32 t,
 // multiplies them with the vector's f16x2 words by packed f16 FMAs (exact block partials), scales
-// each block partial by sfa * sfb in fp32 and accumulates per row.  A warp reduces its 4 row sums
+// each block partial by sfa (mixed-precision FMAs, exact) and by sfb (one packed fp32x2 FMA into
+// the row's two accumulators) and accumulates per row.  A warp reduces its 4 row sums
 // across lanes and writes them to partial[row][slot] in shared memory; after the last tile,
 // thread t sums partial[t][0 .. slots) in slot order (deterministic), applies g_a and g_b in fp32
 // and stores fp16.
