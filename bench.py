@@ -192,15 +192,37 @@ class ClockSampler:
 RV_KERNEL_HEADERS = ("gemv_kernels.cuh", "gemv_tma.cuh", "nvfp4_device.cuh", "quantize.cuh")
 
 
+def _code_only(text: str) -> str:
+    """C++ source with comments removed and whitespace collapsed (string literals kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest() -> str:
-    """Digest of the device-code headers of the reported kernel; the host planner and the other
-    kernels' headers are not part of it."""
+    """Digest of the code (comments and layout excluded) of the device headers the reported kernel
+    is built from; the host planner and the other kernels' headers are not part of it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "decode_nvfp4_gemv_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f in RV_KERNEL_HEADERS:
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(f.encode() + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -75,3 +75,13 @@ def test_traffic_record_requires_matching_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("c9") == 120.0
     monkeypatch.setattr(bench, "kernel_source_digest", lambda: "ffffffffffffffff")
     assert bench.recorded_traffic("c9") is None
+
+
+def test_code_only_digest_ignores_comments_not_code():
+    import bench
+
+    a = 'int x = 1; // note\n/* block\n comment */ const char* s = "a // b";\n'
+    b = 'int x = 1;\n\n   const char* s = "a // b"; // other note'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(a.replace("x = 1", "x = 2"))
+    assert '"a // b"' in bench._code_only(a)
