@@ -85,3 +85,12 @@ def test_code_only_digest_ignores_comments_not_code():
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(a.replace("x = 1", "x = 2"))
     assert '"a // b"' in bench._code_only(a)
+
+
+def test_cpu_baseline_uses_every_core():
+    import bench
+    import workloads
+
+    r = bench.cpu_baseline(workloads.make("c1"), 1.0, "c1")
+    assert r["kind"] == "oracle" and r["value"] > 0 and r["cores"] >= 1
+    assert r["single_thread"]["cores"] == 1
