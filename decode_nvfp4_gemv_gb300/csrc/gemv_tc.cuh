@@ -456,8 +456,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
     int l, tile, ar, br;
     tc_rows(p, w.u0, l, tile, ar, br);
     const float* red = reinterpret_cast<const float*>(base + p.red_off);
-    for (int it = tid; it < (r1 - r0) * p.N; it += kTcThreads) {
-      const int idx = it / p.N, n = it - idx * p.N;
+    const int nr = r1 - r0;
+    for (int it = tid; it < nr * p.N; it += kTcThreads) {  // consecutive threads: consecutive rows
+      const int n = it / nr, idx = it - n * nr;
       const int64_t m = (int64_t)tile * kTcRows + r0 + idx;
       float v = 0.f;
       for (int src = 0; src < p.S; ++src) v += red[(src * rmax + idx) * 16 + n];
