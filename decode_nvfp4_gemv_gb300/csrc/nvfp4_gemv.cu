@@ -360,16 +360,12 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   }
   const int64_t slots = rv ? std::min(Wc, nseg) : Wc;
   const int64_t rg_step = (rv && nseg < Wc) ? Wc / nseg : 1;
-  // two CTAs per SM if the ring fits, else one
-  for (int occ = 2; occ >= 1; --occ) {
-    const int64_t budget =
-        std::min<int64_t>(d.max_smem_optin, d.max_smem_sm / occ - 1024);
-    const int64_t slots_sm = (int64_t)d.sms * occ;
-    int64_t P = f.ctas_per_batch ? f.ctas_per_batch : std::max<int64_t>(1, slots_sm / L);
-    P = std::min(P, M);
+  const int64_t row_bytes = K / 2 + K / 16;
+  const int64_t unit = 4 * rg_step;  // rows one round of the consumer warps covers
+  // Tile rows and ring depth for P CTAs per batch within `budget` bytes of shared memory; false
+  // if the partial sums and a two-stage ring do not fit.
+  auto shape = [&](int64_t P, int64_t budget, int64_t* TR_out, int64_t* NS_out) -> bool {
     const int64_t rows_cap = ceil_div(M, P);
-    const int64_t row_bytes = K / 2 + K / 16;
-    const int64_t unit = 4 * rg_step;  // rows one round of the consumer warps covers
     int64_t TR = f.tile_rows;
     if (TR == 0) {
       TR = std::max<int64_t>(1, kTmaStageTarget / row_bytes);
@@ -391,9 +387,43 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
           NS = ns;
           break;
         }
-      if (NS == 0) continue;
+      if (NS == 0) return false;
     }
-    if (tma_layout(rv, K, TR, NS, rows_cap, slots).total > d.max_smem_optin) continue;
+    if (tma_layout(rv, K, TR, NS, rows_cap, slots).total > d.max_smem_optin) return false;
+    *TR_out = TR;
+    *NS_out = NS;
+    return true;
+  };
+  // two CTAs per SM if the ring fits, else one
+  for (int occ = 2; occ >= 1; --occ) {
+    const int64_t budget = std::min<int64_t>(d.max_smem_optin, d.max_smem_sm / occ - 1024);
+    const int64_t slots_sm = (int64_t)d.sms * occ;
+    int64_t P = 0, TR = 0, NS = 0;
+    if (f.ctas_per_batch) {
+      P = std::min<int64_t>(f.ctas_per_batch, M);
+      if (!shape(P, budget, &TR, &NS)) continue;
+    } else {
+      // CTAs per batch: start from one wave of CTA slots; where L does not divide the slots (or
+      // the rows of one wave's CTAs overflow shared memory) take more CTAs when they fill their
+      // last wave at least 1% better.  Measured on GB300: a grid of 0.84 waves ran at 77% of the
+      // bandwidth of four exact waves, and a 4.7 GB call at 2.1x the stream kernel's rate.
+      const int64_t P0 = std::min<int64_t>(M, std::max<int64_t>(1, slots_sm / L));
+      const int64_t P_hi = std::min<int64_t>(M, 8 * P0 + 8);
+      double best_fill = -1.0;
+      for (int64_t p = P0; p <= P_hi; ++p) {
+        const int64_t grid = p * L;
+        const double fill = (double)grid / (double)(ceil_div(grid, slots_sm) * slots_sm);
+        if (fill <= best_fill + 0.01) continue;
+        int64_t tr = 0, ns = 0;
+        if (!shape(p, budget, &tr, &ns)) continue;
+        P = p;
+        TR = tr;
+        NS = ns;
+        best_fill = fill;
+        if (fill >= 0.999) break;
+      }
+      if (P == 0) continue;
+    }
     if (P * L > (int64_t(1) << 31) - 1)
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
     pl->kernel = rv ? NVFP4_KERNEL_TMA_RV : NVFP4_KERNEL_TMA;

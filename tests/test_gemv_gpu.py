@@ -168,6 +168,19 @@ def test_auto_plans_are_complete(pkg):
             assert p.kernel in (3, 4) and p.stages >= 2 and p.tile_rows >= 1
 
 
+def test_auto_plans_fill_their_waves(pkg):
+    """Batch counts that do not divide the CTA slots, or whose one-wave CTAs would hold too many
+    rows, still get the register-vector kernel with a well-filled last wave."""
+    slots = 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    for M, K, L in [(7168, 16384, 80), (4096, 7168, 64), (7168, 16384, 5), (270000, 16384, 5),
+                    (3584, 6144, 16), (7168, 2048, 4), (4096, 7168, 8)]:
+        p = pkg.nvfp4_gemv_plan(M, K, L)
+        assert p.kernel == 4, (M, K, L, p.kernel)
+        grid = p.ctas_per_batch * L
+        fill = grid / (-(-grid // slots) * slots)
+        assert fill >= 0.95, (M, K, L, p.ctas_per_batch, fill)
+
+
 def test_largest_stream_k_and_beyond(pkg):
     kmax = pkg.nvfp4_max_stream_k()
     assert kmax >= 65536

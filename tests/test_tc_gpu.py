@@ -148,3 +148,54 @@ def test_workloads_on_tensor_cores(pkg, workload, name):
     torch.cuda.synchronize()
     ref, T = oracle.gemv(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, w.M, w.K, w.L)
     assert_parity(c.cpu().numpy(), ref, T, f"{name} on tensor cores")
+
+
+def test_tensor_core_plan_rules(pkg):
+    """Forced TC plans outside the kernel's range are refused on the host (UNSUPPORTED_SHAPE),
+    and the TC kernel takes neither the grouped form nor bf16 output."""
+    M, K, N = 128, 512, 2
+    A, sfa, b, sfb, g_a, g_b = make(M, K, N, seed=4)
+    for plan in (dict(kernel=TC, k_split=3), dict(kernel=TC, k_split=9), dict(kernel=TC, stages=1),
+                 dict(kernel=TC, stages=7), dict(kernel=TC, warps_per_cta=8),
+                 dict(kernel=TC, tile_rows=64)):
+        with pytest.raises(pkg.NVFP4Error) as e:
+            small_n(pkg, A, sfa, b, sfb, g_a, g_b, M, K, N, plan)
+        assert e.value.status == 3, plan
+    g = workloads.make_grouped("g0")
+    d = {k: torch.from_numpy(np.ascontiguousarray(getattr(g, k))).cuda()
+         for k in ("A", "sfa", "g_a", "g_b", "b", "sfb", "expert_of")}
+    c = torch.empty((g.T, g.M), dtype=torch.float16, device="cuda")
+    with pytest.raises(pkg.NVFP4Error) as e:
+        pkg.nvfp4_gemv_grouped(d["A"], d["sfa"], d["g_a"], d["b"], d["sfb"], d["g_b"], c, g.M,
+                               g.K, g.E, g.T, expert_of_token=d["expert_of"],
+                               plan=dict(kernel=TC))
+    assert e.value.status == 3
+
+
+def test_tensor_cores_after_other_work_in_the_stream(pkg):
+    """A TC call whose vectors are written by the kernel just before it (programmatic dependent
+    launch must still see them), on a non-default stream, then captured in a graph."""
+    M, K, N = 384, 1024, 3
+    A, sfa, b, sfb, g_a, g_b = make(M, K, N, seed=6)
+    ref, T = ref_small_n(A, sfa, b, sfb, g_a, g_b, M, K, N)
+    tA, tS = torch.from_numpy(A).cuda(), torch.from_numpy(sfa).cuda()
+    src_b, src_s = torch.from_numpy(b).cuda(), torch.from_numpy(sfb).cuda()
+    tb, ts = torch.zeros_like(src_b), torch.zeros_like(src_s)
+    c = torch.full((N, M), float("nan"), dtype=torch.float16, device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        tb.copy_(src_b)
+        ts.copy_(src_s)
+        pkg.nvfp4_gemm_small_n(tA, tS, g_a, tb, ts, g_b, c, M, K, N, stream=s,
+                               plan={"flags": 1})
+    s.synchronize()
+    assert_parity(c.cpu().numpy(), ref, T, "after a copy kernel")
+    g = torch.cuda.CUDAGraph()
+    c2 = torch.full((N, M), float("nan"), dtype=torch.float16, device="cuda")
+    with torch.cuda.graph(g, stream=s):
+        pkg.nvfp4_gemm_small_n(tA, tS, g_a, tb, ts, g_b, c2, M, K, N, stream=s)
+    with torch.cuda.stream(s):
+        g.replay()
+    s.synchronize()
+    assert np.array_equal(c.cpu().numpy().view(np.uint16), c2.cpu().numpy().view(np.uint16))
