@@ -507,6 +507,44 @@ def _graph_time(fn, stream, steps, warmup, dist, dev):
     return ev0.elapsed_time(ev1) / 1e3, reps * chunk
 
 
+def time_large(pkg, device, stream, steps, warmup, dist, M=7168, K=16384, L=80):
+    """A many-batch call of the decode projection shape: 80 batches of 7168 x 16384 (5.29 GB per
+    call, far larger than L2, so no rotation).  Batch q's A is one seeded block with every byte
+    XORed with a per-batch key; every batch has its own vector.  The per-call start and drain
+    are small against 0.7 ms of streaming, so this shows the kernel's streaming rate."""
+    import torch
+
+    blk = workloads.random_workload(M, K, 1, seed=31)
+    vec = workloads.random_workload(1, K, L, seed=32)
+    dA = torch.from_numpy(blk.A[0]).to(device)
+    dS = torch.from_numpy(blk.sfa[0]).to(device)
+    A = torch.empty((L, M, K // 2), dtype=torch.uint8, device=device)
+    S = torch.empty((L, M, K // 16), dtype=torch.uint8, device=device)
+    for q in range(L):
+        torch.bitwise_xor(dA, (37 * q + 11) & 0xFF, out=A[q])
+        S[q].copy_(dS)
+    b = torch.from_numpy(vec.b).to(device)
+    sfb = torch.from_numpy(vec.sfb).to(device)
+    c = torch.empty((L, M), dtype=torch.float16, device=device)
+    plan = {"flags": FLAG_EARLY_WEIGHTS}
+
+    def fn(i):
+        pkg.nvfp4_gemv_batched_ex(A, S, blk.g_a, b, sfb, vec.g_b, c, M, K, L, stream=stream,
+                                  plan=plan)
+    sec, calls = _graph_time(fn, stream, steps, warmup, dist, device)
+    assert not torch.isnan(c).any().item()
+    nbytes = workloads.algorithmic_bytes(M, K, L)
+    gbs = nbytes * calls / sec / 1e9
+    peak, _ = measured_peak_gbs()
+    p = pkg.nvfp4_gemv_plan(M, K, L)
+    del A, S
+    torch.cuda.empty_cache()
+    return {"workload": f"M={M} K={K} L={L} ({nbytes / 1e9:.2f} GB per call)",
+            "kernel": KERNEL_NAMES.get(p.kernel), "ctas_per_batch": p.ctas_per_batch,
+            "us_per_call": round(sec / calls * 1e6, 3), "calls": calls,
+            "GB/s": round(gbs, 2), "frac": round(gbs / peak, 4)}
+
+
 def time_small_n(pkg, device, stream, steps, warmup, dist, M=7168, K=16384, Ns=(2, 8, 16)):
     """N vectors sharing one weight matrix (a decode batch): the tensor-core kernel (automatic
     plan) against the register-vector CUDA-core kernel reading A once per vector.  Bytes: A and
@@ -655,6 +693,10 @@ def run_ours(args):
     if not args.plan and not args.no_general:
         general = time_general(pkg, w, stream, min(args.steps, 2000), args.warmup, dist, n_copies)
 
+    large = None
+    if not args.plan and not args.no_large:
+        large = time_large(pkg, device, stream, min(args.steps, 100), args.warmup, dist)
+
     grouped = None
     if not args.plan and not args.no_grouped:
         grouped = time_grouped(pkg, device, stream, min(args.steps, 20000), args.warmup, dist)
@@ -715,6 +757,8 @@ def run_ours(args):
             line["grouped"] = grouped
         if general is not None:
             line["general_unaligned"] = general
+        if large is not None:
+            line["large_batch"] = large
         if tc_n1 is not None:
             line["tensor_cores_n1"] = tc_n1
         if small is not None:
@@ -938,6 +982,8 @@ def main():
                     help="skip the grouped (mixture-of-experts) timing")
     ap.add_argument("--no-general", action="store_true",
                     help="skip the unaligned-input (byte-load kernel) timing")
+    ap.add_argument("--no-large", action="store_true",
+                    help="skip the 80-batch (5.29 GB per call) timing")
     ap.add_argument("--no-tc", action="store_true",
                     help="skip the tensor-core timings (N = 1 and small N)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
