@@ -7,6 +7,7 @@ memory and streams.  The entry points have the C names:
     nvfp4_gemv_batched(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream=None)
     nvfp4_gemv_batched_ex(A, sfa, g_a, b, sfb, g_b, c, M, K, L, stream=None, plan=None)
     nvfp4_gemv_plan(M, K, L) -> Plan
+    nvfp4_plan_for_limits(M, K, L, plan=None, sms=..., max_smem_optin=..., max_smem_sm=...) -> Plan
     nvfp4_max_stream_k(), nvfp4_status_string(status), nvfp4_last_error(), nvfp4_abi_version()
 
 Tensor arguments are contiguous CUDA tensors (A, sfa, b, sfb: uint8; c: float16, or uint16/int16
@@ -30,6 +31,7 @@ __all__ = [
     "OUT_BF16", "nvfp4_gemv_grouped", "library_path",
     "load_library", "nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_plan",
     "nvfp4_max_stream_k", "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version", "gemv",
+    "DeviceLimits", "GB300_LIMITS", "nvfp4_plan_for_limits",
 ]
 
 KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV, KERNEL_TC = 0, 1, 2, 3, 4, 5
@@ -58,6 +60,16 @@ class Plan(ctypes.Structure):
 
     def __repr__(self):
         return f"Plan({self.as_dict()})"
+
+
+class DeviceLimits(ctypes.Structure):
+    """The device limits the planner reads (nvfp4_device_limits)."""
+    _fields_ = [("sms", ctypes.c_int32), ("max_smem_optin", ctypes.c_int32),
+                ("max_smem_sm", ctypes.c_int32)]
+
+
+# GB300: 152 SMs, 227 KiB of shared memory per CTA (opt-in), 228 KiB per SM
+GB300_LIMITS = dict(sms=152, max_smem_optin=232448, max_smem_sm=233472)
 
 
 _lib = None
@@ -96,6 +108,9 @@ def load_library():
     lib.nvfp4_gemm_small_n.restype = ctypes.c_int
     lib.nvfp4_gemv_plan.argtypes = [i64, i64, i64, ctypes.POINTER(Plan)]
     lib.nvfp4_gemv_plan.restype = ctypes.c_int
+    lib.nvfp4_plan_for_limits.argtypes = [ctypes.POINTER(DeviceLimits), i64, i64, i64,
+                                          ctypes.POINTER(Plan), ctypes.POINTER(Plan)]
+    lib.nvfp4_plan_for_limits.restype = ctypes.c_int
     lib.nvfp4_max_stream_k.argtypes = []
     lib.nvfp4_max_stream_k.restype = ctypes.c_int64
     lib.nvfp4_status_string.argtypes = [ctypes.c_int]
@@ -118,6 +133,22 @@ def nvfp4_last_error() -> str:
 
 def nvfp4_abi_version() -> int:
     return load_library().nvfp4_abi_version()
+
+
+def nvfp4_plan_for_limits(M, K, L, plan=None, sms=GB300_LIMITS["sms"],
+                          max_smem_optin=GB300_LIMITS["max_smem_optin"],
+                          max_smem_sm=GB300_LIMITS["max_smem_sm"]) -> Plan:
+    """The planner's choice (or its check of ``plan``) for a device with the given limits, without
+    touching any device; raises NVFP4Error with the status a launch would return."""
+    lim = DeviceLimits(int(sms), int(max_smem_optin), int(max_smem_sm))
+    forced = None
+    if plan is not None:
+        forced = Plan(**plan) if isinstance(plan, dict) else plan
+    out = Plan()
+    _check(load_library().nvfp4_plan_for_limits(
+        ctypes.byref(lim), int(M), int(K), int(L),
+        ctypes.byref(forced) if forced is not None else None, ctypes.byref(out)))
+    return out
 
 
 def nvfp4_max_stream_k() -> int:

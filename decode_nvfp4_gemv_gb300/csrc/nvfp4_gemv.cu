@@ -368,7 +368,7 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
     const int64_t rows_cap = ceil_div(M, P);
     int64_t TR = f.tile_rows;
     if (TR == 0) {
-      TR = std::max<int64_t>(1, kTmaStageTarget / row_bytes);
+      TR = std::min<int64_t>(256, std::max<int64_t>(1, kTmaStageTarget / row_bytes));
       if (TR >= unit) TR -= TR % unit;
       else if (TR >= 4) TR -= TR % 4;
       TR = std::min<int64_t>(TR, std::max<int64_t>(4, align_up(rows_cap, 4)));
@@ -406,15 +406,30 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       // CTAs per batch: start from one wave of CTA slots; where L does not divide the slots (or
       // the rows of one wave's CTAs overflow shared memory) take more CTAs when they fill their
       // last wave at least 1% better.  Measured on GB300: a grid of 0.84 waves ran at 77% of the
-      // bandwidth of four exact waves, and a 4.7 GB call at 2.1x the stream kernel's rate.
+      // bandwidth of four exact waves, and an 80-batch call (5.29 GB) ran at 2.1x the stream
+      // kernel's rate.
       const int64_t P0 = std::min<int64_t>(M, std::max<int64_t>(1, slots_sm / L));
-      const int64_t P_hi = std::min<int64_t>(M, 8 * P0 + 8);
+      // the smallest P >= P0 whose partial sums and two-stage ring fit: more CTAs per batch means
+      // fewer rows per CTA, so whether a P fits is monotone in P (doubling, then bisection)
+      int64_t P_fit = P0, tr = 0, ns = 0;
+      if (!shape(P0, budget, &tr, &ns)) {
+        int64_t hi = P0;
+        while (hi < M && !shape(hi, budget, &tr, &ns)) hi = std::min<int64_t>(M, 2 * hi);
+        if (!shape(hi, budget, &tr, &ns)) continue;  // nothing fits at this occupancy
+        int64_t lo = std::max<int64_t>(P0, hi / 2);    // does not fit
+        while (hi - lo > 1) {
+          const int64_t mid = lo + (hi - lo) / 2;
+          if (shape(mid, budget, &tr, &ns)) hi = mid;
+          else lo = mid;
+        }
+        P_fit = hi;
+      }
+      const int64_t P_hi = std::min<int64_t>(M, P_fit + 8 * P0 + 8);
       double best_fill = -1.0;
-      for (int64_t p = P0; p <= P_hi; ++p) {
+      for (int64_t p = P_fit; p <= P_hi; ++p) {
         const int64_t grid = p * L;
         const double fill = (double)grid / (double)(ceil_div(grid, slots_sm) * slots_sm);
         if (fill <= best_fill + 0.01) continue;
-        int64_t tr = 0, ns = 0;
         if (!shape(p, budget, &tr, &ns)) continue;
         P = p;
         TR = tr;
@@ -1007,6 +1022,25 @@ int nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, nvfp4_plan* out) {
   int st = current_device(&d);
   if (st != NVFP4_OK) return st;
   return make_plan(*d, M, K, L, nullptr, out);
+}
+
+int nvfp4_plan_for_limits(const nvfp4_device_limits* lim, int64_t M, int64_t K, int64_t L,
+                          const nvfp4_plan* forced, nvfp4_plan* out) {
+  g_last_error[0] = '\0';
+  if (!lim || !out) return fail(NVFP4_ERR_INVALID_VALUE, "lim and out must not be NULL");
+  if (lim->sms < 1 || lim->max_smem_optin < 1024 || lim->max_smem_sm < lim->max_smem_optin)
+    return fail(NVFP4_ERR_INVALID_VALUE, "implausible device limits (sms %d, smem %d / %d)",
+                lim->sms, lim->max_smem_optin, lim->max_smem_sm);
+  if (M <= 0 || L <= 0 || K <= 0 || K % 16)
+    return fail(NVFP4_ERR_INVALID_VALUE, "need M, L > 0 and K a positive multiple of 16");
+  const int64_t kI32 = (int64_t(1) << 31) - 1;
+  if (M > kI32 || L > kI32 || K / 2 > kI32)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "M, L and K/2 must be below 2^31");
+  DeviceInfo d;
+  d.sms = lim->sms;
+  d.max_smem_optin = lim->max_smem_optin;
+  d.max_smem_sm = lim->max_smem_sm;
+  return make_plan(d, M, K, L, forced, out);
 }
 
 int64_t nvfp4_max_stream_k(void) {

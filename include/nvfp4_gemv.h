@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define NVFP4_ABI_VERSION 4
+#define NVFP4_ABI_VERSION 5
 
 typedef enum nvfp4_status {
   NVFP4_OK = 0,
@@ -150,6 +150,28 @@ int nvfp4_gemv_batched_ex(const uint8_t* A, const uint8_t* sfa, float g_a,
 /* The plan nvfp4_gemv_batched would use for (M, K, L) on the current device, with every field
  * filled in.  Touches no memory other than *out.  Returns an nvfp4_status. */
 int nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, nvfp4_plan* out);
+
+/* The device limits the planner reads. */
+typedef struct nvfp4_device_limits {
+  int32_t sms;             /* streaming multiprocessors (152 on GB300) */
+  int32_t max_smem_optin;  /* bytes of shared memory one CTA may opt into (232448 on GB300) */
+  int32_t max_smem_sm;     /* bytes of shared memory per SM (233472 on GB300) */
+} nvfp4_device_limits;
+
+/* The plan nvfp4_gemv_batched_ex would use for (M, K, L) and `forced` (NULL = automatic), or the
+ * status it would return for an unsupported forced plan, computed for a device with the given
+ * limits and without touching any device.  For host-side tests and capacity planning.
+ *
+ * Arguments: lim and out non-NULL; lim plausible (sms >= 1, max_smem_optin >= 1024,
+ * max_smem_sm >= max_smem_optin), else NVFP4_ERR_INVALID_VALUE; M, L >= 1 and K a positive
+ * multiple of 16, each below 2^31 (K/2 for K), else NVFP4_ERR_INVALID_VALUE or
+ * NVFP4_ERR_UNSUPPORTED_SHAPE as for the launching entry points.  Inputs are taken as 16-byte
+ * aligned.  The STREAM kernel's CTAs per SM come from the driver's occupancy query when a device
+ * is present, else 1; every other choice depends on the limits alone, so a plan computed here
+ * with a device's own limits equals the one that device's launches use.  No counterpart in the
+ * pages: it exposes this library's planner. */
+int nvfp4_plan_for_limits(const nvfp4_device_limits* lim, int64_t M, int64_t K, int64_t L,
+                          const nvfp4_plan* forced, nvfp4_plan* out);
 
 /* Largest K the STREAM kernel accepts on the current device (its shared-memory bound), or 0 if the
  * device cannot be queried. */

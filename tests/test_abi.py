@@ -34,7 +34,8 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ("nvfp4_gemv_batched", "nvfp4_gemv_batched_ex", "nvfp4_gemv_plan",
-              "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version"):
+              "nvfp4_status_string", "nvfp4_last_error", "nvfp4_abi_version",
+              "nvfp4_plan_for_limits"):
         assert n in names
 
 
@@ -46,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_status_strings(lib):
     import decode_nvfp4_gemv_gb300 as pkg
 
-    assert pkg.nvfp4_abi_version() == 4
+    assert pkg.nvfp4_abi_version() == 5
     assert pkg.nvfp4_status_string(0) == "ok"
     assert pkg.nvfp4_status_string(2) == "misaligned pointer"
     assert pkg.nvfp4_status_string(99) == "unknown status"

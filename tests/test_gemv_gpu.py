@@ -168,6 +168,23 @@ def test_auto_plans_are_complete(pkg):
             assert p.kernel in (3, 4) and p.stages >= 2 and p.tile_rows >= 1
 
 
+def test_device_free_planner_matches_the_device(pkg):
+    """nvfp4_plan_for_limits with this device's own limits gives the plans its launches use."""
+    props = torch.cuda.get_device_properties(0)
+    lim = {}
+    for key, attr in (("sms", "multi_processor_count"),
+                      ("max_smem_optin", "shared_memory_per_block_optin"),
+                      ("max_smem_sm", "shared_memory_per_multiprocessor")):
+        if not hasattr(props, attr):
+            pytest.skip(f"torch does not report {attr}")
+        lim[key] = int(getattr(props, attr))
+    for M, K, L in [(7168, 16384, 1), (4096, 7168, 8), (7168, 2048, 4), (3584, 6144, 16),
+                    (7168, 16384, 80), (4096, 7168, 64), (270000, 16384, 5), (128, 256, 1),
+                    (1000, 1040, 3), (64, 7168, 3), (7168, 32768, 1)]:
+        assert (pkg.nvfp4_plan_for_limits(M, K, L, **lim).as_dict()
+                == pkg.nvfp4_gemv_plan(M, K, L).as_dict()), (M, K, L)
+
+
 def test_auto_plans_fill_their_waves(pkg):
     """Batch counts that do not divide the CTA slots, or whose one-wave CTAs would hold too many
     rows, still get the register-vector kernel with a well-filled last wave."""

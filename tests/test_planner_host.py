@@ -1,0 +1,151 @@
+"""The planner without a GPU, through nvfp4_plan_for_limits (the C ABI's device-free planning
+entry point).
+
+It checks:
+- the plans the four large decode workloads get on GB300's limits (the ones the bench reports);
+- that every automatic plan over a grid of shapes takes the register-vector TMA kernel with a
+  well-filled last wave;
+- that plans scale with the device's SM count;
+- that a forced plan is honoured field by field, or refused with the status a launch would
+  return;
+- that implausible limits and shapes are rejected.
+"""
+import pytest
+
+import decode_nvfp4_gemv_gb300 as pkg
+
+
+KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV, KERNEL_TC = 2, 3, 4, 5
+INVALID, UNSUPPORTED = 1, 3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from decode_nvfp4_gemv_gb300 import build
+
+    build.build()
+    return pkg.load_library()
+
+
+def plan(M, K, L, forced=None, **lim):
+    return pkg.nvfp4_plan_for_limits(M, K, L, plan=forced, **lim).as_dict()
+
+
+def status_of(M, K, L, forced=None, **lim):
+    with pytest.raises(pkg.NVFP4Error) as e:
+        pkg.nvfp4_plan_for_limits(M, K, L, plan=forced, **lim)
+    return e.value.status
+
+
+# (M, K, L): kernel, CTAs per batch, consumer warps, 1024-element segments per warp, tile rows,
+# ring stages -- one wave of 304 CTAs (two per SM) for each workload
+DECODE_PLANS = {
+    (7168, 16384, 1): (KERNEL_TMA_RV, 304, 8, 2, 4, 2),
+    (4096, 7168, 8): (KERNEL_TMA_RV, 38, 7, 1, 12, 2),
+    (7168, 2048, 4): (KERNEL_TMA_RV, 76, 12, 1, 24, 2),
+    (3584, 6144, 16): (KERNEL_TMA_RV, 19, 12, 1, 16, 2),
+}
+
+
+@pytest.mark.parametrize("shape", list(DECODE_PLANS), ids=lambda s: "x".join(map(str, s)))
+def test_decode_workload_plans_on_gb300(shape):
+    p = plan(*shape, forced={"flags": 1})
+    got = (p["kernel"], p["ctas_per_batch"], p["warps_per_cta"], p["k_split"], p["tile_rows"],
+           p["stages"])
+    assert got == DECODE_PLANS[shape]
+    assert p["flags"] == 1 and p["rows_per_warp"] == 4
+    assert p["ctas_per_batch"] * shape[2] == 2 * 152
+
+
+def _fill(grid, slots):
+    return grid / (-(-grid // slots) * slots)
+
+
+def test_automatic_plans_fill_their_waves():
+    """Every shape with at least 8 rows per CTA slot and K % 256 == 0 (K <= 16384, two CTAs per
+    SM) gets the register-vector kernel, a valid warp mapping and a last wave >= 95% full."""
+    n = 0
+    for K in (256, 512, 1024, 2048, 3072, 4096, 6144, 7168, 16384):
+        nseg = -(-K // 1024)
+        for M in (256, 1000, 3584, 4096, 7168, 20000, 100000):
+            for L in (1, 2, 3, 5, 7, 8, 16, 24, 33, 50, 64, 80, 100, 150, 304, 500):
+                if M * L < 8 * 304:
+                    continue
+                p = plan(M, K, L)
+                n += 1
+                assert p["kernel"] == KERNEL_TMA_RV, (M, K, L, p)
+                W, P = p["warps_per_cta"], p["ctas_per_batch"]
+                assert 1 <= P <= M and 1 <= W <= 16
+                assert (nseg % W == 0 and p["k_split"] == nseg // W <= 2) or \
+                       (W % nseg == 0 and p["k_split"] == 1), (M, K, L, p)
+                assert 1 <= p["tile_rows"] <= 256 and 2 <= p["stages"] <= 8
+                assert _fill(P * L, 304) >= 0.95, (M, K, L, p)
+    assert n > 700
+
+
+def test_plans_follow_the_sm_count():
+    half = dict(sms=76, max_smem_optin=232448, max_smem_sm=233472)
+    assert plan(7168, 16384, 1, **half)["ctas_per_batch"] == 152
+    assert plan(7168, 2048, 4, **half)["ctas_per_batch"] == 38
+    assert plan(4096, 7168, 8, **half)["ctas_per_batch"] == 19
+
+
+def test_wide_k_keeps_two_ctas_per_sm():
+    """K = 32768 (18 KB per row): tiles shrink below four rows so that two CTAs still share an
+    SM, and 16 warps take two 1024-element segments each."""
+    p = plan(7168, 32768, 1)
+    assert p["kernel"] == KERNEL_TMA_RV and p["ctas_per_batch"] == 304
+    assert p["tile_rows"] < 4 and p["warps_per_cta"] == 16 and p["k_split"] == 2
+
+
+def test_planning_is_deterministic_and_forced_plans_are_echoed():
+    for shape in list(DECODE_PLANS) + [(20000, 4096, 33), (100000, 16384, 80)]:
+        a = plan(*shape)
+        assert plan(*shape) == a
+        forced = {k: v for k, v in a.items()}
+        assert plan(*shape, forced=forced) == a
+
+
+@pytest.mark.parametrize("forced", [
+    {"kernel": KERNEL_TC, "k_split": 9}, {"kernel": KERNEL_TC, "stages": 7},
+    {"kernel": KERNEL_TC, "stages": 1}, {"kernel": KERNEL_TC, "warps_per_cta": 8},
+    {"kernel": KERNEL_TC, "tile_rows": 64}, {"kernel": KERNEL_TMA, "tile_rows": 300},
+    {"kernel": KERNEL_TMA_RV, "stages": 9}, {"kernel": KERNEL_TMA_RV, "stages": 1},
+    {"kernel": KERNEL_TMA_RV, "warps_per_cta": 17}, {"kernel": KERNEL_TMA_RV, "rows_per_warp": 2},
+    {"kernel": 9}, {"flags": 0x100}, {"ctas_per_batch": -1},
+], ids=lambda f: ",".join(f"{k}={v}" for k, v in f.items()))
+def test_forced_plans_out_of_range_are_refused(forced):
+    assert status_of(7168, 2048, 4, forced=forced) == UNSUPPORTED
+
+
+def test_kernels_that_need_k_multiples_refuse_other_k():
+    for kernel in (KERNEL_TMA, KERNEL_TMA_RV, KERNEL_TC):
+        assert status_of(512, 1056, 2, forced={"kernel": kernel}) == UNSUPPORTED
+    assert status_of(512, 1040, 2, forced={"kernel": KERNEL_STREAM}) == UNSUPPORTED
+    assert plan(512, 1040, 2)["kernel"] == 1            # any K % 16 == 0: the simple kernel
+    assert plan(512, 1056, 2)["kernel"] in (1, 2)       # K % 32 == 0: CUDA-core kernels
+
+
+def test_tensor_core_plans():
+    p = plan(7168, 16384, 1, forced={"kernel": KERNEL_TC})
+    assert p["kernel"] == KERNEL_TC and p["tile_rows"] == 128 and p["warps_per_cta"] == 4
+    assert 2 <= p["k_split"] <= 8 and 2 <= p["stages"] <= 6   # 56 tiles leave slots: split K
+    q = plan(7168, 16384, 16, forced={"kernel": KERNEL_TC})
+    assert q["k_split"] == 1                               # 896 tiles fill the GPU unsplit
+    r = plan(7168, 512, 1, forced={"kernel": KERNEL_TC, "k_split": 2})
+    assert r["k_split"] == 2
+    assert status_of(7168, 512, 1, forced={"kernel": KERNEL_TC, "k_split": 3}) == UNSUPPORTED
+
+
+@pytest.mark.parametrize("lim", [dict(sms=0), dict(max_smem_optin=512),
+                                 dict(max_smem_sm=1000, max_smem_optin=2000)],
+                         ids=["no SMs", "tiny smem", "sm smem below cta smem"])
+def test_implausible_limits_are_rejected(lim):
+    assert status_of(7168, 16384, 1, **lim) == INVALID
+
+
+def test_shapes_are_checked_like_the_launching_entry_points():
+    assert status_of(0, 256, 1) == INVALID
+    assert status_of(16, 256, 0) == INVALID
+    assert status_of(16, 40, 1) == INVALID                 # K % 16 != 0
+    assert status_of(2 ** 31, 256, 1) == UNSUPPORTED
