@@ -577,7 +577,46 @@ def time_small_n(pkg, device, stream, steps, warmup, dist, M=7168, K=16384, Ns=(
         row["speedup"] = round(row["cuda_cores_rv"]["us_per_call"] /
                                row["tensor_cores"]["us_per_call"], 2)
         out[f"N={N}"] = row
+    out["context_torch_scaled_mm"] = time_scaled_mm_context(device, stream, steps, warmup, dist,
+                                                            As, Ss, M, K)
     return out
+
+
+def time_scaled_mm_context(device, stream, steps, warmup, dist, As, Ss, M, K, N=16):
+    """Context, not this library: the route the pages take for a small batch of tokens,
+    torch._scaled_mm on NVFP4 operands (a cuBLASLt kernel), on the same rotated weight bytes and
+    byte count.  Its vector side must be a multiple of 16, so N < 16 pads to 16 and costs the same.
+    The block scales are one constant byte (1.0), so their tile layout does not matter: this times
+    the call and compares no values."""
+    import torch
+
+    if not hasattr(torch, "float4_e2m1fn_x2"):
+        return {"unavailable": "this torch has no float4_e2m1fn_x2 type"}
+    rup = lambda x, m: (x + m - 1) // m * m
+    ncp = len(As)
+    a4 = [a.view(torch.float4_e2m1fn_x2) for a in As]
+    sa = [torch.full((rup(M, 128) * rup(K // 16, 4),), 0x38, dtype=torch.uint8,
+                     device=device).view(torch.float8_e4m3fn) for _ in range(ncp)]
+    b = torch.from_numpy(workloads.random_workload(1, K, N, seed=3).b).to(device)
+    b4 = b.view(torch.float4_e2m1fn_x2)
+    sb = torch.full((rup(N, 128) * rup(K // 16, 4),), 0x38, dtype=torch.uint8,
+                    device=device).view(torch.float8_e4m3fn)
+    byt = M * K * 9 // 16 + N * K * 9 // 16 + 2 * M * N
+    peak, _ = measured_peak_gbs()
+    res = {"route": "torch._scaled_mm, NVFP4 operands (cuBLASLt), vector side padded to 16",
+           "N": N, "values": "not compared (timing only)"}
+    for name, od in (("fp16_out", torch.float16), ("bf16_out", torch.bfloat16)):
+        try:
+            def fn(i, od=od):
+                torch._scaled_mm(a4[i % ncp], b4.t(), sa[i % ncp], sb, out_dtype=od)
+            sec, calls = _graph_time(fn, stream, steps, warmup, dist, device)
+        except Exception as ex:  # an older torch or a cuBLASLt without this path
+            res[name] = {"unavailable": f"{type(ex).__name__}: {str(ex)[:120]}"}
+            continue
+        gbs = byt * calls / sec / 1e9
+        res[name] = {"us_per_call": round(sec / calls * 1e6, 3), "GB/s": round(gbs, 2),
+                     "frac": round(gbs / peak, 4)}
+    return res
 
 
 def time_tc_n1(pkg, w, sets, outs, stream, steps, warmup, dist, device):
