@@ -691,6 +691,20 @@ def run_ours(args):
     # correctness spot check of the timed launches' last output (NaN would mean an unwritten c)
     assert not torch.isnan(outs[(args.steps - 1) % n_copies]).any().item()
 
+    # spread: after the timed region, 20 more replays of the same graph, each between two events
+    n_rep = 20
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(n_rep):
+            g_full.replay()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize(device)
+    per = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 / chunk for i in range(n_rep))
+    spread = {"replays": n_rep, "calls_per_replay": chunk,
+              "p10_us": round(per[n_rep // 10], 3), "median_us": round(per[n_rep // 2], 3),
+              "p90_us": round(per[(9 * n_rep) // 10], 3)}
+
     strict = None
     if not args.plan and not args.no_strict:
         steps_s = min(args.steps, 20000)
@@ -759,6 +773,7 @@ def run_ours(args):
             "warmup": args.warmup,
             "ms_per_step": round(slowest / args.steps * 1e3, 6),
             "us_per_call": round(per_call_s * 1e6, 3),
+            "us_per_call_spread": spread,
             "pct_of_peak": round(100.0 * achieved / peak, 2),
             "higher_is_better": True,
             "scaling": "weak",
