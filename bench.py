@@ -50,7 +50,7 @@ GRAPH_CHUNK = 1000
 FLAG_EARLY_WEIGHTS = 1      # nvfp4_plan.flags: A and sfa are not written by preceding work
 FLAG_QUANTIZE_IN_GEMV = 4   # nvfp4_plan.flags: quantize the bf16 vector inside the GEMV kernel
 KERNEL_NAMES = {1: "gemv_simple_kernel", 2: "gemv_stream_kernel", 3: "gemv_tma_kernel",
-                4: "gemv_tma_rv_kernel"}
+                4: "gemv_tma_rv_kernel", 5: "gemv_tc_kernel", 6: "gemv_shift_kernel"}
 DEFAULT_PEAK_GBS = 6800.0   # only if MEASURED_PEAKS.json is absent
 
 
@@ -438,42 +438,21 @@ def time_general(pkg, w, stream, steps, warmup, dist, n_copies):
         sets.append(s)
     outs = [torch.empty((w.L, w.M), dtype=torch.float16, device=dev) for _ in range(n_copies)]
 
-    def call(i):
-        s = sets[i % n_copies]
-        pkg.nvfp4_gemv_batched(s["A"], s["sfa"], w.g_a, s["b"], s["sfb"], w.g_b, outs[i % n_copies],
-                               w.M, w.K, w.L, stream=stream)
-
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        for i in range(max(warmup, 1)):
-            call(i)
-    stream.synchronize()
-    chunk = min(GRAPH_CHUNK, steps)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(chunk):
-            call(i)
-    reps = max(1, steps // chunk)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g.replay()
-        barrier(dist)
-        torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(dist)
-    sec = ev0.elapsed_time(ev1) / 1e3
-    calls = reps * chunk
-    tot, slow = aggregate(dist, w.algorithmic_bytes * calls, sec)
     peak, _ = measured_peak_gbs()
-    del g
-    return {"inputs": "A, sfa, b, sfb each 1 byte past a 16-byte boundary",
-            "kernel": KERNEL_NAMES.get(1), "us_per_call": round(sec / calls * 1e6, 3),
-            "calls": calls, "GB/s": round(tot / slow / 1e9, 2), "frac": round(tot / slow / 1e9 / peak, 4)}
+    out = {"inputs": "A, sfa, b, sfb each 1 byte past a 16-byte boundary"}
+    # the automatic plan (the shift kernel: aligned loads shifted into place), then the byte-load
+    # kernel forced on the same inputs
+    for name, plan in (("automatic", None), ("byte_loads", {"kernel": 1})):
+        def fn(i, plan=plan):
+            s = sets[i % n_copies]
+            pkg.nvfp4_gemv_batched_ex(s["A"], s["sfa"], w.g_a, s["b"], s["sfb"], w.g_b,
+                                      outs[i % n_copies], w.M, w.K, w.L, stream=stream, plan=plan)
+        sec, calls = _graph_time(fn, stream, steps, warmup, dist, dev)
+        tot, slow = aggregate(dist, w.algorithmic_bytes * calls, sec)
+        out[name] = {"kernel": KERNEL_NAMES[6 if plan is None else 1],
+                     "us_per_call": round(sec / calls * 1e6, 3), "calls": calls,
+                     "GB/s": round(tot / slow / 1e9, 2), "frac": round(tot / slow / 1e9 / peak, 4)}
+    return out
 
 
 def _graph_time(fn, stream, steps, warmup, dist, dev):

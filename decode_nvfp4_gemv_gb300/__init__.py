@@ -25,7 +25,7 @@ from .build import LIB_PATH
 
 __all__ = [
     "NVFP4Error", "Plan", "KERNEL_AUTO", "KERNEL_SIMPLE", "KERNEL_STREAM", "KERNEL_TMA",
-    "KERNEL_TMA_RV", "KERNEL_TC", "nvfp4_gemm_small_n", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "FLAG_QUANTIZE_IN_GEMV",
+    "KERNEL_TMA_RV", "KERNEL_TC", "KERNEL_SHIFT", "nvfp4_gemm_small_n", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "FLAG_QUANTIZE_IN_GEMV",
     "ROUND_HALF_STEP_TABLE",
     "ROUND_NEAREST_EVEN", "nvfp4_quantize_activation", "nvfp4_gemv_batched_bf16", "OUT_F16",
     "OUT_BF16", "nvfp4_gemv_grouped", "library_path",
@@ -34,7 +34,8 @@ __all__ = [
     "DeviceLimits", "GB300_LIMITS", "nvfp4_plan_for_limits",
 ]
 
-KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV, KERNEL_TC = 0, 1, 2, 3, 4, 5
+KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV, KERNEL_TC, KERNEL_SHIFT = (
+    0, 1, 2, 3, 4, 5, 6)
 FLAG_EARLY_WEIGHTS, FLAG_NO_PDL, FLAG_QUANTIZE_IN_GEMV = 1, 2, 4
 ROUND_HALF_STEP_TABLE, ROUND_NEAREST_EVEN = 0, 1
 OUT_F16, OUT_BF16 = 0, 1

@@ -14,6 +14,7 @@
 
 #include "../../include/nvfp4_gemv.h"
 #include "gemv_kernels.cuh"
+#include "gemv_shift.cuh"
 #include "gemv_tc.cuh"
 #include "gemv_tma.cuh"
 
@@ -87,6 +88,8 @@ void init_device(int dev) {
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false>, d.max_smem_optin)) ||
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, true>, d.max_smem_optin)) ||
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, true>, d.max_smem_optin)) ||
+      (e = cudaFuncSetAttribute(nvfp4::gemv_shift_kernel,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin)) ||
       (e = cudaFuncSetAttribute(nvfp4::gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 d.max_smem_optin))) {
     d.err = e;
@@ -227,6 +230,49 @@ int plan_simple(const DeviceInfo& d, int64_t M, int64_t L, const nvfp4_plan& f, 
   pl->warps_per_cta = W;
   pl->ctas_per_batch = (int32_t)std::max<int64_t>(1, ceil_div(ctas, L));
   pl->rows_per_warp = 1;
+  pl->k_split = 1;
+  return NVFP4_OK;
+}
+
+// CTAs per batch for a grid of whole waves where L allows: from one wave of `slots` CTA slots,
+// the smallest P up to 8 P0 + 8 whose last wave is at least 1% fuller than the best so far.
+int64_t wave_filling_ctas(int64_t M, int64_t L, int64_t slots) {
+  const int64_t P0 = std::min<int64_t>(M, std::max<int64_t>(1, slots / L));
+  int64_t best = P0;
+  double best_fill = -1.0;
+  for (int64_t p = P0; p <= std::min<int64_t>(M, 8 * P0 + 8); ++p) {
+    const int64_t grid = p * L;
+    const double fill = (double)grid / (double)(ceil_div(grid, slots) * slots);
+    if (fill <= best_fill + 0.01) continue;
+    best = p;
+    best_fill = fill;
+    if (fill >= 0.999) break;
+  }
+  return best;
+}
+
+// General-alignment kernel: CTAs of 8 warps over contiguous rows, two per SM when the staged
+// vector leaves room for two.
+int plan_shift(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan& f,
+               nvfp4_plan* pl) {
+  const int64_t smem = nvfp4::shift_smem_bytes(K);
+  if (smem > d.max_smem_optin)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                "shift kernel: the vector for K=%lld needs %lld bytes of shared memory",
+                (long long)K, (long long)smem);
+  if (f.warps_per_cta > 8)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "shift kernel: at most 8 warps per CTA");
+  if (f.rows_per_warp && f.rows_per_warp != 4)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "shift kernel processes 4 rows per warp");
+  const int W = f.warps_per_cta ? f.warps_per_cta : 8;
+  const int64_t occ = smem + 1024 <= d.max_smem_sm / 2 ? 2 : 1;
+  int64_t P = f.ctas_per_batch ? std::min<int64_t>(f.ctas_per_batch, M)
+                               : wave_filling_ctas(M, L, (int64_t)d.sms * occ);
+  if (P * L > (int64_t(1) << 31) - 1) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
+  pl->kernel = NVFP4_KERNEL_SHIFT;
+  pl->warps_per_cta = W;
+  pl->ctas_per_batch = (int32_t)P;
+  pl->rows_per_warp = 4;
   pl->k_split = 1;
   return NVFP4_OK;
 }
@@ -515,11 +561,11 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
   nvfp4_plan f;
   memset(&f, 0, sizeof f);
   if (forced) f = *forced;
-  if (!aligned16 && f.kernel != NVFP4_KERNEL_AUTO && f.kernel != NVFP4_KERNEL_SIMPLE)
+  if (!aligned16 && f.kernel != NVFP4_KERNEL_AUTO && f.kernel != NVFP4_KERNEL_SIMPLE &&
+      f.kernel != NVFP4_KERNEL_SHIFT)
     return fail(NVFP4_ERR_MISALIGNED,
-                "kernel %d needs 16-byte aligned A, sfa, b and sfb (the simple kernel takes any)",
+                "kernel %d needs 16-byte aligned A, sfa, b and sfb (SHIFT and SIMPLE take any)",
                 f.kernel);
-  if (!aligned16) f.kernel = NVFP4_KERNEL_SIMPLE;
   if (f.flags & ~(NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_NO_PDL | NVFP4_FLAG_QUANTIZE_IN_GEMV))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown plan flags 0x%x", (unsigned)f.flags);
   if (f.warps_per_cta < 0 || f.rows_per_warp < 0 || f.k_split < 0 || f.ctas_per_batch < 0 ||
@@ -533,12 +579,14 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
     case NVFP4_KERNEL_TMA: st = plan_tma(d, M, K, L, f, false, pl); break;
     case NVFP4_KERNEL_TMA_RV: st = plan_tma(d, M, K, L, f, true, pl); break;
     case NVFP4_KERNEL_TC: st = plan_tc(d, M, K, tc_groups, f, pl); break;
+    case NVFP4_KERNEL_SHIFT: st = plan_shift(d, M, K, L, f, pl); break;
     case NVFP4_KERNEL_AUTO: {
-      // the TMA ring (vector in registers if the warp mapping allows) when every CTA gets at least
-      // 8 rows, else the stream kernel, else the simple kernel
+      // 16-byte aligned operands: the TMA ring (vector in registers if the warp mapping allows)
+      // when every CTA gets at least 8 rows, else the stream kernel; any other alignment or K:
+      // the shift kernel, else the simple kernel
       const int64_t rows_per_cta = (M * L) / std::max<int64_t>(1, (int64_t)d.sms * 2);
       st = -1;
-      if (K % 256 == 0 && rows_per_cta >= 8) {
+      if (aligned16 && K % 256 == 0 && rows_per_cta >= 8) {
         char saved[sizeof g_last_error];
         memcpy(saved, g_last_error, sizeof saved);
         for (bool rv : {true, false}) {
@@ -550,8 +598,21 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
         }
         memcpy(g_last_error, saved, sizeof saved);
       }
-      if (st != NVFP4_OK)
-        st = stream_ok(d, K) ? plan_stream(d, M, K, L, f, pl) : plan_simple(d, M, L, f, pl);
+      if (st == NVFP4_OK) break;
+      memset(pl, 0, sizeof *pl);
+      if (aligned16 && stream_ok(d, K)) {
+        st = plan_stream(d, M, K, L, f, pl);
+        break;
+      }
+      // any alignment, any K % 16 == 0: aligned loads shifted into place when the vector fits
+      char saved[sizeof g_last_error];
+      memcpy(saved, g_last_error, sizeof saved);
+      st = plan_shift(d, M, K, L, f, pl);
+      memcpy(g_last_error, saved, sizeof saved);
+      if (st != NVFP4_OK) {
+        memset(pl, 0, sizeof *pl);
+        st = plan_simple(d, M, L, f, pl);
+      }
       break;
     }
     default: return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown kernel %d", f.kernel);
@@ -680,6 +741,32 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                   "the tensor-core kernel takes packed vectors and fp16 output only");
     return launch_tc(d, pl, A, sfa, g_a, b, sfb, g_b, c, M, K, L, 1, M, stream);
+  }
+  if (pl.kernel == NVFP4_KERNEL_SHIFT) {
+    if (fx) return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "the shift kernel takes a packed vector");
+    nvfp4::ShiftArgs a;
+    a.A = A; a.sfa = sfa; a.b = b; a.sfb = sfb; a.c = c;
+    a.g_a = g_a; a.g_b = g_b;
+    a.M = M; a.K = K; a.L = L;
+    const int64_t n_mats = G.E > 0 ? (int64_t)G.E : (G.shared_a ? 1 : L);  // matrices in A
+    a.a_bytes = n_mats * M * (K / 2);
+    a.P = pl.ctas_per_batch;
+    a.G = G;
+    a.out_bf16 = out_bf16;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)(pl.ctas_per_batch * L));
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)nvfp4::shift_smem_bytes(K);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (pl.flags & NVFP4_FLAG_NO_PDL) ? 0 : 1;
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, nvfp4::gemv_shift_kernel, a);
+    if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
+    return NVFP4_OK;
   }
   if (pl.kernel == NVFP4_KERNEL_SIMPLE) {
     const int64_t grid = std::min<int64_t>((int64_t)pl.ctas_per_batch * L, (int64_t(1) << 31) - 1);

@@ -47,11 +47,11 @@
  *   NVFP4_ERR_INVALID_VALUE   M < 0, L < 0, K <= 0, K % 16 != 0, a NULL pointer when M*L > 0,
  *                             c overlapping an input, or an inaccessible pointer
  *   NVFP4_ERR_UNSUPPORTED_SHAPE  M, L or K/2 above 2^31 - 1, or an invalid forced plan
- *   NVFP4_ERR_MISALIGNED      c not 2-byte aligned, or a forced plan other than SIMPLE while A,
- *                             sfa, b or sfb is not 16-byte aligned
- *   Any alignment of A, sfa, b and sfb is accepted: when one of them is not 16-byte aligned the
- *   automatic plan is the simple kernel (byte loads), the general path for any alignment and any
- *   K % 16 == 0.
+ *   NVFP4_ERR_MISALIGNED      c not 2-byte aligned, or a forced plan other than SIMPLE or SHIFT
+ *                             while A, sfa, b or sfb is not 16-byte aligned
+ *   Any alignment of A, sfa, b and sfb is accepted: when one of them is not 16-byte aligned (or
+ *   K % 32 != 0) the automatic plan is the SHIFT kernel (aligned 16-byte loads shifted into
+ *   place), or the SIMPLE kernel (byte loads) when the vector does not fit shared memory.
  *   NVFP4_ERR_ARCH            the current device is not compute capability 10.3 (GB300)
  *   NVFP4_ERR_CUDA            a CUDA runtime call or the launch failed (nvfp4_last_error() has
  *                             the runtime's message)
@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define NVFP4_ABI_VERSION 5
+#define NVFP4_ABI_VERSION 6
 
 typedef enum nvfp4_status {
   NVFP4_OK = 0,
@@ -88,11 +88,15 @@ typedef enum nvfp4_kernel {
   NVFP4_KERNEL_TMA_RV = 4,  /* as TMA with each consumer warp's vector slice held in registers;
                                needs K % 256 == 0 and the warp count to divide the number of
                                1024-element K segments (or be a multiple of it) */
-  NVFP4_KERNEL_TC = 5       /* tensor cores (tcgen05.mma kind::mxf4nvf4, block scales applied by
+  NVFP4_KERNEL_TC = 5,      /* tensor cores (tcgen05.mma kind::mxf4nvf4, block scales applied by
                                the MMA, fp32 accumulator in tensor memory): 128-row tiles x up to
                                16 vectors, K split over a cluster of k_split (<= 8) CTAs with a
                                deterministic on-chip reduction; needs K % 256 == 0 and
                                non-negative block scales (the MMA reads them as unsigned E4M3) */
+  NVFP4_KERNEL_SHIFT = 6    /* any K % 16 == 0 and any byte alignment of A, sfa, b, sfb: 16-byte
+                               aligned loads around each lane's bytes, funnel-shifted into place,
+                               vector staged in shared memory; needs the vector to fit there
+                               (about 2.25 bytes per element of K) */
 } nvfp4_kernel;
 
 /* Plan flags. */
@@ -120,11 +124,11 @@ typedef struct nvfp4_plan {
   int32_t k_split;         /* STREAM: K slices per row inside a CTA (1 .. ceil(K/1024));
                               TMA_RV: 1024-element segments per warp (filled in by the planner);
                               TC: K slices = cluster size (1 .. 8, at most K/256) */
-  int32_t ctas_per_batch;  /* SIMPLE, STREAM, TMA*: CTAs sharing one batch's rows (1 .. M);
+  int32_t ctas_per_batch;  /* SIMPLE, STREAM, TMA*, SHIFT: CTAs sharing one batch's rows (1 .. M);
                               TC with k_split 1: persistent CTAs for the whole launch (0 = as many
                               as fit); TC with k_split > 1: filled in (tiles x k_split) */
-  int32_t warps_per_cta;   /* SIMPLE: 1 .. 8; STREAM: 1 .. 16; TMA*: consumer warps 1 .. 16 (one
-                              producer warp is added); TC: 4 (fixed) */
+  int32_t warps_per_cta;   /* SIMPLE, SHIFT: 1 .. 8; STREAM: 1 .. 16; TMA*: consumer warps 1 .. 16
+                              (one producer warp is added); TC: 4 (fixed) */
   int32_t tile_rows;       /* TMA*: rows per ring stage (1 .. 256); TC: 128 (fixed) */
   int32_t stages;          /* TMA*: ring stages (2 .. 8); TC: 2 .. 6 stages of 256 elements */
   int32_t flags;           /* NVFP4_FLAG_* (honoured by the automatic plan too) */

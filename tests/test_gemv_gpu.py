@@ -161,7 +161,9 @@ def test_auto_plans_are_complete(pkg):
     for M, K, L in [(7168, 16384, 1), (4096, 7168, 8), (7168, 2048, 4), (3584, 6144, 16),
                     (128, 256, 1), (1, 16, 1)]:
         p = pkg.nvfp4_gemv_plan(M, K, L)
-        assert p.kernel in (1, 2, 3, 4) and p.warps_per_cta >= 1 and p.ctas_per_batch >= 1
+        assert p.kernel in (1, 2, 3, 4, 6) and p.warps_per_cta >= 1 and p.ctas_per_batch >= 1
+        if K % 32 != 0:
+            assert p.kernel == 6                            # the general-alignment kernel
         if K % 32 == 0:
             assert p.kernel in (2, 3, 4) and p.rows_per_warp in (1, 2, 4) and p.k_split >= 1
         if K % 256 == 0 and M * L >= 8 * 304:
@@ -205,8 +207,15 @@ def test_largest_stream_k_and_beyond(pkg):
     assert pkg.nvfp4_gemv_plan(6, kmax, 1).kernel in (2, 3, 4)
     check(w, run(pkg, w), f"K={kmax}")
     w2 = workloads.random_workload(3, kmax + 32, 1, seed=4)
-    assert pkg.nvfp4_gemv_plan(3, kmax + 32, 1).kernel == 1
+    assert pkg.nvfp4_gemv_plan(3, kmax + 32, 1).kernel == 6   # the shift kernel's bound is wider
     check(w2, run(pkg, w2), f"K={kmax + 32}")
+    # past the shift kernel's shared memory (2.25 bytes per element of K): the byte-load kernel
+    smem = torch.cuda.get_device_properties(0).shared_memory_per_block_optin \
+        if hasattr(torch.cuda.get_device_properties(0), "shared_memory_per_block_optin") else 232448
+    k3 = (int(smem / 2.25) // 32 + 1) * 32
+    assert pkg.nvfp4_gemv_plan(3, k3, 1).kernel == 1
+    w3 = workloads.random_workload(3, k3, 1, seed=5)
+    check(w3, run(pkg, w3), f"K={k3}")
 
 
 # ------------------------------------------------------------------ the five workloads, full size

@@ -1,6 +1,9 @@
 """GPU parity of the general path: any byte alignment of A, sfa, b and sfb, and any K % 16 == 0
 (K not a multiple of 32 included), through the C ABI against the oracle.  The planner sends such
-calls to the simple kernel (byte loads); the vector-load and TMA kernels refuse them."""
+calls to the shift kernel (aligned 16-byte loads funnel-shifted into place); the simple kernel
+(byte loads) takes them when forced; the vector-load and TMA kernels refuse them.  The buffers sit
+inside larger allocations filled with other bytes, so a read before the first or past the last
+byte of an operand would change the result."""
 import numpy as np
 import pytest
 import torch
@@ -48,6 +51,16 @@ def test_unaligned_inputs(pkg, offsets):
     torch.cuda.synchronize()
     ref, T = oracle.gemv(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, w.M, w.K, w.L)
     assert_parity(c.cpu().numpy(), ref, T, f"offsets {offsets}")
+    auto = c.cpu().numpy()
+    for plan in (dict(kernel=6), dict(kernel=6, warps_per_cta=3, ctas_per_batch=5),
+                 dict(kernel=6, flags=2), dict(kernel=1)):
+        c2 = torch.full((w.L, w.M), float("nan"), dtype=torch.float16, device="cuda")
+        pkg.nvfp4_gemv_batched_ex(args[0], args[1], w.g_a, args[2], args[3], w.g_b, c2, w.M, w.K,
+                                  w.L, plan=plan)
+        torch.cuda.synchronize()
+        assert_parity(c2.cpu().numpy(), ref, T, f"offsets {offsets} {plan}")
+        if plan.get("kernel") == 6:   # the automatic plan is the shift kernel: same bits
+            assert np.array_equal(c2.cpu().numpy().view(np.uint16), auto.view(np.uint16))
     for plan in (dict(kernel=2), dict(kernel=3), dict(kernel=4)):
         with pytest.raises(pkg.NVFP4Error) as e:
             pkg.nvfp4_gemv_batched_ex(args[0], args[1], w.g_a, args[2], args[3], w.g_b, c, w.M,
@@ -83,3 +96,74 @@ def test_unaligned_grouped(pkg):
     from oracle import grouped as G
     ref, T = G.gemv_grouped(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, w.expert_of, w.M, w.K)
     assert_parity(c.cpu().numpy(), ref, T, "unaligned grouped")
+
+
+SHIFT_SHAPES = [(1, 16, 1), (5, 1040, 3), (257, 2064, 2), (130, 4096, 1), (33, 16400, 2),
+                (1000, 7184, 1)]
+
+
+@pytest.mark.parametrize("shape", SHIFT_SHAPES, ids=[f"{m}x{k}x{l}" for m, k, l in SHIFT_SHAPES])
+@pytest.mark.parametrize("offset", [0, 1, 7, 8, 15])
+def test_shift_kernel_shapes_and_offsets(pkg, shape, offset):
+    """Ragged M, K % 32 == 16 and K % 1024 != 0, every row-start residue mod 16 (K % 32 == 16
+    alternates it), A placed so that its first chunk begins before it and its last ends past it."""
+    M, K, L = shape
+    w = workloads.random_workload(M, K, L, seed=M * 7 + K + offset,
+                                  scale_bytes=workloads.pow2_scale_bytes(-4, 3), g_a=0.75, g_b=1.25)
+    keep, args = [], []
+    for name, off in zip(("A", "sfa", "b", "sfb"), (offset, (offset * 3) % 16, offset, 0)):
+        v, raw = placed(getattr(w, name), off)
+        keep.append(raw)
+        args.append(v)
+    ref, T = oracle.gemv(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, M, K, L)
+    for plan in (None, dict(kernel=6), dict(kernel=6, warps_per_cta=1, ctas_per_batch=1),
+                 dict(kernel=6, warps_per_cta=8, ctas_per_batch=M)):
+        c = torch.full((L, M), float("nan"), dtype=torch.float16, device="cuda")
+        pkg.nvfp4_gemv_batched_ex(args[0], args[1], w.g_a, args[2], args[3], w.g_b, c, M, K, L,
+                                  plan=plan)
+        torch.cuda.synchronize()
+        out = c.cpu().numpy()
+        assert not np.isnan(out).any(), plan
+        assert_parity(out, ref, T, f"{shape} offset {offset} {plan}")
+
+
+def test_shift_kernel_small_n_shares_a(pkg):
+    """Unaligned operands of the small-N entry point: the shift kernel reads the one matrix for
+    every vector."""
+    M, K, N = 300, 2064, 5
+    wa = workloads.random_workload(M, K, 1, seed=77, scale_bytes=workloads.pow2_scale_bytes(-3, 2))
+    wv = workloads.random_workload(1, K, N, seed=78, scale_bytes=workloads.pow2_scale_bytes(-3, 2))
+    A, rA = placed(wa.A[0], 5)
+    sfa, rS = placed(wa.sfa[0], 3)
+    b, rB = placed(wv.b, 9)
+    sfb, rSB = placed(wv.sfb, 1)
+    c = torch.full((N, M), float("nan"), dtype=torch.float16, device="cuda")
+    pkg.nvfp4_gemm_small_n(A, sfa, wa.g_a, b, sfb, wv.g_b, c, M, K, N)
+    torch.cuda.synchronize()
+    ref, T = oracle.gemv(np.repeat(wa.A, N, 0), np.repeat(wa.sfa, N, 0), wa.g_a, wv.b, wv.sfb,
+                         wv.g_b, M, K, N)
+    assert_parity(c.cpu().numpy(), ref, T, "small N, unaligned")
+
+
+def test_shift_kernel_grouped_forms(pkg):
+    """The grouped form (per-token routing) through the shift kernel, with a token that no expert
+    owns."""
+    w = workloads.make_grouped("g0")
+    A, rA = placed(w.A, 11)
+    sfa, rS = placed(w.sfa, 2)
+    b, rB = placed(w.b, 4)
+    sfb, rSB = placed(w.sfb, 7)
+    g_a = torch.from_numpy(np.ascontiguousarray(w.g_a)).cuda()
+    g_b = torch.from_numpy(np.ascontiguousarray(w.g_b)).cuda()
+    emap = np.array(w.expert_of, dtype=np.int32).copy()
+    emap[-1] = -1                                          # this token has no expert
+    from oracle import grouped as G
+    ref, T = G.gemv_grouped(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, emap, w.M, w.K)
+    for plan in (None, dict(kernel=6), dict(kernel=1)):
+        c = torch.full((w.T, w.M), float("nan"), dtype=torch.float16, device="cuda")
+        pkg.nvfp4_gemv_grouped(A, sfa, g_a, b, sfb, g_b, c, w.M, w.K, w.E, w.T,
+                               expert_of_token=torch.from_numpy(emap).cuda(), plan=plan)
+        torch.cuda.synchronize()
+        out = c.cpu().numpy()
+        assert np.all(out[-1] == 0), plan
+        assert_parity(out, ref, T, f"grouped unaligned {plan}")

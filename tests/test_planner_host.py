@@ -122,8 +122,23 @@ def test_kernels_that_need_k_multiples_refuse_other_k():
     for kernel in (KERNEL_TMA, KERNEL_TMA_RV, KERNEL_TC):
         assert status_of(512, 1056, 2, forced={"kernel": kernel}) == UNSUPPORTED
     assert status_of(512, 1040, 2, forced={"kernel": KERNEL_STREAM}) == UNSUPPORTED
-    assert plan(512, 1040, 2)["kernel"] == 1            # any K % 16 == 0: the simple kernel
+    assert plan(512, 1040, 2)["kernel"] == 6            # K % 32 == 16: the shift kernel
     assert plan(512, 1056, 2)["kernel"] in (1, 2)       # K % 32 == 0: CUDA-core kernels
+
+
+def test_shift_kernel_plans():
+    """K % 32 == 16 takes the general-alignment kernel: 8 warps, 4 rows per warp, one wave of CTA
+    slots (two per SM while the staged vector fits half an SM); a forced plan outside its range is
+    refused, and a vector too long for shared memory falls back to the byte-load kernel."""
+    p = plan(7168, 16400, 1)
+    assert (p["kernel"], p["warps_per_cta"], p["rows_per_warp"], p["ctas_per_batch"]) == \
+        (6, 8, 4, 304)
+    assert plan(4096, 7184, 8)["ctas_per_batch"] == 38
+    assert plan(7168, 2064, 1, forced={"kernel": 6})["kernel"] == 6
+    assert status_of(7168, 2064, 1, forced={"kernel": 6, "warps_per_cta": 9}) == UNSUPPORTED
+    assert status_of(7168, 2064, 1, forced={"kernel": 6, "rows_per_warp": 2}) == UNSUPPORTED
+    assert plan(64, 160016, 2)["kernel"] == 1            # 2.25 B/element of K > 227 KB
+    assert status_of(64, 160016, 2, forced={"kernel": 6}) == UNSUPPORTED
 
 
 def test_tensor_core_plans():
