@@ -449,7 +449,12 @@ def time_general(pkg, w, stream, steps, warmup, dist, n_copies):
                                       outs[i % n_copies], w.M, w.K, w.L, stream=stream, plan=plan)
         sec, calls = _graph_time(fn, stream, steps, warmup, dist, dev)
         tot, slow = aggregate(dist, w.algorithmic_bytes * calls, sec)
-        out[name] = {"kernel": KERNEL_NAMES[6 if plan is None else 1],
+        # the automatic plan for unaligned operands: the register-vector TMA kernel's unaligned
+        # form when K % 256 == 0 and every CTA slot gets at least 8 rows, else the shift kernel
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        auto = (KERNEL_NAMES[4] + " (unaligned form)"
+                if w.K % 256 == 0 and w.M * w.L // (2 * sms) >= 8 else KERNEL_NAMES[6])
+        out[name] = {"kernel": auto if plan is None else KERNEL_NAMES[1],
                      "us_per_call": round(sec / calls * 1e6, 3), "calls": calls,
                      "GB/s": round(tot / slow / 1e9, 2), "frac": round(tot / slow / 1e9 / peak, 4)}
     return out

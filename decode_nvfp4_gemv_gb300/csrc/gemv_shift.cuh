@@ -54,60 +54,6 @@ __host__ __device__ constexpr int64_t shift_smem_bytes(int64_t K) {
   return ((K + 31) / 32) * 32 * 2 + ((K + 31) / 32) * 2 * 4;
 }
 
-// 16-byte read-only load kept in L1, for data a neighbouring lane reads again.
-__device__ __forceinline__ uint4 ld_l1_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-// The 16 bytes that start d bytes into the 32 bytes lo:hi (d < 16, the same for the whole warp).
-__device__ __forceinline__ uint4 shift16(const uint4& lo, const uint4& hi, uint32_t d) {
-  const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  const uint32_t r = 8u * (d & 3u);
-  uint32_t o[4];
-  switch (d >> 2) {  // the word part of the shift: warp-uniform, so no divergence
-#define NVFP4_SHIFT_CASE(Q)                               \
-    case Q:                                               \
-      _Pragma("unroll") for (int i = 0; i < 4; ++i)       \
-        o[i] = __funnelshift_r(v[i + Q], v[i + Q + 1], r); \
-      break;
-    NVFP4_SHIFT_CASE(0)
-    NVFP4_SHIFT_CASE(1)
-    NVFP4_SHIFT_CASE(2)
-    default:
-      NVFP4_SHIFT_CASE(3)
-#undef NVFP4_SHIFT_CASE
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// The 16 bytes at p read one by one, those outside [start, end) taken as zero (the first and the
-// last chunk of a buffer).
-__device__ __forceinline__ uint4 ld16_bytes(const uint8_t* p, const uint8_t* start,
-                                            const uint8_t* end) {
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
-  for (uint32_t j = 0; j < 16u; ++j)
-    if (p + j >= start && p + j < end) w[j >> 2] |= (uint32_t)p[j] << (8u * (j & 3u));
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
-
-// The 16 bytes at p (any alignment); d = p mod 16, the same for every lane of the warp.  Only
-// bytes in [start, end) are read: when the two aligned chunks around p do not both lie inside it,
-// the bytes are loaded one by one and those outside are zero.
-__device__ __forceinline__ uint4 ld16_shifted(const uint8_t* p, uint32_t d, const uint8_t* start,
-                                              const uint8_t* end) {
-  const uint8_t* a = p - d;
-  if (a >= start && a + 32 <= end) {
-    const uint4 lo = ld_l1_v4(a);
-    if (d == 0) return lo;
-    return shift16(lo, ld_l1_v4(a + 16), d);  // the second chunk is mostly an L1 hit
-  }
-  return ld16_bytes(p, start, end);
-}
-
 __global__ void __launch_bounds__(256, 2) gemv_shift_kernel(const ShiftArgs p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int64_t K = p.K, K2 = p.K >> 1, K16 = p.K >> 4;
@@ -133,12 +79,12 @@ __global__ void __launch_bounds__(256, 2) gemv_shift_kernel(const ShiftArgs p) {
     gb = __ldcg(p.G.g_b + e);
   }
 
-  // stage b[l] as f16x2 words and sfb[l] as fp32, 16 bytes per load (shifted into place as for A;
-  // bytes past the batch's vector are zero)
+  // stage b[l] as f16x2 words and sfb[l] as fp32, 16 bytes per load through L2 (shifted into place
+  // as for A; bytes past the batch's vector are zero)
   const uint8_t* b_l = p.b + l * K2;
   const uint32_t db = (uint32_t)((uintptr_t)b_l & 15u);
   for (int64_t i = threadIdx.x; i < Kp / 32; i += blockDim.x) {
-    const uint4 v = ld16_shifted(b_l + 16 * i, db, b_l, b_l + K2);
+    const uint4 v = ld16_shifted<true>(b_l + 16 * i, db, b_l, b_l + K2);
     uint4 w0, w1, w2, w3;
     e2m1x8_to_f16x2x4(v.x, w0.x, w0.y, w0.z, w0.w);
     e2m1x8_to_f16x2x4(v.y, w1.x, w1.y, w1.z, w1.w);
@@ -154,7 +100,7 @@ __global__ void __launch_bounds__(256, 2) gemv_shift_kernel(const ShiftArgs p) {
   const uint8_t* sfb_l = p.sfb + l * K16;
   const uint32_t dsb = (uint32_t)((uintptr_t)sfb_l & 15u);
   for (int64_t i = threadIdx.x; i < (Kp / 16 + 15) / 16; i += blockDim.x) {
-    const uint4 v = ld16_shifted(sfb_l + 16 * i, dsb, sfb_l, sfb_l + K16);
+    const uint4 v = ld16_shifted<true>(sfb_l + 16 * i, dsb, sfb_l, sfb_l + K16);
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 16; ++j) {

@@ -86,6 +86,9 @@ struct TmaArgs {
   Groups G;              // grouped form (G.E > 0; never with early_weights: e(l) is read after
                          // the programmatic-launch wait)
   int32_t out_bf16;      // 1: bfloat16 output instead of fp16
+  // operands not 16-byte aligned: the 16-byte aligned interiors [lo, hi) of the A and sfa buffers,
+  // and the ends of the b and sfb buffers (unused when aligned)
+  const uint8_t *A_lo, *A_hi, *S_lo, *S_hi, *b_end, *sfb_end;
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -100,6 +103,11 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
                : "r"(a));
   return v;
 }
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
 __device__ __forceinline__ uint16_t lds_u16(uint32_t a) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
@@ -109,6 +117,71 @@ __device__ __forceinline__ float2 lds_f2(uint32_t a) {
   float2 v;
   asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
   return v;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Reading 16 bytes at any alignment (the operands' rows need not start on 16-byte boundaries).
+// ------------------------------------------------------------------------------------------------
+// 16-byte read-only load kept in L1, for data a neighbouring lane reads again.
+__device__ __forceinline__ uint4 ld_l1_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// The 16 bytes that start d bytes into the 32 bytes lo:hi (d < 16, the same for the whole warp).
+__device__ __forceinline__ uint4 shift16(const uint4& lo, const uint4& hi, uint32_t d) {
+  const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const uint32_t r = 8u * (d & 3u);
+  uint32_t o[4];
+  switch (d >> 2) {  // the word part of the shift: warp-uniform, so no divergence
+#define NVFP4_SHIFT_CASE(Q)                               \
+    case Q:                                               \
+      _Pragma("unroll") for (int i = 0; i < 4; ++i)       \
+        o[i] = __funnelshift_r(v[i + Q], v[i + Q + 1], r); \
+      break;
+    NVFP4_SHIFT_CASE(0)
+    NVFP4_SHIFT_CASE(1)
+    NVFP4_SHIFT_CASE(2)
+    default:
+      NVFP4_SHIFT_CASE(3)
+#undef NVFP4_SHIFT_CASE
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The 16 bytes at p read one by one, those outside [start, end) taken as zero (the first and the
+// last chunk of a buffer).
+__device__ __forceinline__ uint4 ld16_bytes(const uint8_t* p, const uint8_t* start,
+                                            const uint8_t* end) {
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  for (uint32_t j = 0; j < 16u; ++j)
+    if (p + j >= start && p + j < end) w[j >> 2] |= (uint32_t)p[j] << (8u * (j & 3u));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The 16 bytes at p (any alignment); d = p mod 16, the same for every lane of the warp.  Only
+// bytes in [start, end) are read: when the two aligned chunks around p do not both lie inside it,
+// the bytes are loaded one by one and those outside are zero.  L2 = true reads through L2 only
+// (.cg), as every load of the vector must (a preceding grid may have written it).
+template <bool L2 = false>
+__device__ __forceinline__ uint4 ld16_shifted(const uint8_t* p, uint32_t d, const uint8_t* start,
+                                              const uint8_t* end) {
+  const uint8_t* a = p - d;
+  if (a >= start && a + 32 <= end) {
+    const uint4 lo = L2 ? ld_l2_v4(a) : ld_l1_v4(a);
+    if (d == 0) return lo;
+    return shift16(lo, L2 ? ld_l2_v4(a + 16) : ld_l1_v4(a + 16), d);
+  }
+  if constexpr (L2) {
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    for (uint32_t j = 0; j < 16u; ++j)
+      if (p + j >= start && p + j < end) w[j >> 2] |= (uint32_t)__ldcg(p + j) << (8u * (j & 3u));
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  return ld16_bytes(p, start, end);
 }
 
 // One row group (4 rows) times one 32-element lane slice: decode, exact block partials, scale.
@@ -210,7 +283,58 @@ struct RingPos {
   }
 };
 
-// The producer lane: streams the CTA's row tiles into the ring.
+// Unaligned operands: a tile's bytes [g0, g1) go to the stage at offset g - floor16(g0).  The part
+// of the aligned superset [floor16(g0), ceil16(g1)) that lies inside the 16-byte aligned interior
+// [lo, hi) of the operand's buffer, [c0, c1), arrives by one bulk copy; bytes of [g0, g1) outside
+// it (only in the buffer's first and last partial chunk, at most 15 bytes each) are stored by the
+// producer one by one, so nothing outside the buffer is read.
+struct USpan {
+  const uint8_t *u0, *c0, *c1;
+  uint32_t n;  // bytes of the bulk copy (0: none)
+};
+
+__device__ __forceinline__ USpan unaligned_span(const uint8_t* g0, const uint8_t* g1,
+                                                const uint8_t* lo, const uint8_t* hi) {
+  USpan sp;
+  sp.u0 = reinterpret_cast<const uint8_t*>((uintptr_t)g0 & ~(uintptr_t)15);
+  const uint8_t* u1 = reinterpret_cast<const uint8_t*>(((uintptr_t)g1 + 15) & ~(uintptr_t)15);
+  sp.c0 = sp.u0 > lo ? sp.u0 : lo;
+  sp.c1 = u1 < hi ? u1 : hi;
+  sp.n = sp.c1 > sp.c0 ? (uint32_t)(sp.c1 - sp.c0) : 0u;
+  return sp;
+}
+
+__device__ __forceinline__ void stage_unaligned(uint8_t* st, const uint8_t* g0, const uint8_t* g1,
+                                                const USpan& sp, uint32_t full, uint64_t pol) {
+  if (sp.c0 > g0 || sp.c1 < g1) {  // edge bytes: all loads issued before the stores
+    uint32_t head[4] = {0u, 0u, 0u, 0u}, tail[4] = {0u, 0u, 0u, 0u};  // 16 bytes each, packed
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint8_t* x = g0 + j;
+      if (x < g1 && x < sp.c0) head[j >> 2] |= (uint32_t)*x << (8 * (j & 3));
+      const uint8_t* y = g1 - 16 + j;
+      if (y >= g0 && y >= sp.c1) tail[j >> 2] |= (uint32_t)*y << (8 * (j & 3));
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint8_t* x = g0 + j;
+      if (x < g1 && x < sp.c0) st[x - sp.u0] = (uint8_t)(head[j >> 2] >> (8 * (j & 3)));
+      const uint8_t* y = g1 - 16 + j;
+      if (y >= g0 && y >= sp.c1) st[y - sp.u0] = (uint8_t)(tail[j >> 2] >> (8 * (j & 3)));
+    }
+  }
+  if (sp.n) bulk_copy_g2s(smem_addr(st + (sp.c0 - sp.u0)), sp.c0, sp.n, full, pol);
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// The producer lane: streams the CTA's row tiles into the ring.  UA: operands not 16-byte aligned
+// (stage_unaligned above); the stage then holds each tile's bytes from the 16-byte boundary at or
+// below its first byte.
+template <bool UA>
 __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, uint64_t* bars,
                                             volatile int* abort_flag, uint8_t* ring) {
   const int64_t K2 = p.K >> 1, K16 = p.K >> 4;
@@ -236,9 +360,22 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
     const uint32_t bytesA = (uint32_t)(rows_t * K2), bytesS = (uint32_t)(rows_t * K16);
     const uint32_t full = smem_addr(&bars[s]);
     uint8_t* st = ring + (size_t)s * p.stage_bytes;
-    mbar_arrive_expect_tx(full, bytesA + bytesS);
-    bulk_copy_g2s(smem_addr(st), A_c + (int64_t)T * TR * K2, bytesA, full, pol);
-    bulk_copy_g2s(smem_addr(st + p.sfa_off), S_c + (int64_t)T * TR * K16, bytesS, full, pol);
+    if constexpr (UA) {
+      // the copies' bytes are expected first; the arrival comes after the edge stores, so the
+      // consumers that see the phase complete see those bytes too
+      const uint8_t* ga = A_c + (int64_t)T * TR * K2;
+      const uint8_t* gs = S_c + (int64_t)T * TR * K16;
+      const USpan sa = unaligned_span(ga, ga + bytesA, p.A_lo, p.A_hi);
+      const USpan ss = unaligned_span(gs, gs + bytesS, p.S_lo, p.S_hi);
+      mbar_expect_tx(full, sa.n + ss.n);
+      stage_unaligned(st, ga, ga + bytesA, sa, full, pol);
+      stage_unaligned(st + p.sfa_off, gs, gs + bytesS, ss, full, pol);
+      mbar_arrive(full);
+    } else {
+      mbar_arrive_expect_tx(full, bytesA + bytesS);
+      bulk_copy_g2s(smem_addr(st), A_c + (int64_t)T * TR * K2, bytesA, full, pol);
+      bulk_copy_g2s(smem_addr(st + p.sfa_off), S_c + (int64_t)T * TR * K16, bytesS, full, pol);
+    }
     issued = T + 1;
   }
   if (!ok) {
@@ -299,7 +436,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
   tma_resolve_group(p, g, lane);
   if (g.skip) return;
   if (warp == g.Wc) {
-    if (lane == 0) tma_produce(p, g, bars, abort_flag, ring);
+    if (lane == 0) tma_produce<false>(p, g, bars, abort_flag, ring);
     return;
   }
   if (p.early_weights) pdl_wait();
@@ -398,8 +535,8 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
 // QX: the vector is bf16 and is quantized to NVFP4 here (see quantize.cuh); its bytes feed the same
 // decode as packed input would.
 // ------------------------------------------------------------------------------------------------
-template <int NSW, bool QX>
-__global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
+template <int NSW, bool QX, bool UA>
+__global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel(const TmaArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16 * kTmaMaxStages);
@@ -413,7 +550,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
   tma_resolve_group(p, g, lane);
   if (g.skip) return;
   if (warp == g.Wc) {
-    if (lane == 0) tma_produce(p, g, bars, abort_flag, ring);
+    if (lane == 0) tma_produce<UA>(p, g, bars, abort_flag, ring);
     return;
   }
   if (p.early_weights) pdl_wait();
@@ -456,6 +593,11 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
         *reinterpret_cast<uint4*>(p.b_out + g.l * K2 + (kk >> 1)) = v;
         *reinterpret_cast<uint16_t*>(p.sfb_out + g.l * K16 + (kk >> 4)) = s2;
       }
+    } else if constexpr (UA) {  // any alignment, through L2
+      const uint8_t* bp = p.b + g.l * K2 + (kk >> 1);
+      v = ld16_shifted<true>(bp, (uint32_t)((uintptr_t)bp & 15u), p.b, p.b_end);
+      const uint8_t* sp = p.sfb + g.l * K16 + (kk >> 4);
+      s2 = (uint16_t)((uint32_t)__ldcg(sp) | ((uint32_t)__ldcg(sp + 1) << 8));
     } else {
       v = ld_l2_v4(p.b + g.l * K2 + (kk >> 1));
       s2 = ld_l2_u16(p.sfb + g.l * K16 + (kk >> 4));
@@ -477,6 +619,12 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
     lane_a[j] = (uint32_t)seg[j] * 512u + 16u * lane;
     lane_s[j] = (uint32_t)seg[j] * 64u + 2u * lane;
   }
+  // UA: a tile's A (sfa) bytes sit in the stage from the 16-byte boundary at or below their first
+  // byte, so row r starts dA + r K/2 (dS + r K/16) bytes in.  K/2 and K/16 are multiples of 16
+  // here, so every row of a tile has the same residue dA (dS): a lane reads the aligned 16-byte
+  // words at and after its row offset and shifts them by dA, the same for the whole CTA.
+  const uint8_t* A_c = p.A + (g.ea * p.M + g.m0) * K2;
+  const uint8_t* S_c = p.sfa + (g.ea * p.M + g.m0) * K16;
   RingPos rp;
   for (int T = 0; T < g.NT; ++T, rp.advance(p.stages)) {
     if (!tma_consume_wait(p, bars, abort_flag, rp, lane)) break;
@@ -484,6 +632,8 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
     const int rgs = (rows_t + 3) >> 2;
     const uint32_t stA = ring32 + (uint32_t)rp.s * p.stage_bytes;
     const uint32_t stS = stA + p.sfa_off;
+    const uint32_t dA = UA ? (uint32_t)((uintptr_t)(A_c + (int64_t)T * p.tile_rows * K2) & 15u) : 0u;
+    const uint32_t dS = UA ? (uint32_t)((uintptr_t)(S_c + (int64_t)T * p.tile_rows * K16) & 15u) : 0u;
     float* part_tile = part + (size_t)T * p.tile_rows * p.slots;
     for (int rg = rg_first; rg < rgs; rg += rg_step) {
       uint32_t aoff[4], soff[4];
@@ -491,7 +641,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
       for (int i = 0; i < 4; ++i) {
         const uint32_t r = (uint32_t)min(4 * rg + i, rows_t - 1);  // re-read the last row
         aoff[i] = stA + r * K2u;
-        soff[i] = stS + r * K16u;
+        soff[i] = stS + dS + r * K16u;
       }
       float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
@@ -501,8 +651,16 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_rv_kernel(const TmaArgs p) {
           uint16_t sv[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            av[i] = lds_v4(aoff[i] + lane_a[j]);
-            sv[i] = lds_u16(soff[i] + lane_s[j]);
+            if constexpr (UA) {
+              const uint32_t o = aoff[i] + lane_a[j];
+              const uint4 lo = lds_v4(o);
+              av[i] = dA ? shift16(lo, lds_v4(o + 16), dA) : lo;
+              const uint32_t so = soff[i] + lane_s[j];
+              sv[i] = (dS & 1u) ? (uint16_t)(lds_u8(so) | (lds_u8(so + 1) << 8)) : lds_u16(so);
+            } else {
+              av[i] = lds_v4(aoff[i] + lane_a[j]);
+              sv[i] = lds_u16(soff[i] + lane_s[j]);
+            }
           }
           item_compute4(av, sv, bw[j], sb[j], acc);
         }

@@ -84,10 +84,12 @@ void init_device(int dev) {
       (e = prepare_stream_kernel<2>(d.max_smem_optin)) ||
       (e = prepare_stream_kernel<4>(d.max_smem_optin)) ||
       (e = prepare_tma_kernel(nvfp4::gemv_tma_kernel, d.max_smem_optin)) ||
-      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, false>, d.max_smem_optin)) ||
-      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false>, d.max_smem_optin)) ||
-      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, true>, d.max_smem_optin)) ||
-      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, true>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, false, false>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false, false>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, true, false>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, true, false>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, false, true>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false, true>, d.max_smem_optin)) ||
       (e = cudaFuncSetAttribute(nvfp4::gemv_shift_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin)) ||
       (e = cudaFuncSetAttribute(nvfp4::gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -342,14 +344,19 @@ struct TmaLayout {
   int64_t b_off, sb_off, part_off, ring_off, sfa_off, stage_bytes, total;
 };
 
-TmaLayout tma_layout(bool rv, int64_t K, int64_t TR, int64_t NS, int64_t rows_cap, int64_t slots) {
+// ua: operands not 16-byte aligned; a stage then holds each tile's A and sfa bytes from the
+// 16-byte boundary at or below their first byte, plus the 16 bytes a lane's second aligned read
+// may reach past them: 32 bytes more for each.
+TmaLayout tma_layout(bool rv, int64_t K, int64_t TR, int64_t NS, int64_t rows_cap, int64_t slots,
+                     bool ua = false) {
   TmaLayout t;
   t.b_off = nvfp4::kTmaHeaderBytes;
   t.sb_off = t.b_off + (rv ? 0 : 2 * K);
   t.part_off = align_up(t.sb_off + (rv ? 0 : K / 4), 16);
   t.ring_off = align_up(t.part_off + 4 * rows_cap * slots, 128);
-  t.sfa_off = align_up(TR * (K / 2), 128);
-  t.stage_bytes = align_up(t.sfa_off + TR * (K / 16), 128);
+  const int64_t slack = ua ? 32 : 0;
+  t.sfa_off = align_up(TR * (K / 2) + slack, 128);
+  t.stage_bytes = align_up(t.sfa_off + TR * (K / 16) + slack, 128);
   t.total = t.ring_off + NS * t.stage_bytes;
   return t;
 }
@@ -362,9 +369,9 @@ constexpr int64_t kTmaSmallStage = 24576;   // stages below this get up to 4 rin
 
 // Consumer warps for the register-vector variant: they must divide the K-segment count (NSW = 1
 // or 2 segments per warp) or be a multiple of it.  Returns 0 if no such count fits.
-int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw) {
+int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw, int64_t max_warps = 16) {
   auto ok = [&](int64_t w) -> bool {
-    if (w < 1 || w > 16) return false;
+    if (w < 1 || w > max_warps) return false;
     if (nseg >= w) {
       if (nseg % w || nseg / w > 2) return false;
       *nsw = nseg / w;
@@ -382,8 +389,12 @@ int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw) {
   return 0;
 }
 
+// ua: operands not 16-byte aligned (register-vector kernel only; stages carry 32 bytes of slack).
 int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan& f, bool rv,
-             nvfp4_plan* pl) {
+             nvfp4_plan* pl, bool ua = false) {
+  if (ua && !rv)
+    return fail(NVFP4_ERR_MISALIGNED,
+                "the shared-memory-vector TMA kernel needs 16-byte aligned A, sfa, b and sfb");
   if (K % 256 != 0)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernels need K %% 256 == 0 (K=%lld)",
                 (long long)K);
@@ -398,7 +409,9 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   const int64_t nseg = ceil_div(K, nvfp4::kStep);
   int64_t Wc = f.warps_per_cta ? f.warps_per_cta : 8, nsw = 1;
   if (rv) {
-    Wc = rv_warps(nseg, f.warps_per_cta, &nsw);
+    // the unaligned form needs more registers (about 88-96 a thread): at most 8 consumer warps
+    // keep two CTAs per SM
+    Wc = rv_warps(nseg, f.warps_per_cta, &nsw, ua ? 8 : 16);
     if (!Wc)
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                   "register-vector TMA kernel: no warp count fits %lld K segments",
@@ -421,21 +434,21 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       // at least ~4 tiles per CTA, so the last tile's compute is a small part of the CTA's time
       TR = std::min<int64_t>(TR, std::max<int64_t>(unit, align_up(ceil_div(rows_cap, 4), unit)));
       // shrink by whole rounds until two stages fit this occupancy's budget
-      while (TR > unit && tma_layout(rv, K, TR, 2, rows_cap, slots).total > budget) TR -= unit;
-      while (TR > 4 && tma_layout(rv, K, TR, 2, rows_cap, slots).total > budget) TR -= 4;
+      while (TR > unit && tma_layout(rv, K, TR, 2, rows_cap, slots, ua).total > budget) TR -= unit;
+      while (TR > 4 && tma_layout(rv, K, TR, 2, rows_cap, slots, ua).total > budget) TR -= 4;
     }
     int64_t NS = f.stages;
     if (NS == 0) {
-      const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots).stage_bytes;
+      const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots, ua).stage_bytes;
       const int64_t want = stage < kTmaSmallStage ? 4 : 2;
       for (int64_t ns = want; ns >= 2; --ns)
-        if (tma_layout(rv, K, TR, ns, rows_cap, slots).total <= budget) {
+        if (tma_layout(rv, K, TR, ns, rows_cap, slots, ua).total <= budget) {
           NS = ns;
           break;
         }
       if (NS == 0) return false;
     }
-    if (tma_layout(rv, K, TR, NS, rows_cap, slots).total > d.max_smem_optin) return false;
+    if (tma_layout(rv, K, TR, NS, rows_cap, slots, ua).total > d.max_smem_optin) return false;
     *TR_out = TR;
     *NS_out = NS;
     return true;
@@ -562,10 +575,10 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
   memset(&f, 0, sizeof f);
   if (forced) f = *forced;
   if (!aligned16 && f.kernel != NVFP4_KERNEL_AUTO && f.kernel != NVFP4_KERNEL_SIMPLE &&
-      f.kernel != NVFP4_KERNEL_SHIFT)
+      f.kernel != NVFP4_KERNEL_SHIFT && f.kernel != NVFP4_KERNEL_TMA_RV)
     return fail(NVFP4_ERR_MISALIGNED,
-                "kernel %d needs 16-byte aligned A, sfa, b and sfb (SHIFT and SIMPLE take any)",
-                f.kernel);
+                "kernel %d needs 16-byte aligned A, sfa, b and sfb (TMA_RV, SHIFT and SIMPLE take "
+                "any)", f.kernel);
   if (f.flags & ~(NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_NO_PDL | NVFP4_FLAG_QUANTIZE_IN_GEMV))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown plan flags 0x%x", (unsigned)f.flags);
   if (f.warps_per_cta < 0 || f.rows_per_warp < 0 || f.k_split < 0 || f.ctas_per_batch < 0 ||
@@ -577,20 +590,22 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
     case NVFP4_KERNEL_SIMPLE: st = plan_simple(d, M, L, f, pl); break;
     case NVFP4_KERNEL_STREAM: st = plan_stream(d, M, K, L, f, pl); break;
     case NVFP4_KERNEL_TMA: st = plan_tma(d, M, K, L, f, false, pl); break;
-    case NVFP4_KERNEL_TMA_RV: st = plan_tma(d, M, K, L, f, true, pl); break;
+    case NVFP4_KERNEL_TMA_RV: st = plan_tma(d, M, K, L, f, true, pl, !aligned16); break;
     case NVFP4_KERNEL_TC: st = plan_tc(d, M, K, tc_groups, f, pl); break;
     case NVFP4_KERNEL_SHIFT: st = plan_shift(d, M, K, L, f, pl); break;
     case NVFP4_KERNEL_AUTO: {
-      // 16-byte aligned operands: the TMA ring (vector in registers if the warp mapping allows)
-      // when every CTA gets at least 8 rows, else the stream kernel; any other alignment or K:
-      // the shift kernel, else the simple kernel
+      // K % 256 == 0 and at least 8 rows per CTA: the TMA ring (vector in registers if the warp
+      // mapping allows; the register-vector kernel alone for operands not 16-byte aligned); else
+      // aligned operands with K % 32 == 0: the stream kernel; else the shift kernel, else the
+      // simple kernel
       const int64_t rows_per_cta = (M * L) / std::max<int64_t>(1, (int64_t)d.sms * 2);
       st = -1;
-      if (aligned16 && K % 256 == 0 && rows_per_cta >= 8) {
+      if (K % 256 == 0 && rows_per_cta >= 8) {
         char saved[sizeof g_last_error];
         memcpy(saved, g_last_error, sizeof saved);
         for (bool rv : {true, false}) {
-          if (plan_tma(d, M, K, L, f, rv, pl) == NVFP4_OK) {
+          if (!aligned16 && !rv) break;  // unaligned operands: the register-vector kernel only
+          if (plan_tma(d, M, K, L, f, rv, pl, !aligned16) == NVFP4_OK) {
             st = NVFP4_OK;
             break;
           }
@@ -806,7 +821,28 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     const int64_t nseg = ceil_div(K, nvfp4::kStep);
     a.slots = (int32_t)(rv ? std::min<int64_t>(pl.warps_per_cta, nseg) : pl.warps_per_cta);
     a.early_weights = (pl.flags & NVFP4_FLAG_EARLY_WEIGHTS) ? 1 : 0;
-    const TmaLayout t = tma_layout(rv, K, pl.tile_rows, pl.stages, a.rows_cap, a.slots);
+    // operands not 16-byte aligned (the register-vector kernel's unaligned form): the aligned
+    // interiors of A and sfa and the ends of b and sfb bound every read
+    const bool ua = (((uintptr_t)A | (uintptr_t)sfa | (uintptr_t)b | (uintptr_t)sfb) & 15u) != 0;
+    if (ua && (!rv || fx))
+      return fail(NVFP4_ERR_MISALIGNED, "this TMA plan needs 16-byte aligned operands");
+    a.A_lo = a.A_hi = a.S_lo = a.S_hi = a.b_end = a.sfb_end = nullptr;
+    if (ua) {
+      const int64_t n_mats = G.E > 0 ? (int64_t)G.E : (G.shared_a ? 1 : L);  // matrices in A
+      auto up16 = [](const uint8_t* q) {
+        return reinterpret_cast<const uint8_t*>(((uintptr_t)q + 15) & ~(uintptr_t)15);
+      };
+      auto down16 = [](const uint8_t* q) {
+        return reinterpret_cast<const uint8_t*>((uintptr_t)q & ~(uintptr_t)15);
+      };
+      a.A_lo = up16(A);
+      a.A_hi = down16(A + n_mats * M * (K / 2));
+      a.S_lo = up16(sfa);
+      a.S_hi = down16(sfa + n_mats * M * (K / 16));
+      a.b_end = b + L * (K / 2);
+      a.sfb_end = sfb + L * (K / 16);
+    }
+    const TmaLayout t = tma_layout(rv, K, pl.tile_rows, pl.stages, a.rows_cap, a.slots, ua);
     a.stage_bytes = (uint32_t)t.stage_bytes;
     a.sfa_off = (uint32_t)t.sfa_off;
     a.b_off = (uint32_t)t.b_off;
@@ -827,11 +863,14 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     }
     if (rv) {
       if (fx)
-        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, true>
-                               : nvfp4::gemv_tma_rv_kernel<1, true>;
+        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, true, false>
+                               : nvfp4::gemv_tma_rv_kernel<1, true, false>;
+      else if (ua)
+        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false, true>
+                               : nvfp4::gemv_tma_rv_kernel<1, false, true>;
       else
-        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false>
-                               : nvfp4::gemv_tma_rv_kernel<1, false>;
+        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false, false>
+                               : nvfp4::gemv_tma_rv_kernel<1, false, false>;
     }
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);

@@ -47,11 +47,12 @@
  *   NVFP4_ERR_INVALID_VALUE   M < 0, L < 0, K <= 0, K % 16 != 0, a NULL pointer when M*L > 0,
  *                             c overlapping an input, or an inaccessible pointer
  *   NVFP4_ERR_UNSUPPORTED_SHAPE  M, L or K/2 above 2^31 - 1, or an invalid forced plan
- *   NVFP4_ERR_MISALIGNED      c not 2-byte aligned, or a forced plan other than SIMPLE or SHIFT
- *                             while A, sfa, b or sfb is not 16-byte aligned
- *   Any alignment of A, sfa, b and sfb is accepted: when one of them is not 16-byte aligned (or
- *   K % 32 != 0) the automatic plan is the SHIFT kernel (aligned 16-byte loads shifted into
- *   place), or the SIMPLE kernel (byte loads) when the vector does not fit shared memory.
+ *   NVFP4_ERR_MISALIGNED      c not 2-byte aligned, or a forced plan other than TMA_RV, SHIFT or
+ *                             SIMPLE while A, sfa, b or sfb is not 16-byte aligned
+ *   Any alignment of A, sfa, b and sfb is accepted.  When one of them is not 16-byte aligned the
+ *   automatic plan is TMA_RV's unaligned form if K % 256 == 0 and every CTA gets 8 rows; else
+ *   (and for aligned operands with K % 32 != 0) the SHIFT kernel (aligned 16-byte loads shifted
+ *   into place), or the SIMPLE kernel (byte loads) when the vector does not fit shared memory.
  *   NVFP4_ERR_ARCH            the current device is not compute capability 10.3 (GB300)
  *   NVFP4_ERR_CUDA            a CUDA runtime call or the launch failed (nvfp4_last_error() has
  *                             the runtime's message)
@@ -87,7 +88,11 @@ typedef enum nvfp4_kernel {
                                (TMA) and mbarriers, vector in shared memory; needs K % 256 == 0 */
   NVFP4_KERNEL_TMA_RV = 4,  /* as TMA with each consumer warp's vector slice held in registers;
                                needs K % 256 == 0 and the warp count to divide the number of
-                               1024-element K segments (or be a multiple of it) */
+                               1024-element K segments (or be a multiple of it).  Operands that are
+                               not 16-byte aligned take its unaligned form (bulk copies of each
+                               tile's aligned interior, the buffers' first and last partial
+                               16 bytes copied one by one, shifted out of shared memory; at most
+                               8 consumer warps) */
   NVFP4_KERNEL_TC = 5,      /* tensor cores (tcgen05.mma kind::mxf4nvf4, block scales applied by
                                the MMA, fp32 accumulator in tensor memory): 128-row tiles x up to
                                16 vectors, K split over a cluster of k_split (<= 8) CTAs with a

@@ -1,7 +1,9 @@
 """GPU parity of the general path: any byte alignment of A, sfa, b and sfb, and any K % 16 == 0
 (K not a multiple of 32 included), through the C ABI against the oracle.  The planner sends such
-calls to the shift kernel (aligned 16-byte loads funnel-shifted into place); the simple kernel
-(byte loads) takes them when forced; the vector-load and TMA kernels refuse them.  The buffers sit
+calls to the register-vector TMA kernel when K % 256 == 0 (bulk copies of each tile's aligned
+interior, edge bytes stored one by one, shifted out of shared memory) and otherwise to the shift
+kernel (aligned 16-byte loads funnel-shifted into place); the simple kernel (byte loads) takes them
+when forced; the vector-load, shared-memory-vector TMA and tensor-core kernels refuse them.  The buffers sit
 inside larger allocations filled with other bytes, so a read before the first or past the last
 byte of an operand would change the result."""
 import numpy as np
@@ -61,11 +63,14 @@ def test_unaligned_inputs(pkg, offsets):
         assert_parity(c2.cpu().numpy(), ref, T, f"offsets {offsets} {plan}")
         if plan.get("kernel") == 6:   # the automatic plan is the shift kernel: same bits
             assert np.array_equal(c2.cpu().numpy().view(np.uint16), auto.view(np.uint16))
-    for plan in (dict(kernel=2), dict(kernel=3), dict(kernel=4)):
+    # the vector-load and shared-memory-vector TMA kernels refuse unaligned operands; the
+    # register-vector TMA kernel takes them but needs K % 256 == 0 (here K = 1056)
+    for plan, status in ((dict(kernel=2), 2), (dict(kernel=3), 2), (dict(kernel=4), 3),
+                         (dict(kernel=5), 2)):
         with pytest.raises(pkg.NVFP4Error) as e:
             pkg.nvfp4_gemv_batched_ex(args[0], args[1], w.g_a, args[2], args[3], w.g_b, c, w.M,
                                       w.K, w.L, plan=plan)
-        assert e.value.status == 2
+        assert e.value.status == status, plan
 
 
 @pytest.mark.parametrize("K", [16, 272, 2064, 16368])
@@ -167,3 +172,58 @@ def test_shift_kernel_grouped_forms(pkg):
         out = c.cpu().numpy()
         assert np.all(out[-1] == 0), plan
         assert_parity(out, ref, T, f"grouped unaligned {plan}")
+
+
+RING_SHAPES = [(2432, 2048, 1), (300, 4096, 9), (97, 1024, 3), (1000, 16384, 1)]
+
+
+@pytest.mark.parametrize("shape", RING_SHAPES, ids=[f"{m}x{k}x{l}" for m, k, l in RING_SHAPES])
+@pytest.mark.parametrize("offsets", [(1, 0, 0, 0), (0, 5, 0, 0), (0, 0, 3, 9), (15, 13, 11, 7),
+                                     (8, 8, 0, 0)])
+def test_unaligned_operands_on_the_tma_ring(pkg, shape, offsets):
+    """K % 256 == 0 with operands off 16-byte boundaries: the register-vector TMA kernel copies each
+    tile's aligned interior in bulk and the buffer's first and last partial chunks byte by byte.
+    Every plan gives the oracle's values; the ring plans agree bit for bit with each other."""
+    M, K, L = shape
+    w = workloads.random_workload(M, K, L, seed=M + K + sum(offsets),
+                                  scale_bytes=workloads.pow2_scale_bytes(-4, 3), g_a=0.5, g_b=1.5)
+    keep, args = [], []
+    for name, off in zip(("A", "sfa", "b", "sfb"), offsets):
+        v, raw = placed(getattr(w, name), off)
+        keep.append(raw)
+        args.append(v)
+    ref, T = oracle.gemv(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, M, K, L)
+    ring = None
+    for plan in (None, dict(kernel=4), dict(kernel=4, flags=1), dict(kernel=4, flags=2),
+                 dict(kernel=4, tile_rows=3, stages=3, ctas_per_batch=2),
+                 dict(kernel=4, tile_rows=5, stages=2), dict(kernel=6), dict(kernel=1)):
+        c = torch.full((L, M), float("nan"), dtype=torch.float16, device="cuda")
+        pkg.nvfp4_gemv_batched_ex(args[0], args[1], w.g_a, args[2], args[3], w.g_b, c, M, K, L,
+                                  plan=plan)
+        torch.cuda.synchronize()
+        out = c.cpu().numpy()
+        assert not np.isnan(out).any(), plan
+        assert_parity(out, ref, T, f"{shape} {offsets} {plan}")
+        if plan == dict(kernel=4):
+            ring = out
+        elif plan is not None and plan.get("kernel") == 4 and "tile_rows" not in plan:
+            assert np.array_equal(out.view(np.uint16), ring.view(np.uint16)), plan
+
+
+def test_unaligned_grouped_on_the_tma_ring(pkg):
+    """The grouped form with unaligned experts on the register-vector TMA kernel."""
+    w = workloads.make_grouped("g0")
+    A, rA = placed(w.A, 9)
+    sfa, rS = placed(w.sfa, 14)
+    b, rB = placed(w.b, 1)
+    sfb, rSB = placed(w.sfb, 6)
+    g_a = torch.from_numpy(np.ascontiguousarray(w.g_a)).cuda()
+    g_b = torch.from_numpy(np.ascontiguousarray(w.g_b)).cuda()
+    from oracle import grouped as G
+    ref, T = G.gemv_grouped(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, w.expert_of, w.M, w.K)
+    for plan in (dict(kernel=4), dict(kernel=4, tile_rows=7, stages=4)):
+        c = torch.full((w.T, w.M), float("nan"), dtype=torch.float16, device="cuda")
+        pkg.nvfp4_gemv_grouped(A, sfa, g_a, b, sfb, g_b, c, w.M, w.K, w.E, w.T,
+                               expert_of_token=torch.from_numpy(w.expert_of).cuda(), plan=plan)
+        torch.cuda.synchronize()
+        assert_parity(c.cpu().numpy(), ref, T, f"grouped unaligned ring {plan}")
