@@ -114,7 +114,8 @@ enum {
   NVFP4_FLAG_NO_PDL = 2,
   /* nvfp4_gemv_batched_bf16 only (INVALID_VALUE elsewhere): quantize the bf16 vector inside the
      register-vector TMA kernel (one launch; every CTA quantizes the part of the vector it reads)
-     instead of a quantizer launch ahead of the GEMV.  The plan's kernel must be TMA_RV. */
+     instead of a quantizer launch ahead of the GEMV.  The plan's kernel must be TMA_RV, and A and
+     sfa 16-byte aligned (NVFP4_ERR_MISALIGNED otherwise). */
   NVFP4_FLAG_QUANTIZE_IN_GEMV = 4
 };
 

@@ -288,6 +288,23 @@ def test_in_gemv_flag_rules(pkg):
     with pytest.raises(pkg.NVFP4Error) as e:          # meaningless for a packed vector
         packed_gemv(pkg, A, sfa, 1.0, w.b, w.sfb, 1.0, M, K, L, {"flags": IN_GEMV})
     assert e.value.status == 1
+    # a matrix off a 16-byte boundary: the in-GEMV form refuses it; the two-launch form (the
+    # default) quantizes first and runs the GEMV's unaligned form
+    raw = torch.empty(A.numel() + 16, dtype=torch.uint8, device="cuda")
+    A1 = raw[3:3 + A.numel()]
+    A1.copy_(A.reshape(-1))
+    with pytest.raises(pkg.NVFP4Error) as e:          # the automatic plan here: not the ring
+        gemv_bf16(pkg, A1, sfa, 1.0, x, 1.0, 0, M, {"flags": IN_GEMV})
+    assert e.value.status == 3
+    with pytest.raises(pkg.NVFP4Error) as e:          # the ring forced: its unaligned form
+        gemv_bf16(pkg, A1, sfa, 1.0, x, 1.0, 0, M, {"kernel": 4, "flags": IN_GEMV})
+    assert e.value.status == 2
+    c1, b1, s1 = gemv_bf16(pkg, A1, sfa, 1.0, x, 1.0, 0, M, None)
+    pr, sr = Q.quantize_activation(x, 1.0, "lut")
+    assert_bytes_equal(b1, pr, "b_out, misaligned A")
+    assert_bytes_equal(s1, sr, "sfb_out, misaligned A")
+    ref, T = oracle.gemv(w.A, w.sfa, 1.0, pr, sr, 1.0, M, K, L)
+    assert_parity(c1, ref, T, "bf16 vector, misaligned A")
 
 
 def test_gemv_bf16_empty_and_statuses(pkg):
