@@ -320,3 +320,39 @@ def test_gemv_bf16_empty_and_statuses(pkg):
     with pytest.raises(pkg.NVFP4Error) as e:
         pkg.nvfp4_gemv_batched_bf16(A, sfa, 1.0, x, -2.0, b, s, c, 4, 256, 1)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("case", list(range(100)))
+def test_random_bf16_vector_cases(pkg, case):
+    """Seeded random bf16-vector GEMVs: K (any multiple of 16), L, M, global scale, rounding, the
+    matrix's alignment and the plan drawn at random.  The packed vector the call writes must equal
+    the oracle's quantization byte for byte; the output is checked under the tolerance."""
+    rng = np.random.default_rng(21_000 + case)
+    K = 16 * int(rng.choice([1, 3, 16, 17, 64, 65, 128, 256, 513]))
+    L = int(rng.integers(1, 5))
+    M = int(rng.integers(1, 300))
+    gs = float(np.float32(rng.choice([1.0, 2.0 ** -5, 0.0173, 3.7])))
+    rounding, name = ROUNDINGS[int(rng.integers(0, 2))]
+    w = workloads.random_workload(M, K, L, seed=22_000 + case,
+                                  scale_bytes=workloads.pow2_scale_bytes(-4, 3), g_a=0.75)
+    x = activation(K, L, seed=23_000 + case, gs=gs, plant=K >= 256)
+    pr, sr = Q.quantize_activation(x, gs, name)
+    ref, T = oracle.gemv(w.A, w.sfa, w.g_a, pr, sr, gs, M, K, L)
+    A = torch.from_numpy(w.A).cuda()
+    if rng.random() < 0.4:                            # the matrix off a 16-byte boundary
+        off = int(rng.integers(1, 16))
+        raw = torch.empty(A.numel() + 32, dtype=torch.uint8, device="cuda")
+        A = raw[off:off + w.A.size]
+        A.copy_(torch.from_numpy(w.A.ravel()).cuda())
+    sfa = torch.from_numpy(w.sfa).cuda()
+    plan = [None, {"flags": 1}, {"flags": 1 | IN_GEMV}, {"kernel": 6}][int(rng.integers(0, 4))]
+    try:
+        c, b, s = gemv_bf16(pkg, A, sfa, w.g_a, x, gs, rounding, M, plan)
+    except pkg.NVFP4Error as e:   # the in-GEMV form needs the aligned register-vector kernel
+        assert plan is not None and plan["flags"] & IN_GEMV and e.status in (2, 3), (plan, e)
+        return
+    what = f"case {case}: M={M} K={K} L={L} gs={gs} {name} plan={plan}"
+    assert_bytes_equal(b, pr, what + " b_out")
+    assert_bytes_equal(s, sr, what + " sfb_out")
+    assert not np.isnan(c).any(), what
+    assert_parity(c, ref, T, what)
