@@ -36,7 +36,7 @@ __all__ = [
 
 KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV, KERNEL_TC, KERNEL_SHIFT = (
     0, 1, 2, 3, 4, 5, 6)
-FLAG_EARLY_WEIGHTS, FLAG_NO_PDL, FLAG_QUANTIZE_IN_GEMV = 1, 2, 4
+FLAG_EARLY_WEIGHTS, FLAG_NO_PDL, FLAG_QUANTIZE_IN_GEMV, FLAG_TEST_STALL = 1, 2, 4, 8
 ROUND_HALF_STEP_TABLE, ROUND_NEAREST_EVEN = 0, 1
 OUT_F16, OUT_BF16 = 0, 1
 

@@ -76,6 +76,7 @@ struct TcArgs {
   int32_t early_weights;
   int32_t total_tiles;        // L * tiles
   uint32_t red_off;           // split-K partial buffer (bytes from the aligned window), S > 1
+  int32_t test_stall;  // tests of the failure path: the producer issues nothing
 };
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -268,7 +269,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    if (lane == 0 && !p.test_stall) {  // stalled: every wait for its copies runs out
       const uint32_t bytes = kTcRows * kTcChunkBytes + (uint32_t)p.N * kTcChunkBytes +
                              kTcRows * 16u + (uint32_t)p.N * 16u;
       // with static weights the first stages' A and sfa copies start before the launch wait
@@ -347,11 +348,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
                    (i > 0 || j > 0) ? 1u : 0u);
           tc_commit(smem_addr(&h->empty[rp.s]));
         }
-        tc_commit(smem_addr(&h->acc_full[ab]));  // also on failure, so the epilogue goes on
-        if (!ok) {
+        if (!ok) {  // the flag first: an epilogue warp that sees this commit reads it after
           *abort_flag = 1;
-          break;
+          __threadfence_block();
         }
+        tc_commit(smem_addr(&h->acc_full[ab]));  // also on failure, so the epilogue goes on
+        if (!ok) break;
       }
     }
     __syncwarp();

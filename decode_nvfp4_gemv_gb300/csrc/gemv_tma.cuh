@@ -89,6 +89,7 @@ struct TmaArgs {
   // operands not 16-byte aligned: the 16-byte aligned interiors [lo, hi) of the A and sfa buffers,
   // and the ends of the b and sfb buffers (unused when aligned)
   const uint8_t *A_lo, *A_hi, *S_lo, *S_hi, *b_end, *sfb_end;
+  int32_t test_stall;    // tests of the failure path: the producer issues nothing
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -344,6 +345,7 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
   const uint8_t* S_c = p.sfa + (g.ea * p.M + g.m0) * K16;
   int issued = 0;
   bool ok = true;
+  if (p.test_stall) return;  // every consumer wait then runs out at its limit
   RingPos rp;
   for (int T = 0; T < g.NT; ++T, rp.advance(NS)) {
     const int s = rp.s;

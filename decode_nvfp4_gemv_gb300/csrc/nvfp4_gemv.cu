@@ -579,7 +579,8 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
     return fail(NVFP4_ERR_MISALIGNED,
                 "kernel %d needs 16-byte aligned A, sfa, b and sfb (TMA_RV, SHIFT and SIMPLE take "
                 "any)", f.kernel);
-  if (f.flags & ~(NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_NO_PDL | NVFP4_FLAG_QUANTIZE_IN_GEMV))
+  if (f.flags & ~(NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_NO_PDL | NVFP4_FLAG_QUANTIZE_IN_GEMV |
+                  NVFP4_FLAG_TEST_STALL))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown plan flags 0x%x", (unsigned)f.flags);
   if (f.warps_per_cta < 0 || f.rows_per_warp < 0 || f.k_split < 0 || f.ctas_per_batch < 0 ||
       f.tile_rows < 0 || f.stages < 0)
@@ -696,6 +697,7 @@ int launch_tc(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const
   a.stages = pl.stages;
   a.a_rows_per_batch = (int32_t)a_rows_per_batch;
   a.early_weights = (pl.flags & NVFP4_FLAG_EARLY_WEIGHTS) ? 1 : 0;
+  a.test_stall = (pl.flags & NVFP4_FLAG_TEST_STALL) ? 1 : 0;
   a.total_tiles = (int32_t)(groups * a.tiles);
   a.red_off = nvfp4::kTcHeaderBytes + (uint32_t)pl.stages * nvfp4::kTcStageBytes;
   const int64_t smem = tc_smem_bytes(pl.stages, a.S);
@@ -821,6 +823,7 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     const int64_t nseg = ceil_div(K, nvfp4::kStep);
     a.slots = (int32_t)(rv ? std::min<int64_t>(pl.warps_per_cta, nseg) : pl.warps_per_cta);
     a.early_weights = (pl.flags & NVFP4_FLAG_EARLY_WEIGHTS) ? 1 : 0;
+    a.test_stall = (pl.flags & NVFP4_FLAG_TEST_STALL) ? 1 : 0;
     // operands not 16-byte aligned (the register-vector kernel's unaligned form): the aligned
     // interiors of A and sfa and the ends of b and sfb bound every read
     const bool ua = (((uintptr_t)A | (uintptr_t)sfa | (uintptr_t)b | (uintptr_t)sfb) & 15u) != 0;

@@ -116,7 +116,12 @@ enum {
      register-vector TMA kernel (one launch; every CTA quantizes the part of the vector it reads)
      instead of a quantizer launch ahead of the GEMV.  The plan's kernel must be TMA_RV, and A and
      sfa 16-byte aligned (NVFP4_ERR_MISALIGNED otherwise). */
-  NVFP4_FLAG_QUANTIZE_IN_GEMV = 4
+  NVFP4_FLAG_QUANTIZE_IN_GEMV = 4,
+  /* For tests of the failure path only: the producer of the TMA and tensor-core kernels issues no
+     copies, so every wait for them gives up at its one-second limit and the launch writes NaN
+     (0x7E00) to all of its outputs; nothing faults and the context stays usable.  The other
+     kernels ignore it.  Never set in normal use. */
+  NVFP4_FLAG_TEST_STALL = 8
 };
 
 /*
