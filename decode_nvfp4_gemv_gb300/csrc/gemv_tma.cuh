@@ -37,8 +37,9 @@
 // next kernel in the stream may be scheduled while this one drains.  Every thread executes
 // griddepcontrol.wait before its first access to memory a preceding kernel may write; with the
 // `early_weights` flag (the caller guarantees that no kernel still running writes A or sfa) the
-// producer starts streaming A and sfa before that wait and only the vector, its scales and the
-// outputs wait.  griddepcontrol.wait returns at once for a launch without the attribute.
+// producer requests the first NS - 1 tiles of A and sfa before that wait, and only the vector, its
+// scales, the outputs and the rest of the ring wait.  griddepcontrol.wait returns at once for a
+// launch without the attribute.
 //
 // Bounded waits.  Every mbarrier wait gives up after one second of wall time (%globaltimer).  A
 // consumer that gives up sets a shared abort flag; a producer that gives up waits (again bounded)
@@ -349,6 +350,11 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
   RingPos rp;
   for (int T = 0; T < g.NT; ++T, rp.advance(NS)) {
     const int s = rp.s;
+    // Early weights: the first NS - 1 tiles are requested before the preceding work has finished,
+    // the last tile of the first fill only once it has.  Requested early, that tile's bytes would
+    // compete for HBM with the preceding call's last tiles: measured on GB300 against requesting
+    // the whole ring early, c2 12.34 -> 11.50 us, c3 -3.6%, c4 -1.2%, c5 -1.3%.
+    if (p.early_weights && T == NS - 1) pdl_wait();
     // stage s was last filled in the previous round: wait until its consumers released it
     if (T >= NS && !mbar_wait_bounded(smem_addr(&bars[NS + s]), rp.phase ^ 1u, kWaitLimitNs)) {
       ok = false;
