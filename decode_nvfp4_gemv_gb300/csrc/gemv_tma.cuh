@@ -37,8 +37,8 @@
 // next kernel in the stream may be scheduled while this one drains.  Every thread executes
 // griddepcontrol.wait before its first access to memory a preceding kernel may write; with the
 // `early_weights` flag (the caller guarantees that no kernel still running writes A or sfa) the
-// producer requests the first NS - 1 tiles of A and sfa before that wait, and only the vector, its
-// scales, the outputs and the rest of the ring wait.  griddepcontrol.wait returns at once for a
+// producer requests the first NS - 1 tiles of A and sfa before that wait (all but the tail of the
+// last of them), and only the vector, its scales, the outputs and the rest of the ring wait.  griddepcontrol.wait returns at once for a
 // launch without the attribute.
 //
 // Bounded waits.  Every mbarrier wait gives up after one second of wall time (%globaltimer).  A
@@ -380,9 +380,22 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
       stage_unaligned(st + p.sfa_off, gs, gs + bytesS, ss, full, pol);
       mbar_arrive(full);
     } else {
+      // Early weights: the last tile requested before the wait keeps the tail of its A bytes (one
+      // row of a tile of more than 4 rows, else 16 bytes) until after the wait, so that tile
+      // completes only once the preceding work has.  Measured on GB300 against requesting the
+      // whole tile early: c2 -0.5%, c3 -0.5%, c4 7.64 -> 7.34 us, c5 -1%; holding back one row of
+      // c2's 4-row tile measured 1% slower than 16 bytes.
+      const uint8_t* ga = A_c + (int64_t)T * TR * K2;
+      uint32_t hold = 0;
+      if (p.early_weights && T == NS - 2) hold = rows_t > 4 ? (uint32_t)K2 : 16u;
+      if (hold >= bytesA) hold = 0;
       mbar_arrive_expect_tx(full, bytesA + bytesS);
-      bulk_copy_g2s(smem_addr(st), A_c + (int64_t)T * TR * K2, bytesA, full, pol);
+      bulk_copy_g2s(smem_addr(st), ga, bytesA - hold, full, pol);
       bulk_copy_g2s(smem_addr(st + p.sfa_off), S_c + (int64_t)T * TR * K16, bytesS, full, pol);
+      if (hold) {
+        pdl_wait();
+        bulk_copy_g2s(smem_addr(st) + bytesA - hold, ga + (bytesA - hold), hold, full, pol);
+      }
     }
     issued = T + 1;
   }
