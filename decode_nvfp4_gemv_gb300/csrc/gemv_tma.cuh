@@ -71,6 +71,7 @@ struct TmaArgs {
   int32_t tile_rows;     // TR: rows per ring stage
   int32_t stages;        // NS <= kTmaMaxStages
   int32_t rows_cap;      // ceil(M / P)
+  int32_t rows_q, rows_r; // M = P rows_q + rows_r: the first rows_r CTAs of a batch take one row more
   int32_t slots;         // partial sums per row (consumer warps, or segments for the rv kernel)
   int32_t early_weights; // 1: stream A and sfa before the programmatic-launch wait
   uint32_t stage_bytes;  // bytes per ring stage (A rows, then sfa rows at sfa_off)
@@ -233,11 +234,16 @@ struct TmaCta {
 __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
                                             volatile int* abort_flag) {
   TmaCta g;
-  g.l = blockIdx.x / p.P;
-  g.pi = blockIdx.x - g.l * p.P;
-  g.m0 = (p.M * g.pi) / p.P;
-  const int64_t m1 = (p.M * (g.pi + 1)) / p.P;
-  g.n = (int)(m1 - g.m0);
+  // The batch and the CTA's rows, in 32-bit arithmetic and without a 64-bit division: this runs
+  // before the CTA's first copy.  Measured on GB300 against floor(M pi / P) in 64-bit arithmetic:
+  // c2 11.58 -> 11.42 us, c3 -0.6%, c4 and c5 unchanged (32-bit floor(M pi / P) alone: 11.50 us).
+  const uint32_t bid = blockIdx.x, P = (uint32_t)p.P;
+  const uint32_t l = bid / P, pi = bid - l * P;
+  const uint32_t q = (uint32_t)p.rows_q, r = (uint32_t)p.rows_r;
+  g.l = l;
+  g.pi = pi;
+  g.m0 = (int64_t)pi * q + (pi < r ? pi : r);
+  g.n = (int)(q + (pi < r ? 1u : 0u));
   g.NT = (g.n + p.tile_rows - 1) / p.tile_rows;
   g.Wc = (blockDim.x >> 5) - 1;
   g.ea = p.G.shared_a ? 0 : g.l;

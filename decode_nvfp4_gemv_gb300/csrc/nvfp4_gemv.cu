@@ -820,6 +820,8 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     a.tile_rows = pl.tile_rows;
     a.stages = pl.stages;
     a.rows_cap = (int32_t)ceil_div(M, pl.ctas_per_batch);
+    a.rows_q = (int32_t)(M / pl.ctas_per_batch);
+    a.rows_r = (int32_t)(M % pl.ctas_per_batch);
     const int64_t nseg = ceil_div(K, nvfp4::kStep);
     a.slots = (int32_t)(rv ? std::min<int64_t>(pl.warps_per_cta, nseg) : pl.warps_per_cta);
     a.early_weights = (pl.flags & NVFP4_FLAG_EARLY_WEIGHTS) ? 1 : 0;
