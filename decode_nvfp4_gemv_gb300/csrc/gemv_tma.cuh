@@ -6,7 +6,8 @@
 // each and need no registers to keep them in flight.  (Measured on GB300: many small bulk copies
 // are slow, so tiles are whole rows and one copy each.)
 //
-// Decomposition.  CTA (l, p), p < P, owns the contiguous rows [M*p/P, M*(p+1)/P) of batch l.
+// Decomposition.  CTA (l, p), p < P, owns q or q + 1 contiguous rows of batch l (M = P q + r; the
+// first r CTAs take q + 1), starting at row p q + min(p, r).
 // Because rows are contiguous in memory, the CTA's A bytes (and its sfa bytes) form one
 // contiguous run, cut into tiles of TR whole rows.  Warp W_c (the last) is the producer: one lane
 // walks the tiles and, for each, waits until ring stage s = T mod NS is free, then issues two
