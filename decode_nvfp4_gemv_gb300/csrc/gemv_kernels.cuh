@@ -106,15 +106,15 @@ __global__ void __launch_bounds__(256) gemv_simple_kernel(
 // ------------------------------------------------------------------------------------------------
 // STREAM: the bandwidth kernel.
 //
-// Decomposition.  CTA (l, p), p < P, owns the contiguous rows [M*p/P, M*(p+1)/P) of batch l (so
-// P * L CTAs, sized by the host to one wave: a multiple of the SM count).  It first decodes b[l]
-// into shared memory as one f16x2 word per packed byte and sfb[l] as fp32.  Its rows are cut
-// into groups of R rows and K into S slices of whole 1024-element steps; each (group, slice) is
-// a unit, and warp w takes units w, w + W, ...  Within a unit, lane t of a step reads 16 bytes
-// (32 elements, two scale blocks) of each of its R rows at k = k0 + 32 t: one warp-wide request
-// covers 512 contiguous bytes of a row.  The step after next is loaded before the current one is
-// computed (across unit boundaries too), so each warp keeps up to 2 * R 16-byte loads per lane in
-// flight.
+// Decomposition.  CTA (l, p), p < P, owns q or q + 1 contiguous rows of batch l, M = P q + r, the
+// first r CTAs taking q + 1 (so P * L CTAs, sized by the host to one wave: a multiple of the SM
+// count).  It first decodes b[l] into shared memory as one f16x2 word per packed byte and sfb[l] as
+// fp32.  Its rows are cut into groups of R rows and K into S slices of whole 1024-element steps;
+// each (group, slice) is a unit, and warp w takes units w, w + W, ...  Within a unit, lane t of a
+// step reads 16 bytes (32 elements, two scale blocks) of each of its R rows at k = k0 + 32 t: one
+// warp-wide request covers 512 contiguous bytes of a row.  The step after next is loaded before the
+// current one is computed (across unit boundaries too), so each warp keeps up to 2 * R 16-byte
+// loads per lane in flight.
 //
 // Per row and step the lane decodes 16 bytes with cvt.rn.f16x2.e2m1x2, multiplies them by the
 // staged vector words with packed f16 FMAs (two chains of 8, one per block: each half-lane sum is
@@ -144,6 +144,7 @@ struct StreamArgs {
   int32_t S;            // K slices per row
   int32_t slice_steps;  // 1024-element steps per slice (the last slice may be shorter)
   int32_t rows_cap;     // ceil(M / P): row capacity of the shared partial array
+  int32_t rows_q, rows_r;  // M = P rows_q + rows_r: the first rows_r CTAs of a batch take one more
   Groups G;             // grouped form (G.E > 0)
   int32_t out_bf16;     // 1: bfloat16 output instead of fp16
 };
@@ -236,10 +237,12 @@ __global__ void __launch_bounds__(512) gemv_stream_kernel(const StreamArgs p) {
   float* part = reinterpret_cast<float*>(smem + 4 * K2 + 4 * K16);     // S x rows_cap floats
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, W = blockDim.x >> 5;
-  const int64_t l = blockIdx.x / p.P;
-  const int64_t pi = blockIdx.x - l * p.P;
-  const int64_t m0 = (p.M * pi) / p.P, m1 = (p.M * (pi + 1)) / p.P;
-  const int n = (int)(m1 - m0);
+  // the batch and the CTA's rows in 32-bit arithmetic, as in the TMA kernels
+  const uint32_t P32 = (uint32_t)p.P, l32 = blockIdx.x / P32, pi32 = blockIdx.x - l32 * P32;
+  const uint32_t q = (uint32_t)p.rows_q, r = (uint32_t)p.rows_r;
+  const int64_t l = l32;
+  const int64_t m0 = (int64_t)pi32 * q + (pi32 < r ? pi32 : r);
+  const int n = (int)(q + (pi32 < r ? 1u : 0u));
   int64_t ea = p.G.shared_a ? 0 : l;  // which matrix of A this CTA reads
   float ga = p.g_a, gb = p.g_b;
   if (p.G.E > 0) {  // grouped: every warp finds the same expert (the offsets do not change)

@@ -10,16 +10,16 @@
 // warp.  A lane's second chunk is the next lane's first, so it is read through L1: DRAM sees
 // each byte once.
 //
-// Decomposition.  CTA (l, p), p < P, owns the contiguous rows [M*p/P, M*(p+1)/P) of batch l.  The
-// CTA stages its vector b[l] in shared memory (one f16x2 word per packed byte, chunk-swizzled;
-// fp32 block scales; both zero-padded to a whole 32-element step).  Warp w takes the row groups
-// (4 rows) w, w + W, ... and walks K in 1024-element steps: lane t takes the 32 elements at
-// 1024 s + 32 t of each of the 4 rows, exactly the item of the TMA kernels (exact f16x2 block
-// partials, mixed-precision scaling, fp32 accumulation).  A lane whose 32 elements straddle K
-// (K % 32 == 16) zeroes its second block's scale byte.  Every load stays inside the caller's
-// buffers: a chunk that would begin before the first or end past the last byte of A (or of the
-// batch's vector) is assembled from byte loads instead.  All loads of a step are issued before the
-// first use, so the four rows' DRAM round trips overlap.
+// Decomposition.  CTA (l, p), p < P, owns q or q + 1 contiguous rows of batch l (M = P q + r; the
+// first r CTAs take q + 1).  The CTA stages its vector b[l] in shared memory (one f16x2 word per
+// packed byte, chunk-swizzled; fp32 block scales; both zero-padded to a whole 32-element step).
+// Warp w takes the row groups (4 rows) w, w + W, ... and walks K in 1024-element steps: lane t
+// takes the 32 elements at 1024 s + 32 t of each of the 4 rows, exactly the item of the TMA kernels
+// (exact f16x2 block partials, mixed-precision scaling, fp32 accumulation).  A lane whose 32
+// elements straddle K (K % 32 == 16) zeroes its second block's scale byte.  Every load stays inside
+// the caller's buffers: a chunk that would begin before the first or end past the last byte of A
+// (or of the batch's vector) is assembled from byte loads instead.  All loads of a step are issued
+// before the first use, so the four rows' DRAM round trips overlap.
 //
 // Measured on GB300 (7168 x 16384, every operand 1 byte off): 27.9 us per call against 35.1 us for
 // the byte-load kernel.  It is latency-bound: a warp owns whole rows, so the 7168 rows keep at
@@ -45,6 +45,7 @@ struct ShiftArgs {
   int64_t M, K, L;
   int64_t a_bytes;   // readable bytes of A from A (every matrix), for the end-of-buffer guard
   int32_t P;         // CTAs per batch
+  int32_t rows_q, rows_r;  // M = P rows_q + rows_r: the first rows_r CTAs of a batch take one more
   Groups G;
   int32_t out_bf16;
 };
@@ -61,8 +62,12 @@ __global__ void __launch_bounds__(256, 2) gemv_shift_kernel(const ShiftArgs p) {
   uint32_t* bq = reinterpret_cast<uint32_t*>(smem);             // Kp/2 words, chunk-swizzled
   float* sbf = reinterpret_cast<float*>(smem + Kp * 2);         // Kp/16 block scales
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
-  const int64_t l = blockIdx.x / p.P, pi = blockIdx.x - l * p.P;
-  const int64_t m0 = (p.M * pi) / p.P, n = (p.M * (pi + 1)) / p.P - m0;
+  // the batch and the CTA's rows in 32-bit arithmetic, as in the TMA kernels
+  const uint32_t P32 = (uint32_t)p.P, l32 = blockIdx.x / P32, pi32 = blockIdx.x - l32 * P32;
+  const uint32_t q = (uint32_t)p.rows_q, r = (uint32_t)p.rows_r;
+  const int64_t l = l32;
+  const int64_t m0 = (int64_t)pi32 * q + (pi32 < r ? pi32 : r);
+  const int64_t n = q + (pi32 < r ? 1u : 0u);
 
   pdl_launch_dependents();
   pdl_wait();

@@ -768,6 +768,8 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     const int64_t n_mats = G.E > 0 ? (int64_t)G.E : (G.shared_a ? 1 : L);  // matrices in A
     a.a_bytes = n_mats * M * (K / 2);
     a.P = pl.ctas_per_batch;
+    a.rows_q = (int32_t)(M / pl.ctas_per_batch);
+    a.rows_r = (int32_t)(M % pl.ctas_per_batch);
     a.G = G;
     a.out_bf16 = out_bf16;
     cudaLaunchConfig_t cfg;
@@ -797,6 +799,8 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     a.G = G;
     a.out_bf16 = out_bf16;
     a.P = pl.ctas_per_batch;
+    a.rows_q = (int32_t)(M / pl.ctas_per_batch);
+    a.rows_r = (int32_t)(M % pl.ctas_per_batch);
     const int64_t steps = ceil_div(K, nvfp4::kStep);
     a.slice_steps = (int32_t)ceil_div(steps, pl.k_split);
     a.S = (int32_t)ceil_div(steps, a.slice_steps);
