@@ -231,6 +231,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
   const uint32_t stage_tx = kTcRows * kTcChunkBytes + (uint32_t)p.N * kTcChunkBytes +
                             kTcRows * 16u + (uint32_t)p.N * 16u;  // bytes of one stage's copies
   const bool early_in_setup = p.early_weights && !p.test_stall && p.S > 1;
+  // With static weights the first stages' A and sfa copies go out before the launch wait: stage g
+  // expects all of its bytes, the vectors' copies follow after the wait.
+  auto request_early_weights = [&](int g) {
+    const int k = g / w.nloc, i = g - k * w.nloc;
+    int l, tile, ar, br;
+    tc_rows(p, w.u0 + k * w.ustep, l, tile, ar, br);
+    const uint32_t st = ring32 + g * kTcStageBytes, full = smem_addr(&h->full[g]);
+    mbar_arrive_expect_tx(full, stage_tx);
+    tma_load_2d(st, &mA, (w.c0 + i) * kTcChunkBytes, ar, full);
+    tma_load_2d(st + kTcOffSA, &mSA, (w.c0 + i) * 16, ar, full);
+  };
 
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -259,17 +270,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
     // zeroing below and the CTA barrier.  Measured on GB300 (M = 7168, K = 16384): N = 2 / 8 / 16
     // from 14.00 / 13.92 / 14.35 to 13.38 / 13.56 / 14.16 us; persistent CTAs (S = 1) measured 2%
     // slower with it, so they request them after the CTA barrier.
-    if (early_in_setup) {
-      for (int g = 0; g < min(NS, npairs); ++g) {
-        const int k = g / w.nloc, i = g - k * w.nloc;
-        int l, tile, ar, br;
-        tc_rows(p, w.u0 + k * w.ustep, l, tile, ar, br);
-        const uint32_t st = ring32 + g * kTcStageBytes, full = smem_addr(&h->full[g]);
-        mbar_arrive_expect_tx(full, stage_tx);
-        tma_load_2d(st, &mA, (w.c0 + i) * kTcChunkBytes, ar, full);
-        tma_load_2d(st + kTcOffSA, &mSA, (w.c0 + i) * 16, ar, full);
-      }
-    }
+    if (early_in_setup)
+      for (int g = 0; g < min(NS, npairs); ++g) request_early_weights(g);
   }
   // token rows N .. 15 of every stage are never written by the copies: zero them once
   const int zero_words = (kTcCols - p.N) * 32;
@@ -289,18 +291,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && !p.test_stall) {  // stalled: every wait for its copies runs out
-      // with static weights the first stages' A and sfa copies start before the launch wait
-      // (under split K they already went out during the set-up above)
+      // static weights: the first stages' A and sfa copies before the launch wait (under split K
+      // they already went out during the set-up above)
       const int pre = p.early_weights ? min(NS, npairs) : 0;
-      for (int g = 0; g < (early_in_setup ? 0 : pre); ++g) {
-        const int k = g / w.nloc, i = g - k * w.nloc;
-        int l, tile, ar, br;
-        tc_rows(p, w.u0 + k * w.ustep, l, tile, ar, br);
-        const uint32_t st = ring32 + g * kTcStageBytes, full = smem_addr(&h->full[g]);
-        mbar_arrive_expect_tx(full, stage_tx);
-        tma_load_2d(st, &mA, (w.c0 + i) * kTcChunkBytes, ar, full);
-        tma_load_2d(st + kTcOffSA, &mSA, (w.c0 + i) * 16, ar, full);
-      }
+      if (!early_in_setup)
+        for (int g = 0; g < pre; ++g) request_early_weights(g);
       pdl_wait();
       for (int g = 0; g < pre; ++g) {
         const int k = g / w.nloc, i = g - k * w.nloc;
