@@ -3,13 +3,14 @@
 // cutedsl/bridge.py (nvfp4-megamoe-kernel), section "Quantization", quantize_activation_nvfp4:
 // with the global scale given, every 16-element block is quantized on its own, so one thread (or
 // one lane) owns whole blocks and the step needs no reduction across threads or kernels.  All
-// arithmetic is fp32 in the page's order, with IEEE round-to-nearest divisions:
-//   x_norm = x / gs;  amax = max(max |x_norm|, 1e-8);  scale = e4m3_rn_sat(amax / 6);
+// arithmetic is fp32 with IEEE round-to-nearest divisions, as the page's torch operations are:
+//   x_norm = x / gs;  amax = max(max |x_norm|, 1e-8);  scale = e4m3(amax / 6);
 //   x_scaled = x_norm / max(scale, 1e-8);  magnitude = min(|x_scaled|, 6);
 //   code = table[rint(2 * magnitude)] (the page's half-step table) or the nearest E2M1 grid point
 //   with ties to the even code;  nibble = code | 8 if x_scaled < 0.
-// A block scale that rounds above 448 saturates to 448 (the conversion is `satfinite`).  Inputs
-// are finite bf16 values (a NaN input gives unspecified bytes for its block).
+// The scale conversion is the page's float8_e4m3fn cast: nearest, ties to even, and NaN (0x7F)
+// for a value past 464 (it would round beyond 448, the largest finite E4M3).  The block's codes
+// are then 0.  Inputs are finite bf16 values (a NaN input gives unspecified bytes for its block).
 #pragma once
 
 #include <stdint.h>
@@ -23,10 +24,16 @@ enum : int { kRoundHalfStepTable = 0, kRoundNearestEven = 1 };
 // half-step table [0, 1, 2, 3, 4, 4, 5, 5, 6, 6, 6, 7, 7], entry i in bits 4i .. 4i+3
 constexpr uint64_t kHalfStepTable = 0x7766655443210ull;
 
-// Two fp32 values -> two E4M3FN bytes (round to nearest even, saturating): low byte from `lo`.
-__device__ __forceinline__ uint16_t f32x2_to_e4m3x2_sat(float lo, float hi) {
+// Two non-negative fp32 values -> two E4M3FN bytes, low byte from `lo`: round to nearest even;
+// a value past 464 has no finite encoding and gives NaN (0x7F), as a float8_e4m3fn cast does.
+// (The hardware conversion saturates instead, so those two cases are patched after it.)
+constexpr uint32_t kE4m3Nan = 0x7Fu;
+
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  if (lo > 464.0f) r = (uint16_t)((r & 0xFF00u) | kE4m3Nan);
+  if (hi > 464.0f) r = (uint16_t)((r & 0x00FFu) | (kE4m3Nan << 8));
   return r;
 }
 
@@ -64,16 +71,17 @@ __device__ __forceinline__ void quantize_blocks2(const uint32_t (&xv)[16], float
   }
   a0 = fmaxf(a0, 1e-8f);
   a1 = fmaxf(a1, 1e-8f);
-  sf2 = f32x2_to_e4m3x2_sat(__fdiv_rn(a0, 6.0f), __fdiv_rn(a1, 6.0f));
+  sf2 = f32x2_to_e4m3x2(__fdiv_rn(a0, 6.0f), __fdiv_rn(a1, 6.0f));
   const float2 sv = f16x2_to_f32x2(e4m3x2_to_f16x2(sf2));
   const float d0 = fmaxf(sv.x, 1e-8f), d1 = fmaxf(sv.y, 1e-8f);
+  const bool nan0 = (sf2 & 0xFFu) == kE4m3Nan, nan1 = (sf2 >> 8) == kE4m3Nan;
 #pragma unroll
   for (int w = 0; w < 4; ++w) packed[w] = 0u;
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const float xs = __fdiv_rn(xn[i], i < 16 ? d0 : d1);
     const uint32_t nib = e2m1_code(fminf(fabsf(xs), 6.0f), rounding) | (xs < 0.f ? 8u : 0u);
-    packed[i >> 3] |= nib << (4 * (i & 7));
+    if (!(i < 16 ? nan0 : nan1)) packed[i >> 3] |= nib << (4 * (i & 7));
   }
 }
 
@@ -98,13 +106,14 @@ __global__ void __launch_bounds__(256) quantize_activation_kernel(
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
   a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
   a = fmaxf(a, 1e-8f);
-  const uint16_t s2 = f32x2_to_e4m3x2_sat(__fdiv_rn(a, 6.0f), 0.f);
+  const uint16_t s2 = f32x2_to_e4m3x2(__fdiv_rn(a, 6.0f), 0.f);
   const float d = fmaxf(f16x2_to_f32x2(e4m3x2_to_f16x2(s2)).x, 1e-8f);
   const float xs0 = __fdiv_rn(xn0, d), xs1 = __fdiv_rn(xn1, d);
   const uint32_t nib0 = e2m1_code(fminf(fabsf(xs0), 6.0f), rounding) | (xs0 < 0.f ? 8u : 0u);
   const uint32_t nib1 = e2m1_code(fminf(fabsf(xs1), 6.0f), rounding) | (xs1 < 0.f ? 8u : 0u);
+  const bool nan_scale = (s2 & 0xFFu) == kE4m3Nan;  // the block's codes are 0
   if (valid) {
-    b[t] = (uint8_t)(nib0 | (nib1 << 4));
+    b[t] = nan_scale ? (uint8_t)0 : (uint8_t)(nib0 | (nib1 << 4));
     if ((t & 7) == 0) sfb[t >> 3] = (uint8_t)(s2 & 0xFFu);
   }
 }

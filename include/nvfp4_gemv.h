@@ -204,9 +204,11 @@ const char* nvfp4_last_error(void);
  * x [L][K] -> packed E2M1 b [L][K/2] and E4M3FN block scales sfb [L][K/16], with a fixed fp32
  * global scale (x ~= global_scale * e4m3(sfb) * e2m1(b)).  Per 16-element block, in fp32 with IEEE
  * round-to-nearest divisions: x_norm = x / global_scale; scale = e4m3(max(max|x_norm|, 1e-8) / 6)
- * rounded to nearest even and saturating at 448; x_scaled = x_norm / max(scale, 1e-8); magnitude
- * min(|x_scaled|, 6) rounded to E2M1 by `rounding`; the sign of x_scaled.  Each block is
- * independent, so the step needs no reduction and no workspace.  x must hold finite values.
+ * rounded to nearest even, as the page's float8_e4m3fn cast does: a value past 464 has no finite
+ * encoding and gives the NaN byte 0x7F, and that block's codes are 0 (so every output that uses
+ * the block is NaN); x_scaled = x_norm / max(scale, 1e-8); magnitude min(|x_scaled|, 6) rounded
+ * to E2M1 by `rounding`; the sign of x_scaled.  Each block is independent, so the step needs no
+ * reduction and no workspace.  x must hold finite values.
  * ------------------------------------------------------------------------------------------ */
 enum {
   NVFP4_ROUND_HALF_STEP_TABLE = 0,  /* the page's rule: table[rint(2 * magnitude)], table =

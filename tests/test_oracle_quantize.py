@@ -24,18 +24,54 @@ def _torch_e4m3(v):
     return t.view(torch.uint8).numpy()
 
 
-def test_e4m3_encoder_matches_torch_in_range():
+def _encoder_inputs():
+    """Every finite E4M3 value, every midpoint between neighbours and the fp32 values next to
+    them, the edge past 448 (the midpoint 464 and the NaN range above it), and random values over
+    the whole fp32 range the block scale can take."""
     pos = E4M3FN_TABLE[:0x7F]
-    mids = (pos[:-1] + pos[1:]) / 2
-    vals = np.concatenate([pos, mids, np.nextafter(mids.astype(np.float32), 0),
+    mids = np.concatenate([(pos[:-1] + pos[1:]) / 2, [464.0]])
+    rng = np.random.default_rng(0)
+    return np.concatenate([pos, mids, np.nextafter(mids.astype(np.float32), 0),
                            np.nextafter(mids.astype(np.float32), np.inf),
-                           np.random.default_rng(0).uniform(0, 460, 20000)]).astype(np.float32)
-    vals = vals[vals < 464]                      # torch turns values rounding past 448 into NaN
+                           rng.uniform(0, 500, 20000), rng.uniform(440, 490, 5000),
+                           np.exp2(rng.uniform(-40, 40, 5000)), [479.99, 480.0, 1e30, 3e38],
+                           [np.inf, np.nan]]).astype(np.float32)
+
+
+def test_e4m3_encoder_matches_torch_over_the_whole_range():
+    """[Bridge] casts block_amax / 6 with torch's float8_e4m3fn conversion; the encoder must give
+    the same byte for every non-negative fp32 input, NaN (0x7F) past 464 included."""
+    vals = _encoder_inputs()
     assert np.array_equal(Q.e4m3_encode_rne(vals), _torch_e4m3(vals))
 
 
-def test_e4m3_encoder_saturates():
-    assert Q.e4m3_encode_rne(np.float32([463.9, 464.0, 1e6])).tolist() == [0x7E] * 3
+def test_e4m3_encoder_nan_past_464():
+    got = Q.e4m3_encode_rne(np.float32([448.0, 463.9, 464.0, 464.01, 470.0, 1e6, np.nan]))
+    assert got.tolist() == [0x7E, 0x7E, 0x7E, 0x7F, 0x7F, 0x7F, 0x7F]
+
+
+@pytest.mark.parametrize("rounding", ["lut", "rne"])
+def test_overflowing_block_scale_is_nan_with_zero_codes(rounding):
+    """A block whose largest normalised magnitude / 6 lies past 464 has no finite scale: the
+    cast gives NaN (byte 0x7F); its codes are 0 (reading), other blocks are unaffected."""
+    gs = np.float32(0.25)
+    x = np.random.default_rng(5).standard_normal((2, 64)).astype(np.float32)
+    x[0, 16:32] = np.linspace(-3000, 3000, 16, dtype=np.float32)   # 3000 / 0.25 / 6 = 2000
+    x[1, 48] = np.float32(464.5 * 6 * 0.25)
+    packed, sfb = Q.quantize_activation(x, gs, rounding)
+    assert sfb[0, 1] == 0x7F and sfb[1, 3] == 0x7F
+    assert (packed[0, 8:16] == 0).all() and (packed[1, 24:32] == 0).all()
+    keep = np.ones_like(sfb, dtype=bool)
+    keep[0, 1] = keep[1, 3] = False
+    assert (sfb[keep] != 0x7F).all()
+    x2 = x.copy()
+    x2[0, 16:32] = 0.0
+    x2[1, 48:64] = 0.0
+    p2, s2 = Q.quantize_activation(x2, gs, rounding)
+    assert np.array_equal(s2[keep], sfb[keep])
+    for r, blk in ((0, 1), (1, 3)):
+        p2[r, 8 * blk:8 * blk + 8] = packed[r, 8 * blk:8 * blk + 8]
+    assert np.array_equal(p2, packed)
 
 
 @pytest.mark.parametrize("rounding", ["lut", "rne"])

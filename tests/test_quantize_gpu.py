@@ -53,7 +53,8 @@ def dev_bf16(x32):
 
 
 def special_blocks(gs):
-    """16-element blocks of edge values for global scale gs (bf16-rounded)."""
+    """16-element blocks of edge values for global scale gs (bf16-rounded), all with a finite
+    block scale (overflow_blocks has the ones whose scale is NaN)."""
     up, down = np.float32(1 + 2.0 ** -7), np.float32(1 - 2.0 ** -8)   # bf16 neighbours of 1
     mids = np.concatenate([MIDS, -MIDS, [0.3]]).astype(np.float32)      # 15 values
     rows = [
@@ -64,8 +65,7 @@ def special_blocks(gs):
         np.concatenate([[6.0], mids * up]) * gs,                 # just above the midpoints
         np.concatenate([[6.0], mids * down]) * gs,               # just below
         np.concatenate([[-6.0], mids]) * gs * 448,               # the largest scale, exactly
-        np.full(16, 3000.0 * 6, np.float32) * gs,                # scale saturates at 448
-        np.linspace(-1e5, 1e5, 16, dtype=np.float32) * gs,       # far beyond: clamped magnitudes
+        np.concatenate([[6.0 * 460], mids * 460]) * gs,          # 448 < amax / 6 < 464: 448
         np.full(16, 1e-12, np.float32),                          # scale 0 (floor 1e-8)
         np.array([1e-40, -1e-39, 3e-38, 0.0] * 4, np.float32),   # subnormal and tiny
         np.concatenate([[6.0, 0.0], GRID[1:], -GRID[1:]]) * gs * 2.0 ** -9,   # smallest scale
@@ -75,14 +75,26 @@ def special_blocks(gs):
     return bf16_round(np.stack(rows).astype(np.float32))
 
 
-def activation(K, L, seed, gs, plant=True):
+def overflow_blocks(gs):
+    """Blocks whose largest |x / gs| / 6 lies past 464: no finite E4M3 scale, so the page's cast
+    gives NaN (0x7F) and the block's codes are 0."""
+    rows = [np.full(16, 3000.0 * 6, np.float32) * gs,
+            np.linspace(-1e5, 1e5, 16, dtype=np.float32) * gs,
+            np.concatenate([[6.0 * 466.0, 0.0], GRID[1:], -GRID[1:]]).astype(np.float32) * gs]
+    return bf16_round(np.stack(rows).astype(np.float32))
+
+
+def activation(K, L, seed, gs, plant=True, overflow=False):
     """Seeded normal bf16 values, each 16-block multiplied by 2^e (e spread so that block scales
-    cover the E4M3 range for this gs), with the special blocks planted at seeded positions."""
+    cover the E4M3 range for this gs), with the special blocks planted at seeded positions (and
+    the overflowing ones too, if asked: their scales are NaN)."""
     x = workloads.normal_bf16(seed, "x", K * L).reshape(L, K // 16, 16)
-    e = (np.arange(L * (K // 16)) * 7 % 34 - 22).reshape(L, K // 16, 1).astype(np.float32)
+    e = (np.arange(L * (K // 16)) * 7 % 31 - 22).reshape(L, K // 16, 1).astype(np.float32)
     x = bf16_round(x * np.float32(gs) * np.exp2(e))
     if plant:
         sp = special_blocks(np.float32(gs))
+        if overflow:
+            sp = np.concatenate([sp, overflow_blocks(np.float32(gs))])
         flat = x.reshape(-1, 16)
         idx = (np.arange(len(sp)) * 2654435761 + seed) % len(flat)
         flat[idx] = sp[: len(idx)]
@@ -117,7 +129,7 @@ QSHAPES = [(16, 1), (48, 3), (256, 2), (1040, 1), (4096, 5), (16384, 1), (7168, 
 @pytest.mark.parametrize("gs", [1.0, 2.0 ** -7, 0.0123, 37.5])
 def test_quantizer_bytes_bit_exact(pkg, rounding, name, gs):
     for K, L in QSHAPES:
-        x = activation(K, L, seed=K + 31 * L, gs=gs)
+        x = activation(K, L, seed=K + 31 * L, gs=gs, overflow=True)
         b, s = run_quantize(pkg, x, gs, rounding)
         pr, sr = Q.quantize_activation(x, gs, name)
         assert_bytes_equal(s, sr, f"sfb K={K} L={L} gs={gs} {name}")
@@ -134,8 +146,47 @@ def test_special_blocks_alone(pkg):
             assert_bytes_equal(s, sr, f"special sfb gs={gs} {name}")
             assert_bytes_equal(b, pr, f"special b gs={gs} {name}")
             if gs == 1.0:
-                assert s[7, 0] == 0x7E                     # saturated block scale
-                assert s[9, 0] == 0x00                     # below the smallest subnormal
+                assert s[6, 0] == 0x7E                     # the largest finite block scale
+                assert s[7, 0] == 0x7E                     # rounds down to 448
+                assert s[8, 0] == 0x00                     # below the smallest subnormal
+            ob = overflow_blocks(np.float32(gs))
+            b, s = run_quantize(pkg, ob, gs, rounding)
+            pr, sr = Q.quantize_activation(ob, gs, name)
+            assert_bytes_equal(s, sr, f"overflow sfb gs={gs} {name}")
+            assert_bytes_equal(b, pr, f"overflow b gs={gs} {name}")
+            assert (s == 0x7F).all() and (b == 0).all()    # NaN scales, codes 0
+    # the edge itself (global scale 1, exact): amax / 6 == 464 ties to 448; the next bf16 above
+    # 2784 (= 6 * 464) gives NaN
+    edge = np.zeros((2, 16), np.float32)
+    edge[0, 0], edge[1, 0] = 2784.0, 2800.0
+    for rounding, name in ROUNDINGS:
+        b, s = run_quantize(pkg, edge, 1.0, rounding)
+        assert s[:, 0].tolist() == [0x7E, 0x7F] and (b[1] == 0).all()
+        pr, sr = Q.quantize_activation(edge, 1.0, name)
+        assert_bytes_equal(s, sr, f"edge sfb {name}")
+        assert_bytes_equal(b, pr, f"edge b {name}")
+
+
+@pytest.mark.parametrize("flags", [1, 1 | 4], ids=["quantizer-then-gemv", "in-gemv"])
+def test_overflowing_block_gives_nan_on_both_sides(pkg, flags):
+    """A planted block whose scale has no finite E4M3 encoding: its scale byte is NaN on the GPU
+    as in the oracle, so every output of that batch is NaN on both sides; the other batch is
+    unaffected and within tolerance."""
+    M, K, L = 256, 2048, 2
+    gs = 0.0173
+    w = workloads.random_workload(M, K, L, seed=77, scale_bytes=workloads.pow2_scale_bytes(-3, 2))
+    x = activation(K, L, seed=78, gs=gs, plant=False)
+    x[1, 512:528] = overflow_blocks(np.float32(gs))[0]
+    pr, sr = Q.quantize_activation(x, gs, "lut")
+    assert sr[1, 32] == 0x7F and (sr[0] != 0x7F).all()
+    ref, T = oracle.gemv(w.A, w.sfa, w.g_a, pr, sr, gs, M, K, L)
+    assert np.isnan(ref[1]).all() and not np.isnan(ref[0]).any()
+    A, sfa = torch.from_numpy(w.A).cuda(), torch.from_numpy(w.sfa).cuda()
+    c, b, s = gemv_bf16(pkg, A, sfa, w.g_a, x, gs, 0, M, {"flags": flags})
+    assert_bytes_equal(s, sr, "sfb_out with an overflowing block")
+    assert_bytes_equal(b, pr, "b_out with an overflowing block")
+    assert np.isnan(c[1]).all()
+    assert_parity(c, ref, T, "overflowing block")
 
 
 def test_the_two_roundings_differ_where_expected(pkg):
