@@ -8,14 +8,21 @@ seeded input generator ``workloads``, which holds none of the GEMV's arithmetic.
 
 Contents, each written from the pages' definitions (citations in each module):
 
+* ``nvfp4_ref.c`` (loaded by ``cref``) the plain C oracle: E2M1 / E4M3FN decoders from their
+               closed forms, the GEMV definition in fp64 summed in increasing k (one output row per
+               OpenMP work item, so the thread count does not change a bit), the exact-integer
+               formulation, the grouped form, the activation quantizer (fp32, the page's
+               operations) and fp16 rounding.  ``gemv``, ``gemv_rows``, ``gemv_exact_units`` and
+               ``gemv_fp16`` below are these C functions.
 * ``codecs``   E2M1 / E4M3FN decoders from their bit layouts, nibble unpacking, fp16 rounding.
-* ``nvfp4_gemv`` the GEMV definition in fp64 (``gemv``, ``gemv_rows``) and an independent exact
-               integer formulation (``gemv_exact_units``).
+* ``nvfp4_gemv`` the same GEMV definition written a second time, in numpy fp64 (its ``gemv``,
+               ``gemv_rows``, ``gemv_exact_units``), kept as an independent cross-check of the C
+               code: the two agree bit for bit.
 * ``grouped``  the grouped (mixture-of-experts) decode GEMV: expert ownership from the bridge's
                cumulative offsets or from a per-token index, then the GEMV definition per token.
 * ``quantize`` the NVFP4 activation quantizer with a fixed global scale (bridge.py,
-               ``quantize_activation_nvfp4``): the page's half-step-table rounding and
-               round-to-nearest-even, fp32 steps in the page's order.
+               ``quantize_activation_nvfp4``) in numpy fp32: the page's half-step-table rounding
+               and round-to-nearest-even; a block scale with no finite E4M3 encoding is NaN.
 
 Pins (tests that tie the oracle to something other than itself):
 
@@ -28,6 +35,8 @@ Pins (tests that tie the oracle to something other than itself):
 * algebraic invariants (zero scale, doubled scale, nibble swap, negation, block permutation,
   batch independence);
 * ``gemv`` == ``gemv_exact_units`` bit for bit on all five workloads (sampled rows at full size);
+* the C and numpy formulations bit for bit on all five workloads, the grouped workloads and the
+  quantizer; C planted mistakes (mutated copies of the C source) each fail a pin;
 * planted mistakes (swapped nibbles, dropped scale, off-by-one block index, ...) each fail a pin.
 * quantizer: the printed half-step table; its E4M3 encoder against torch's cast; exact grid
   round-trips; brute-force nearest rounding; error bounds; sign symmetry; bit-for-bit agreement
@@ -40,11 +49,22 @@ Pins (tests that tie the oracle to something other than itself):
 
 No function in this package is "parity unpinned".
 """
+import numpy as _np
+
+from . import cref
 from .codecs import (E2M1_TABLE, E4M3FN_TABLE, e2m1_value, e4m3fn_value, fp16_round,
                      unpack_e2m1_codes)
-from .nvfp4_gemv import BLOCK, TERM_UNIT_EXP, gemv, gemv_exact_units, gemv_fp16, gemv_rows
+from .cref import gemv, gemv_exact_units, gemv_rows
+from .nvfp4_gemv import BLOCK, TERM_UNIT_EXP
+
+
+def gemv_fp16(A, sfa, g_a, b, sfb, g_b, M, K, L):
+    """``gemv`` rounded to binary16 (round to nearest even, from fp64), as float16 [L][M]."""
+    c_ref, _ = gemv(A, sfa, g_a, b, sfb, g_b, M, K, L)
+    return cref.fp16_bits(c_ref).view(_np.float16)
+
 
 __all__ = [
-    "E2M1_TABLE", "E4M3FN_TABLE", "e2m1_value", "e4m3fn_value", "fp16_round", "unpack_e2m1_codes",
+    "cref", "E2M1_TABLE", "E4M3FN_TABLE", "e2m1_value", "e4m3fn_value", "fp16_round", "unpack_e2m1_codes",
     "BLOCK", "TERM_UNIT_EXP", "gemv", "gemv_exact_units", "gemv_fp16", "gemv_rows",
 ]
