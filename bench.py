@@ -8,20 +8,26 @@ is the decode GEMV M=7168, K=16384, L=1 (66.1 MB per call).  Prints ONE JSON lin
   metric / value / unit   achieved HBM GB/s of algorithmic bytes (M*K*L/2 + M*K*L/16 + K*L/2 +
                           K*L/16 + 2*M*L per call), whole job over all ranks, inputs resident in HBM
   us_per_call, pct_of_peak
+  per_config              the five decode workloads c1..c5 in the same run: us per call over the
+                          K timed steps and in steady state (graphs of 1000 calls), GB/s, fraction
+                          of peak, strict stream order, the plan
+  small_ml                few output rows (M*L = 16..512) with long K: the split-K regime
   e2e                     the same metric through the public call with host buffers: every step
                           copies its inputs from pinned host memory and reads back c
   roofline                dominant kernel vs the measured HBM copy bandwidth
-  cpu_baseline            the CPU oracle on a bounded sample of the same workload
+  cpu_baseline            the plain C oracle (fp64) on the host cores, one thread and OpenMP
   clocks                  nvidia-smi samples taken during the timed region
 
 Timing: W warm-up steps, then exactly K steps timed with CUDA events on the launching stream,
 barrier + synchronize on both sides, max over ranks.  L2 residency is defeated by rotating over
 copies of the inputs totalling more than 3x the L2 size (each step reads a different copy).  The
-launches are captured in CUDA graphs (1000 calls per graph) so the host launch rate cannot limit
-the measurement.
+launches are captured in CUDA graphs (up to 1000 calls per graph), and a short spin kernel runs
+ahead of the start event, so that by the time the device reaches the start event the host has
+queued the timed graphs: the device-timed region holds the K calls, not the host's launch latency.
 
-Multi-GPU (torchrun): the GEMV needs no exchange between GPUs, so each rank runs an independent
-replica on its own GPU (weak scaling) and rank 0 reports the sum of bytes over the max time.
+Multi-GPU: the GEMV needs no exchange between GPUs, so each rank runs an independent replica on
+its own GPU (weak scaling) and rank 0 reports the sum of bytes over the max time.  Under torchrun
+(WORLD_SIZE set) --gpus must equal WORLD_SIZE; without it, --gpus N > 1 starts the N ranks itself.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
 """
@@ -31,6 +37,7 @@ import argparse
 import hashlib
 import json
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -52,6 +59,7 @@ FLAG_QUANTIZE_IN_GEMV = 4   # nvfp4_plan.flags: quantize the bf16 vector inside 
 KERNEL_NAMES = {1: "gemv_simple_kernel", 2: "gemv_stream_kernel", 3: "gemv_tma_kernel",
                 4: "gemv_tma_rv_kernel", 5: "gemv_tc_kernel", 6: "gemv_shift_kernel"}
 DEFAULT_PEAK_GBS = 6800.0   # only if MEASURED_PEAKS.json is absent
+PREROLL_CYCLES = 200_000    # spin kernel ahead of every start event (~0.1 ms at 2 GHz)
 
 
 # ---------------------------------------------------------------------------- distributed helpers
@@ -61,6 +69,25 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def free_port() -> int:
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """Starts bench.py once per rank (RANK / LOCAL_RANK / WORLD_SIZE / MASTER_* set, as torchrun
+    would) and waits for all of them; returns the worst exit code."""
+    port = str(free_port())
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n),
+                   LOCAL_WORLD_SIZE=str(n), MASTER_ADDR="127.0.0.1", MASTER_PORT=port)
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), *argv], env=env))
+    codes = [p.wait() for p in procs]
+    return max(abs(c) for c in codes)
 
 
 def dist_init(world):
@@ -254,39 +281,211 @@ def _device_inputs(w, n_copies, device):
     return sets
 
 
-def time_device(pkg, w, sets, outs, plan, steps, warmup, stream):
-    """Returns (seconds for exactly `steps` calls, launches)."""
+def _copies_for(bytes_per_call, device):
+    """Input copies whose total exceeds 3x the L2 size (at least 2)."""
     import torch
 
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    return max(2, -(-3 * l2 // bytes_per_call) + 1), l2
+
+
+def _preroll():
+    """A spin kernel on the current stream ahead of a start event: while it runs, the host queues
+    the start event and the timed graphs, so the device-timed region starts with the first call
+    rather than with the host's graph launch."""
+    import torch
+
+    torch.cuda._sleep(PREROLL_CYCLES)
+
+
+class GraphTimer:
+    """`steps` calls of fn(i) captured in CUDA graphs of up to GRAPH_CHUNK calls (a full graph
+    repeated, plus one graph of the remainder), after `warmup` uncaptured calls."""
+
+    def __init__(self, fn, steps, warmup, stream):
+        import torch
+
+        self.stream, self.steps = stream, steps
+        with torch.cuda.stream(stream):
+            for i in range(max(warmup, 1)):          # uncaptured warm-up (caches device info too)
+                fn(i)
+        stream.synchronize()
+        self.chunk = min(GRAPH_CHUNK, steps)
+        self.full = self._capture(fn, self.chunk)
+        rem = steps % self.chunk
+        self.rem = self._capture(fn, rem) if rem else None
+        with torch.cuda.stream(stream):              # graph warm-up
+            self.full.replay()
+        stream.synchronize()
+
+    def _capture(self, fn, count):
+        import torch
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(count):
+                fn(i)
+        return g
+
+    def replay_all(self):
+        for _ in range(self.steps // self.chunk):
+            self.full.replay()
+        if self.rem is not None:
+            self.rem.replay()
+
+    def time(self, dist, device, sampler=None):
+        """Seconds for the `steps` calls: barrier + synchronize on both sides, the pre-roll spin
+        kernel, then CUDA events on the launching stream around the replays."""
+        import torch
+
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ctx = sampler if sampler is not None else _Null()
+        with ctx, torch.cuda.stream(self.stream):
+            barrier(dist)
+            torch.cuda.synchronize(device)
+            _preroll()
+            ev0.record(self.stream)
+            self.replay_all()
+            ev1.record(self.stream)
+            torch.cuda.synchronize(device)
+            barrier(dist)
+        return ev0.elapsed_time(ev1) / 1e3
+
+    def spread(self, device, n_rep=20):
+        """p10 / median / p90 of us per call over n_rep replays of the full graph, each between
+        two events (after the timed region)."""
+        import torch
+
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+        with torch.cuda.stream(self.stream):
+            _preroll()
+            evs[0].record(self.stream)
+            for i in range(n_rep):
+                self.full.replay()
+                evs[i + 1].record(self.stream)
+            torch.cuda.synchronize(device)
+        per = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 / self.chunk for i in range(n_rep))
+        return {"replays": n_rep, "calls_per_replay": self.chunk,
+                "p10_us": round(per[n_rep // 10], 3), "median_us": round(per[n_rep // 2], 3),
+                "p90_us": round(per[(9 * n_rep) // 10], 3)}
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+def _graph_time(fn, stream, steps, warmup, dist, dev):
+    """Seconds and calls for exactly `steps` calls of fn(i) replayed from CUDA graphs."""
+    t = GraphTimer(fn, steps, warmup, stream)
+    sec = t.time(dist, dev)
+    del t
+    return sec, steps
+
+
+def _gemv_caller(pkg, w, sets, outs, plan, stream):
     n = len(sets)
 
     def call(i):
         s = sets[i % n]
         pkg.nvfp4_gemv_batched_ex(s["A"], s["sfa"], w.g_a, s["b"], s["sfb"], w.g_b, outs[i % n],
                                   w.M, w.K, w.L, stream=stream, plan=plan)
-
-    def make_graph(count, offset):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(count):
-                call(offset + i)
-        return g
-
-    with torch.cuda.stream(stream):
-        for i in range(max(warmup, 1)):            # uncaptured warm-up (also caches device info)
-            call(i)
-    stream.synchronize()
-    chunk = min(GRAPH_CHUNK, steps)
-    g_full = make_graph(chunk, 0) if chunk else None
-    rem = steps % chunk if chunk else 0
-    g_rem = make_graph(rem, 0) if rem else None
-    with torch.cuda.stream(stream):                # graph warm-up
-        for _ in range(2):
-            g_full.replay()
-    stream.synchronize()
-    return g_full, g_rem, chunk, rem
+    return call
 
 
+def _plan_name(pkg, w, flags):
+    p = pkg.nvfp4_gemv_plan(w.M, w.K, w.L).as_dict()
+    p["flags"] = flags
+    return KERNEL_NAMES.get(p["kernel"], "?"), p
+
+
+def time_per_config(pkg, device, stream, steps, warmup, dist, names=("c1", "c2", "c3", "c4", "c5"),
+                    steady_calls=GRAPH_CHUNK):
+    """Every decode workload in the same run.  For each: us per call over `steps` calls (the
+    headline's method: early weights, inputs rotated over copies larger than 3x L2), the same
+    calls in steady state (graphs of `steady_calls` calls, so the first call's start and the last
+    call's drain weigh 1 / steady_calls), and strict stream order (no early weights) over `steps`
+    calls.  c1 (18.8 KB) is launch-bound and is listed for completeness."""
+    import torch
+
+    peak, _ = measured_peak_gbs()
+    out = {}
+    for name in names:
+        w = workloads.make(name)
+        nbytes = w.algorithmic_bytes
+        n_copies, _ = _copies_for(nbytes, device)
+        sets = _device_inputs(w, n_copies, device)
+        outs = [torch.empty((w.L, w.M), dtype=torch.float16, device=device)
+                for _ in range(n_copies)]
+        row = {"M": w.M, "K": w.K, "L": w.L, "bytes_per_call": nbytes, "copies": n_copies}
+        kname, plan = _plan_name(pkg, w, FLAG_EARLY_WEIGHTS)
+        row["kernel"], row["plan"] = kname, plan
+        for key, flags, n in (("early_weights", FLAG_EARLY_WEIGHTS, steps),
+                              ("steady", FLAG_EARLY_WEIGHTS, max(steps, steady_calls)),
+                              ("strict_order", 0, steps)):
+            t = GraphTimer(_gemv_caller(pkg, w, sets, outs, {"flags": flags}, stream), n, warmup,
+                           stream)
+            sec = t.time(dist, device)
+            tot, slow = aggregate(dist, nbytes * n, sec)
+            gbs = tot / slow / 1e9
+            row[key] = {"us_per_call": round(sec / n * 1e6, 3), "calls": n,
+                        "GB/s": round(gbs, 2), "frac": round(gbs / peak, 4)}
+            del t
+        assert not torch.isnan(outs[0]).any().item()
+        out[name] = row
+        del sets, outs
+        torch.cuda.empty_cache()
+    out["note"] = ("early_weights: the headline's method over the K timed steps; steady: graphs "
+                   f"of {steady_calls} calls; strict_order: no early weights, K steps; frac of "
+                   "the measured HBM copy bandwidth")
+    return out
+
+
+def time_small_ml(pkg, device, stream, steps, warmup, dist,
+                  shapes=((16, 16384), (64, 16384), (128, 16384), (512, 16384),
+                          (16, 65536), (64, 65536), (128, 65536), (512, 65536))):
+    """Few output rows with long K (L = 1): the regime where one row per CTA cannot fill the GPU
+    and K is split across CTAs.  Each call reads its own copy of A and sfa (a pool of XOR-keyed
+    copies larger than 3x L2); the vector is shared.  Graphs of up to 1000 calls."""
+    import torch
+
+    peak, _ = measured_peak_gbs()
+    out = {}
+    for M, K in shapes:
+        w = workloads.random_workload(M, K, 1, seed=40 + M + K // 1024,
+                                      scale_bytes=workloads.pow2_scale_bytes(-3, 2), g_a=0.5)
+        nbytes = w.algorithmic_bytes
+        n_copies, _ = _copies_for(M * K * 9 // 16, device)
+        A0 = torch.from_numpy(w.A.ravel()).to(device)
+        S0 = torch.from_numpy(w.sfa.ravel()).to(device)
+        A = torch.empty((n_copies, A0.numel()), dtype=torch.uint8, device=device)
+        S = torch.empty((n_copies, S0.numel()), dtype=torch.uint8, device=device)
+        for q in range(n_copies):
+            torch.bitwise_xor(A0, (29 * q + 3) & 0xFF, out=A[q])
+            S[q].copy_(S0)
+        b = torch.from_numpy(w.b).to(device)
+        sfb = torch.from_numpy(w.sfb).to(device)
+        c = torch.empty((n_copies, M), dtype=torch.float16, device=device)
+        plan = {"flags": FLAG_EARLY_WEIGHTS}
+
+        def fn(i, A=A, S=S, b=b, sfb=sfb, c=c, n=n_copies, M=M, K=K):
+            pkg.nvfp4_gemv_batched_ex(A[i % n], S[i % n], 0.5, b, sfb, 1.0, c[i % n], M, K, 1,
+                                      stream=stream, plan=plan)
+        n_calls = min(steps, 5000)
+        sec, calls = _graph_time(fn, stream, n_calls, warmup, dist, device)
+        tot, slow = aggregate(dist, nbytes * calls, sec)
+        gbs = tot / slow / 1e9
+        kname, p = _plan_name(pkg, w, FLAG_EARLY_WEIGHTS)
+        out[f"M={M} K={K}"] = {"us_per_call": round(sec / calls * 1e6, 3), "calls": calls,
+                               "GB/s": round(gbs, 2), "frac": round(gbs / peak, 4),
+                               "bytes_per_call": nbytes, "kernel": kname, "plan": p}
+        del A, S, c
+        torch.cuda.empty_cache()
+    return out
 def time_bf16_vector(pkg, w, sets, outs, stream, steps, warmup, dist):
     """The GEMV with a bf16 activation vector through nvfp4_gemv_batched_bf16, in its two forms:
     the quantizer launched ahead of the GEMV (the default) and the quantization inside the
@@ -315,35 +514,11 @@ def time_bf16_vector(pkg, w, sets, outs, stream, steps, warmup, dist):
                                         so[i % n], outs[i % n], w.M, w.K, w.L, stream=stream,
                                         plan=plan)
 
-        with torch.cuda.stream(stream):
-            for i in range(max(warmup, 1)):
-                fn(i)
-        stream.synchronize()
-        chunk = min(GRAPH_CHUNK, steps)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(chunk):
-                fn(i)
-        reps = max(1, steps // chunk)
-        ev0 = torch.cuda.Event(enable_timing=True)
-        ev1 = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            barrier(dist)
-            torch.cuda.synchronize(dev)
-            ev0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            ev1.record(stream)
-            torch.cuda.synchronize(dev)
-            barrier(dist)
-        sec = ev0.elapsed_time(ev1) / 1e3
-        calls = reps * chunk
+        sec, calls = _graph_time(fn, stream, steps, warmup, dist, dev)
         tot, slow = aggregate(dist, bytes_call * calls, sec)
         out[name] = {"us_per_call": round(sec / calls * 1e6, 3), "calls": calls,
                      "GB/s": round(tot / slow / 1e9, 2),
                      "launches_per_call": 1 if flags & FLAG_QUANTIZE_IN_GEMV else 2}
-        del g
     out["bytes_per_call"] = bytes_call
     out["bytes"] = "A + sfa + bf16 x read + packed x and its scales written + c"
     out["gemv_kernel"] = KERNEL_NAMES.get(pkg.nvfp4_gemv_plan(w.M, w.K, w.L).kernel, "?")
@@ -376,36 +551,12 @@ def time_grouped(pkg, device, stream, steps, warmup, dist, name="g1", n_routes=4
                                expert_offsets=r["offs"], stream=stream)
 
     torch.cuda.synchronize(device)
-    with torch.cuda.stream(stream):
-        for i in range(max(warmup, 1)):
-            call(i)
-    stream.synchronize()
-    chunk = min(GRAPH_CHUNK, steps)
-    chunk -= chunk % n_routes
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(chunk):
-            call(i)
-    reps = max(1, steps // chunk)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g.replay()
-        barrier(dist)
-        torch.cuda.synchronize(device)
-        ev0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        ev1.record(stream)
-        torch.cuda.synchronize(device)
-        barrier(dist)
-    sec = ev0.elapsed_time(ev1) / 1e3
-    calls = reps * chunk
+    calls = max(n_routes, steps - steps % n_routes)      # every routing equally often
+    sec, calls = _graph_time(call, stream, calls, warmup, dist, device)
     bytes_call = sum(w.algorithmic_bytes for w in ws) / n_routes
     tot, slow = aggregate(dist, bytes_call * calls, sec)
     peak, peak_kind = measured_peak_gbs()
     gbs = tot / slow / 1e9
-    del g
     return {
         "workload": f"grouped decode GEMV {name}: E={E} experts of M={M} K={K}, "
                     f"{workloads.GROUPED[name]['tokens']} tokens x top-"
@@ -458,37 +609,6 @@ def time_general(pkg, w, stream, steps, warmup, dist, n_copies):
                      "us_per_call": round(sec / calls * 1e6, 3), "calls": calls,
                      "GB/s": round(tot / slow / 1e9, 2), "frac": round(tot / slow / 1e9 / peak, 4)}
     return out
-
-
-def _graph_time(fn, stream, steps, warmup, dist, dev):
-    """Seconds and calls for `steps` calls of fn(i) replayed from CUDA graphs on `stream`."""
-    import torch
-
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        for i in range(max(warmup, 1)):
-            fn(i)
-    stream.synchronize()
-    chunk = min(GRAPH_CHUNK, steps)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for i in range(chunk):
-            fn(i)
-    reps = max(1, steps // chunk)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g.replay()
-        barrier(dist)
-        torch.cuda.synchronize(dev)
-        ev0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(dist)
-    del g
-    return ev0.elapsed_time(ev1) / 1e3, reps * chunk
 
 
 def time_large(pkg, device, stream, steps, warmup, dist, M=7168, K=16384, L=80):
@@ -627,13 +747,15 @@ def run_ours(args):
 
     world, rank, local = dist_env()
     dist = dist_init(world)
+    if torch.cuda.device_count() <= local:
+        raise SystemExit(f"rank {rank}: needs GPU {local}, this host has "
+                         f"{torch.cuda.device_count()}")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     pkg.load_library()
     w = workloads.make(args.config)
     bytes_call = w.algorithmic_bytes
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    n_copies = max(2, -(-3 * l2 // bytes_call) + 1)
+    n_copies, l2 = _copies_for(bytes_call, device)
     sets = _device_inputs(w, n_copies, device)
     outs = [torch.empty((w.L, w.M), dtype=torch.float16, device=device) for _ in range(n_copies)]
     # Static weights: the same A and sfa are read by every call and written by none, so the calls
@@ -641,28 +763,16 @@ def run_ours(args):
     # call drains.  The strict-order number (no flag) is reported beside it.
     plan = json.loads(args.plan) if args.plan else {"flags": FLAG_EARLY_WEIGHTS}
     stream = torch.cuda.Stream(device)
-    g_full, g_rem, chunk, rem = time_device(pkg, w, sets, outs, plan, args.steps, args.warmup,
-                                            stream)
+    timer = GraphTimer(_gemv_caller(pkg, w, sets, outs, plan, stream), args.steps, args.warmup,
+                       stream)
     used_plan = pkg.nvfp4_gemv_plan(w.M, w.K, w.L).as_dict()
     used_plan.update({k: v for k, v in plan.items() if v})
     uuid = str(torch.cuda.get_device_properties(device).uuid)
     gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
 
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    # the dominant kernel's launches on the launching stream: one per step
     sampler = ClockSampler(gpu_id)
-    with sampler, torch.cuda.stream(stream):        # graphs replay on the current stream
-        barrier(dist)
-        torch.cuda.synchronize(device)
-        ev0.record(stream)
-        for _ in range(args.steps // chunk):
-            g_full.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        ev1.record(stream)
-        torch.cuda.synchronize(device)
-        barrier(dist)
-    seconds = ev0.elapsed_time(ev1) / 1e3
+    seconds = timer.time(dist, device, sampler)
     clocks = sampler.summary()
 
     total_bytes, slowest = aggregate(dist, bytes_call * args.steps, seconds)
@@ -674,43 +784,31 @@ def run_ours(args):
 
     # correctness spot check of the timed launches' last output (NaN would mean an unwritten c)
     assert not torch.isnan(outs[(args.steps - 1) % n_copies]).any().item()
-
-    # spread: after the timed region, 20 more replays of the same graph, each between two events
-    n_rep = 20
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
-    with torch.cuda.stream(stream):
-        evs[0].record(stream)
-        for i in range(n_rep):
-            g_full.replay()
-            evs[i + 1].record(stream)
-        torch.cuda.synchronize(device)
-    per = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 / chunk for i in range(n_rep))
-    spread = {"replays": n_rep, "calls_per_replay": chunk,
-              "p10_us": round(per[n_rep // 10], 3), "median_us": round(per[n_rep // 2], 3),
-              "p90_us": round(per[(9 * n_rep) // 10], 3)}
+    spread = timer.spread(device)
+    chunk = timer.chunk
+    del timer
 
     strict = None
     if not args.plan and not args.no_strict:
         steps_s = min(args.steps, 20000)
-        gs_full, gs_rem, chunk_s, _ = time_device(pkg, w, sets, outs, {"flags": 0}, steps_s,
-                                                  args.warmup, stream)
-        with torch.cuda.stream(stream):
-            barrier(dist)
-            torch.cuda.synchronize(device)
-            ev0.record(stream)
-            for _ in range(steps_s // chunk_s):
-                gs_full.replay()
-            if gs_rem is not None:
-                gs_rem.replay()
-            ev1.record(stream)
-            torch.cuda.synchronize(device)
-            barrier(dist)
-        sec_s = ev0.elapsed_time(ev1) / 1e3
+        t = GraphTimer(_gemv_caller(pkg, w, sets, outs, {"flags": 0}, stream), steps_s,
+                       args.warmup, stream)
+        sec_s = t.time(dist, device)
+        del t
         tot_s, slow_s = aggregate(dist, bytes_call * steps_s, sec_s)
         strict = {"value": round(tot_s / slow_s / 1e9, 2), "unit": "GB/s",
                   "us_per_call": round(sec_s / steps_s * 1e6, 3), "steps": steps_s,
+                  "frac": round(tot_s / slow_s / 1e9 / peak, 4),
                   "flags": "none (every thread waits for the preceding call before any read)"}
-        del gs_full, gs_rem
+
+    per_config = None
+    if not args.plan and not args.no_per_config:
+        per_config = time_per_config(pkg, device, stream, min(args.steps, 20000), args.warmup,
+                                     dist)
+
+    small_ml = None
+    if not args.plan and not args.no_small_ml:
+        small_ml = time_small_ml(pkg, device, stream, min(args.steps, 5000), args.warmup, dist)
 
     bf16 = None
     if not args.plan and not args.no_bf16:
@@ -745,7 +843,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, args.cpu_seconds, args.config)
+        cpu = cpu_baseline(w, args.cpu_seconds)
 
     if rank == 0:
         line = {
@@ -771,7 +869,7 @@ def run_ours(args):
                 "l2": f"inputs rotated over {n_copies} copies "
                       f"({n_copies * bytes_call / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
                 "plan": used_plan,
-                "launch": f"CUDA graphs of {chunk} calls",
+                "launch": f"CUDA graphs of {chunk} calls after a spin-kernel pre-roll",
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             },
             "roofline": {
@@ -787,24 +885,13 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clocks,
         }
-        if strict is not None:
-            line["strict_order"] = strict
-        if bf16 is not None:
-            line["bf16_vector"] = bf16
-        if grouped is not None:
-            line["grouped"] = grouped
-        if general is not None:
-            line["general_unaligned"] = general
-        if large is not None:
-            line["large_batch"] = large
-        if tc_n1 is not None:
-            line["tensor_cores_n1"] = tc_n1
-        if small is not None:
-            line["small_n"] = small
-        if e2e is not None:
-            line["e2e"] = e2e
-        if cpu is not None:
-            line["cpu_baseline"] = cpu
+        for key, val in (("strict_order", strict), ("per_config", per_config),
+                         ("small_ml", small_ml), ("bf16_vector", bf16), ("grouped", grouped),
+                         ("general_unaligned", general), ("large_batch", large),
+                         ("tensor_cores_n1", tc_n1), ("small_n", small), ("e2e", e2e),
+                         ("cpu_baseline", cpu)):
+            if val is not None:
+                line[key] = val
         print(json.dumps(line), flush=True)
     barrier(dist)
 
@@ -880,123 +967,105 @@ def time_e2e(pkg, w, plan, device, stream, steps, dist, copy_streams=1):
 
 # ---------------------------------------------------------------------------- the oracle on the CPU
 
-def _oracle_rows(w, rows):
-    import oracle
-
-    ls, ms = np.divmod(np.asarray(rows, dtype=np.int64), w.M)
-    oracle.gemv_rows(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, w.M, w.K, w.L, ls, ms)
-
-
 def _row_bytes(w, n_rows):
     """Algorithmic bytes of n_rows outputs (their share of the vector bytes included)."""
     return w.algorithmic_bytes * n_rows / (w.M * w.L)
 
 
-_POOL_W = None
+def _oracle_rows(w, start, n, threads):
+    """The C oracle (fp64) on output rows start .. start+n-1 of the workload (wrapping around)."""
+    from oracle import cref
+
+    idx = (start + np.arange(n, dtype=np.int64)) % (w.M * w.L)
+    ls, ms = np.divmod(idx, w.M)
+    cref.gemv_rows(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, w.M, w.K, w.L, ls, ms, threads=threads)
 
 
-def _pool_init(name):
-    global _POOL_W
-    _POOL_W = workloads.make(name)
+def _host_cpus():
+    cpus = os.cpu_count() or 1
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return cpus, model
 
 
-def _pool_rows(span):
-    lo, hi = span
-    _oracle_rows(_POOL_W, range(lo, hi))
-    return hi - lo
-
-
-def cpu_baseline(w, seconds: float, name: str):
-    """The oracle as it stands (numpy, fp64) timed on this host: on one thread over consecutive
-    output rows for about a third of `seconds`, then on every host core (spawned worker processes,
-    each computing whole rows) for the rest, on a bounded sample of the workload."""
-    total = w.M * w.L
-    chunk = max(1, (1 << 22) // w.K)
+def _timed_rows(w, seconds, threads, chunk):
+    """Rows computed by the C oracle in about `seconds` of wall time, and that time."""
     done = 0
     t0 = time.perf_counter()
-    while done < total and time.perf_counter() - t0 < seconds / 3:
-        n = min(chunk, total - done)
-        _oracle_rows(w, range(done, done + n))
-        done += n
-    elapsed = time.perf_counter() - t0
-    single = {"value": round(_row_bytes(w, done) / elapsed / 1e9, 4), "cores": 1,
-              "sample": f"{done} of {total} output rows, {elapsed:.1f} s"}
-    cores = os.cpu_count() or 1
-    try:
-        import multiprocessing as mp
+    while True:
+        _oracle_rows(w, done, chunk, threads)
+        done += chunk
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done, el
 
-        rate = done / elapsed                          # rows per second on one core
-        rows = int(min(total, max(cores * chunk, rate * cores * seconds * 2 / 3)))
-        spans = [(lo, min(rows, lo + chunk)) for lo in range(0, rows, chunk)]
-        with mp.get_context("spawn").Pool(cores, initializer=_pool_init, initargs=(name,)) as pool:
-            pool.map(_pool_rows, [(0, 1)] * cores)     # every worker has built its inputs
-            t0 = time.perf_counter()
-            got = sum(pool.map(_pool_rows, spans, chunksize=1))
-            el = time.perf_counter() - t0
-        return {"value": round(_row_bytes(w, got) / el / 1e9, 4), "unit": "GB/s", "cores": cores,
-                "kind": "oracle",
-                "sample": f"{got} of {total} output rows ({100.0 * got / total:.1f}% of the "
-                          f"workload) in {el:.1f} s, numpy fp64, {cores} worker processes",
-                "single_thread": single}
-    except Exception as ex:  # no process pool on this host: the single-thread figure stands
-        return {"value": single["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
-                "sample": f"{single['sample']}, numpy fp64, single thread "
-                          f"(worker pool unavailable: {type(ex).__name__})"}
+
+def cpu_baseline(w, seconds: float):
+    """The oracle as it stands (plain C, fp64, built with gcc -O2) timed on this host: one thread
+    over consecutive output rows for a third of `seconds`, then an OpenMP parallel for over output
+    rows on every host thread for the rest; both wrap around the workload, a bounded sample of
+    about `seconds` of CPU time."""
+    from oracle import cref
+
+    total = w.M * w.L
+    chunk1 = max(1, (1 << 21) // w.K)
+    rows1, el1 = _timed_rows(w, seconds / 3, 1, chunk1)
+    single = {"value": round(_row_bytes(w, rows1) / el1 / 1e9, 4), "cores": 1,
+              "sample": f"{rows1} output rows ({rows1 / total:.2f} x the workload) in {el1:.1f} s"}
+    threads = cref.max_threads()
+    cpus, model = _host_cpus()
+    rows, el = _timed_rows(w, seconds * 2 / 3, threads, max(threads * 8, (1 << 24) // w.K))
+    return {"value": round(_row_bytes(w, rows) / el / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{rows} output rows ({rows / total:.2f} x the workload, wrapping) in "
+                      f"{el:.1f} s, plain C fp64 oracle, OpenMP parallel for over rows on "
+                      f"{threads} threads",
+            "host_cpus": cpus, "host_cpu_model": model, "single_thread": single}
 
 
 def run_reference(args):
-    """The oracle as it stands, timed on every host core (spawned worker processes, whole output
-    rows each), each step a bounded sample of the workload sized so that the run fits
-    --reference-seconds.  Falls back to one thread if no worker pool can be started."""
+    """The oracle as it stands (plain C, fp64, OpenMP over output rows on every host thread), each
+    step a bounded sample of consecutive output rows of the workload, sized so that the whole
+    run fits --reference-seconds.  Under several ranks rank 0 alone runs it."""
+    from oracle import cref
+
     world, rank, _ = dist_env()
     if rank != 0:
         return
     w = workloads.make(args.config)
     total = w.M * w.L
+    threads = cref.max_threads()
     per_step_budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    probe = max(threads, 64)
     t0 = time.perf_counter()
-    _oracle_rows(w, range(0, 1))
-    t_row = max(time.perf_counter() - t0, 1e-4)
-    cores = os.cpu_count() or 1
-    pool = None
-    try:
-        import multiprocessing as mp
-
-        pool = mp.get_context("spawn").Pool(cores, initializer=_pool_init, initargs=(args.config,))
-        pool.map(_pool_rows, [(0, 1)] * cores)
-    except Exception:
-        pool, cores = None, 1
-    rows = int(max(cores, min(total, cores * per_step_budget / t_row)))
-    chunk = max(1, -(-rows // cores))
-
-    def one_step(i):
-        s0 = (i * rows) % (total - rows + 1)
-        if pool is None:
-            _oracle_rows(w, range(s0, s0 + rows))
-        else:
-            pool.map(_pool_rows, [(lo, min(s0 + rows, lo + chunk))
-                                  for lo in range(s0, s0 + rows, chunk)], chunksize=1)
-
+    _oracle_rows(w, 0, probe, threads)
+    t_row = max((time.perf_counter() - t0) / probe, 1e-7)
+    rows = int(max(threads, min(4 * total, per_step_budget / t_row)))
     for i in range(args.warmup):
-        one_step(i)
+        _oracle_rows(w, i * rows, rows, threads)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        one_step(args.warmup + i)
+        _oracle_rows(w, (args.warmup + i) * rows, rows, threads)
     elapsed = time.perf_counter() - t0
-    if pool is not None:
-        pool.close()
-        pool.join()
     value = _row_bytes(w, rows) * args.steps / elapsed / 1e9
-    sample = (f"{rows} consecutive output rows per step of the M={w.M} K={w.K} L={w.L} workload, "
-              f"numpy fp64 oracle, {cores} worker process{'es' if cores > 1 else ''}")
+    cpus, model = _host_cpus()
+    sample = (f"{rows} consecutive output rows per step (wrapping) of the M={w.M} K={w.K} L={w.L} "
+              f"workload, plain C fp64 oracle, OpenMP parallel for over rows on {threads} threads")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"NVFP4 decode GEMV M={w.M} K={w.K} L={w.L} ({args.config})",
                        "M": w.M, "K": w.K, "L": w.L},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
-                             "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample, "host_cpus": cpus,
+                             "host_cpu_model": model},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -1014,6 +1083,10 @@ def main():
     ap.add_argument("--no-strict", action="store_true",
                     help="skip the second timing without the early-weights flag")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the timings of all five decode workloads")
+    ap.add_argument("--no-small-ml", action="store_true",
+                    help="skip the few-rows / long-K (split-K) timings")
     ap.add_argument("--no-bf16", action="store_true",
                     help="skip the bf16-vector (activation quantization) timing")
     ap.add_argument("--no-grouped", action="store_true",
@@ -1032,6 +1105,13 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.steps < 1:
         ap.error("--steps must be at least 1")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    world_env = os.environ.get("WORLD_SIZE")
+    if world_env is not None and int(world_env) != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world_env}: launch one rank per GPU")
+    if world_env is None and args.gpus > 1:
+        sys.exit(spawn_ranks(args.gpus, sys.argv[1:]))
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -87,10 +87,60 @@ def test_code_only_digest_ignores_comments_not_code():
     assert '"a // b"' in bench._code_only(a)
 
 
-def test_cpu_baseline_uses_every_core():
+def test_cpu_baseline_times_the_c_oracle_on_every_thread():
     import bench
     import workloads
+    from oracle import cref
 
-    r = bench.cpu_baseline(workloads.make("c1"), 1.0, "c1")
-    assert r["kind"] == "oracle" and r["value"] > 0 and r["cores"] >= 1
-    assert r["single_thread"]["cores"] == 1
+    r = bench.cpu_baseline(workloads.make("c1"), 1.0)
+    assert r["kind"] == "oracle" and r["value"] > 0 and r["cores"] == cref.max_threads()
+    assert r["single_thread"]["cores"] == 1 and r["single_thread"]["value"] > 0
+    assert "plain C" in r["sample"] and r["host_cpus"] == (os.cpu_count() or 1)
+
+
+def test_gpus_flag_starts_the_ranks_itself():
+    """--gpus 2 without torchrun: bench.py starts two ranks (gloo on the CPU for the host-side
+    exchange); under several ranks the reference arm runs on rank 0 alone, which prints the one
+    line with n_gpus 2."""
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--gpus", "2", "--config", "c1", "--steps", "3", "--warmup", "3",
+                          "--reference-seconds", "2"], capture_output=True, text=True,
+                         timeout=300, cwd=ROOT, env=env)
+    assert out.returncode == 0, out.stderr
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_gpus_flag_must_match_world_size():
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--gpus", "3", "--config", "c1", "--steps", "3", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT, env=env)
+    assert out.returncode != 0 and "WORLD_SIZE" in out.stderr
+
+
+def test_spawned_ranks_aggregate_over_gloo(tmp_path):
+    """The ranks bench.py starts for --gpus N join one gloo group: a two-rank job through
+    spawn_ranks whose ranks report sum-over-max exactly as the GPU arm does."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    script = tmp_path / "rank.py"
+    script.write_text(
+        "import os, sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "import bench\n"
+        "world, rank, _ = bench.dist_env()\n"
+        "dist = bench.dist_init(world)\n"
+        "total, slowest = bench.aggregate(dist, (rank + 1) * 1e9, (rank + 1) * 0.5)\n"
+        "assert world == 2 and total == 3e9 and slowest == 1.0, (world, total, slowest)\n"
+        "dist.destroy_process_group()\n")
+    old = bench.__file__
+    try:
+        bench.__file__ = str(script)
+        assert bench.spawn_ranks(2, []) == 0
+    finally:
+        bench.__file__ = old
