@@ -182,7 +182,7 @@ def test_overflowing_block_gives_nan_on_both_sides(pkg, flags):
     ref, T = oracle.gemv(w.A, w.sfa, w.g_a, pr, sr, gs, M, K, L)
     assert np.isnan(ref[1]).all() and not np.isnan(ref[0]).any()
     A, sfa = torch.from_numpy(w.A).cuda(), torch.from_numpy(w.sfa).cuda()
-    c, b, s = gemv_bf16(pkg, A, sfa, w.g_a, x, gs, 0, M, {"flags": flags})
+    c, b, s = gemv_bf16(pkg, A, sfa, w.g_a, x, gs, 0, M, {"kernel": 4, "flags": flags})
     assert_bytes_equal(s, sr, "sfb_out with an overflowing block")
     assert_bytes_equal(b, pr, "b_out with an overflowing block")
     assert np.isnan(c[1]).all()
