@@ -54,7 +54,8 @@ class Plan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("rows_per_warp", ctypes.c_int32),
                 ("k_split", ctypes.c_int32), ("ctas_per_batch", ctypes.c_int32),
                 ("warps_per_cta", ctypes.c_int32), ("tile_rows", ctypes.c_int32),
-                ("stages", ctypes.c_int32), ("flags", ctypes.c_int32)]
+                ("stages", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("k_slices", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}

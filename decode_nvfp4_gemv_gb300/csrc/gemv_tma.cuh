@@ -34,6 +34,17 @@
 //                          segments in every tile, so it decodes its slice of b into registers once.
 //                          No vector reads in the inner loop, and the ring gets the shared memory.
 //
+// Split K over a cluster (register-vector kernel, `CL`).  When the rows of a call are too few to
+// give every CTA slot of one wave enough work, K is cut into S slices of whole 1024-element
+// segments and a thread-block cluster of S CTAs shares each row range: cluster CTA z streams
+// slice z of its rows (one bulk copy per row and operand, since a slice of consecutive rows is not
+// contiguous), holds slice z of the vector in registers and sums its rows' partials over its own
+// warps as above.  Each row is owned by one CTA of the cluster (rows [o n / S, (o+1) n / S) by
+// CTA o); every CTA stores its partial of a row into the owner's shared memory (distributed shared
+// memory), and after one cluster barrier the owner adds the S partials in slice order and stores
+// the row.  Deterministic, and no global workspace: the second pass of the reduction never leaves
+// the cluster.
+//
 // Programmatic dependent launch.  The host launches with programmatic stream serialization, so the
 // next kernel in the stream may be scheduled while this one drains.  Every thread executes
 // griddepcontrol.wait before its first access to memory a preceding kernel may write; with the
@@ -58,6 +69,7 @@ namespace nvfp4 {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second
 constexpr int kTmaMaxStages = 8;
+constexpr int kTmaMaxClusterK = 8;                // K slices (cluster CTAs) of a split-K launch
 constexpr uint32_t kTmaHeaderBytes = 256;         // barriers (16 B per stage) + abort flag
 
 struct TmaArgs {
@@ -93,6 +105,14 @@ struct TmaArgs {
   // and the ends of the b and sfb buffers (unused when aligned)
   const uint8_t *A_lo, *A_hi, *S_lo, *S_hi, *b_end, *sfb_end;
   int32_t test_stall;    // tests of the failure path: the producer issues nothing
+  // split K over a cluster (CL): S slices of slice_segs 1024-element segments each (the last
+  // slice may end short of that at K); a stage holds a tile's rows rs_a (A) and rs_s (sfa) bytes
+  // apart (K/2 and K/16 when unsplit); red_off: the owner's S x red_rows partial sums
+  int32_t k_slices;
+  int32_t slice_segs;
+  uint32_t rs_a, rs_s;
+  uint32_t red_off;
+  int32_t red_rows;
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -230,7 +250,22 @@ struct TmaCta {
   int64_t ea;     // the matrix of A this CTA streams: l, or the expert of token l
   float ga, gb;   // global scales
   bool skip;      // grouped form: token l has no expert, its outputs are zeros
+  int z;          // split K: this CTA's slice (its rank in the cluster); 0 unsplit
+  int64_t k0;     // first element of the slice
+  int kz;         // elements in the slice (K unsplit)
 };
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
 
 __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
                                             volatile int* abort_flag) {
@@ -238,8 +273,13 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
   // The batch and the CTA's rows, in 32-bit arithmetic and without a 64-bit division: this runs
   // before the CTA's first copy.  Measured on GB300 against floor(M pi / P) in 64-bit arithmetic:
   // c2 11.58 -> 11.42 us, c3 -0.6%, c4 and c5 unchanged (32-bit floor(M pi / P) alone: 11.50 us).
-  const uint32_t bid = blockIdx.x, P = (uint32_t)p.P;
+  // split K: a cluster of S CTAs shares one row range, CTA z taking slice z (a launch without
+  // clusters is one-CTA clusters: rank 0, cluster index = CTA index)
+  const uint32_t bid = p.k_slices > 1 ? cluster_id_x() : blockIdx.x, P = (uint32_t)p.P;
   const uint32_t l = bid / P, pi = bid - l * P;
+  g.z = p.k_slices > 1 ? (int)cluster_ctarank() : 0;
+  g.k0 = (int64_t)g.z * p.slice_segs * kStep;
+  g.kz = p.k_slices > 1 ? (int)min(p.K - g.k0, (int64_t)p.slice_segs * kStep) : (int)p.K;
   const uint32_t q = (uint32_t)p.rows_q, r = (uint32_t)p.rows_r;
   g.l = l;
   g.pi = pi;
@@ -269,7 +309,9 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
 __device__ __forceinline__ void tma_resolve_group(const TmaArgs& p, TmaCta& g, int lane) {
   if (p.G.E <= 0) return;
   const int e = group_of_batch(p.G, g.l, lane);
-  g.skip = e < 0;
+  // one verdict for the whole CTA (called by every thread), so no warp can be left waiting at a
+  // barrier for warps that skipped, even if the routing changed under a misbehaving writer
+  g.skip = __syncthreads_or(e < 0) != 0;
   if (g.skip) {
     for (int t = threadIdx.x; t < g.n; t += blockDim.x) p.c[g.l * p.M + g.m0 + t] = 0;
     return;
@@ -342,8 +384,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 
 // The producer lane: streams the CTA's row tiles into the ring.  UA: operands not 16-byte aligned
 // (stage_unaligned above); the stage then holds each tile's bytes from the 16-byte boundary at or
-// below its first byte.
-template <bool UA>
+// below its first byte.  CL: split K, one copy per row of the slice's bytes (A, then sfa).
+template <bool UA, bool CL = false>
 __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, uint64_t* bars,
                                             volatile int* abort_flag, uint8_t* ring) {
   const int64_t K2 = p.K >> 1, K16 = p.K >> 4;
@@ -375,7 +417,27 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
     const uint32_t bytesA = (uint32_t)(rows_t * K2), bytesS = (uint32_t)(rows_t * K16);
     const uint32_t full = smem_addr(&bars[s]);
     uint8_t* st = ring + (size_t)s * p.stage_bytes;
-    if constexpr (UA) {
+    if constexpr (CL) {
+      // the slice [k0, k0 + kz) of each row: kz / 2 bytes of A at K/2-byte row steps, kz / 16 of
+      // sfa at K/16 (every address and size a multiple of 16: K % 256 == 0 and whole segments).
+      // Early weights: the last row's A copy of the last tile requested before the wait follows
+      // the wait, as the unsplit tail does.
+      const uint32_t ra = (uint32_t)(g.kz >> 1), rs = (uint32_t)(g.kz >> 4);
+      const uint8_t* ga = A_c + (int64_t)T * TR * K2 + (g.k0 >> 1);
+      const uint8_t* gs = S_c + (int64_t)T * TR * K16 + (g.k0 >> 4);
+      const bool hold = p.early_weights && T == NS - 2;
+      mbar_arrive_expect_tx(full, (uint32_t)rows_t * (ra + rs));
+      for (int r = 0; r < rows_t; ++r) {
+        bulk_copy_g2s(smem_addr(st + p.sfa_off + r * p.rs_s), gs + (int64_t)r * K16, rs, full, pol);
+        if (!(hold && r == rows_t - 1))
+          bulk_copy_g2s(smem_addr(st + r * p.rs_a), ga + (int64_t)r * K2, ra, full, pol);
+      }
+      if (hold) {
+        pdl_wait();
+        bulk_copy_g2s(smem_addr(st + (rows_t - 1) * p.rs_a), ga + (int64_t)(rows_t - 1) * K2, ra,
+                      full, pol);
+      }
+    } else if constexpr (UA) {
       // the copies' bytes are expected first; the arrival comes after the edge stores, so the
       // consumers that see the phase complete see those bytes too
       const uint8_t* ga = A_c + (int64_t)T * TR * K2;
@@ -558,12 +620,56 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
   tma_epilogue(p, g, part, abort_flag);
 }
 
+// Cluster barrier over every thread of every CTA of the cluster: the release orders this thread's
+// distributed-shared-memory stores before the barrier, the acquire makes the other CTAs' stores
+// visible after it.  Every thread of the cluster reaches it once, after bounded work, so it ends.
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+
+// Stores one float into the shared memory of cluster CTA `rank` at the offset of local_addr.
+__device__ __forceinline__ void st_cluster_f32(uint32_t local_addr, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+// Split K: the second pass of the reduction, inside the cluster.  Every consumer thread sends this
+// CTA's partial of its rows (the sum over its slots, or NaN if the CTA gave up) to the row's owner
+// CTA; after the cluster barrier the owner adds the S partials in slice order and stores the row.
+__device__ __forceinline__ void tma_cluster_reduce(const TmaArgs& p, const TmaCta& g,
+                                                   const float* part, float* red,
+                                                   volatile int* abort_flag) {
+  const int S = p.k_slices, n = g.n, rr = p.red_rows, cthreads = 32 * g.Wc;
+  const bool failed = *abort_flag != 0;
+  const uint32_t red32 = smem_addr(red);
+  for (int t = threadIdx.x; t < n; t += cthreads) {  // rows n <= rows_cap: no divergence at exit
+    float v = 0.f;
+    for (int q = 0; q < p.slots; ++q) v += part[t * p.slots + q];
+    const int o = (t * S + S - 1) / n;       // rows [o n / S, (o+1) n / S) belong to CTA o
+    const int idx = t - (o * n) / S;
+    st_cluster_f32(red32 + 4u * (uint32_t)(g.z * rr + idx), (uint32_t)o,
+                   failed ? __int_as_float(0x7fc00000) : v);
+  }
+  __syncwarp();
+  cluster_barrier();
+  const int r0 = (g.z * n) / S, r1 = ((g.z + 1) * n) / S;
+  uint16_t* c_c = p.c + g.l * p.M + g.m0 + r0;
+  for (int t = threadIdx.x; t < r1 - r0; t += cthreads) {
+    float v = red[t];
+    for (int z = 1; z < S; ++z) v += red[z * rr + t];
+    c_c[t] = f32_to_out_bits((v * g.ga) * g.gb, p.out_bf16 != 0);
+  }
+}
+
 // ------------------------------------------------------------------------------------------------
 // Vector slice in registers (W_c divides the segment count, or the segment count divides W_c).
 // QX: the vector is bf16 and is quantized to NVFP4 here (see quantize.cuh); its bytes feed the same
-// decode as packed input would.
+// decode as packed input would.  CL: split K over a cluster (the CTA's segments are those of its
+// slice; rows of a stage lie rs_a / rs_s bytes apart).
 // ------------------------------------------------------------------------------------------------
-template <int NSW, bool QX, bool UA>
+template <int NSW, bool QX, bool UA, bool CL = false>
 __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel(const TmaArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -576,15 +682,22 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
   TmaCta g = tma_setup(p, bars, abort_flag);
   if (!p.early_weights) pdl_wait();
   tma_resolve_group(p, g, lane);
-  if (g.skip) return;
+  if (g.skip) {
+    if constexpr (CL) cluster_barrier();  // the one cluster barrier every CTA takes part in
+    return;
+  }
   if (warp == g.Wc) {
-    if (lane == 0) tma_produce<UA>(p, g, bars, abort_flag, ring);
+    if (lane == 0) tma_produce<UA, CL>(p, g, bars, abort_flag, ring);
+    if constexpr (CL) {  // the producer warp takes part in the cluster barrier of the reduction
+      __syncwarp();
+      cluster_barrier();
+    }
     return;
   }
   if (p.early_weights) pdl_wait();
 
   const int Wc = g.Wc, cthreads = 32 * Wc;
-  const int nseg = (int)((K + kStep - 1) / kStep);
+  const int nseg = CL ? p.slice_segs : (int)((K + kStep - 1) / kStep);
   const bool many = nseg >= Wc;                     // Wc | nseg: all row groups, NSW segments
   const int rg_first = many ? 0 : warp / nseg;      // nseg | Wc: one segment, every rg_step-th
   const int rg_step = many ? 1 : Wc / nseg;         //   row group
@@ -596,9 +709,10 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
 #pragma unroll
   for (int j = 0; j < NSW; ++j) {
     seg[j] = many ? warp + j * Wc : warp % nseg;
-    const int64_t k = (int64_t)seg[j] * kStep + 32 * lane;
-    live[j] = k < K;
-    const int64_t kk = live[j] ? k : 0;  // lanes past K read element 0 and never use it
+    const int64_t k = (int64_t)seg[j] * kStep + 32 * lane;  // inside the slice
+    live[j] = k < g.kz;
+    // lanes past the slice's end read its first element and never use it
+    const int64_t kk = g.k0 + (live[j] ? k : 0);
     uint4 v;
     uint16_t s2;
     if constexpr (QX) {
@@ -640,7 +754,7 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
   named_barrier(1, (uint32_t)cthreads);
 
   const uint32_t ring32 = smem_addr(ring);
-  const uint32_t K2u = (uint32_t)K2, K16u = (uint32_t)K16;
+  const uint32_t rsA = p.rs_a, rsS = p.rs_s;  // K/2 and K/16 unsplit
   uint32_t lane_a[NSW], lane_s[NSW];  // this lane's byte offsets inside a row, per segment
 #pragma unroll
   for (int j = 0; j < NSW; ++j) {
@@ -668,8 +782,8 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const uint32_t r = (uint32_t)min(4 * rg + i, rows_t - 1);  // re-read the last row
-        aoff[i] = stA + r * K2u;
-        soff[i] = stS + dS + r * K16u;
+        aoff[i] = stA + r * rsA;
+        soff[i] = stS + dS + r * rsS;
       }
       float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
@@ -698,7 +812,10 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
     tma_release(p, bars, rp, lane);
   }
   named_barrier(1, (uint32_t)cthreads);
-  tma_epilogue(p, g, part, abort_flag);
+  if constexpr (CL)
+    tma_cluster_reduce(p, g, part, reinterpret_cast<float*>(smem + p.red_off), abort_flag);
+  else
+    tma_epilogue(p, g, part, abort_flag);
 }
 
 }  // namespace nvfp4

@@ -90,6 +90,14 @@ void init_device(int dev) {
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, true, false>, d.max_smem_optin)) ||
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, false, true>, d.max_smem_optin)) ||
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false, true>, d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, false, false, true>,
+                              d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false, false, true>,
+                              d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, true, false, true>,
+                              d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, true, false, true>,
+                              d.max_smem_optin)) ||
       (e = cudaFuncSetAttribute(nvfp4::gemv_shift_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin)) ||
       (e = cudaFuncSetAttribute(nvfp4::gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -341,24 +349,81 @@ int plan_stream(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp
 // stages of TR rows (A rows, then sfa rows).  Every region starts 16-byte aligned, ring stages
 // 128-byte aligned.
 struct TmaLayout {
-  int64_t b_off, sb_off, part_off, ring_off, sfa_off, stage_bytes, total;
+  int64_t b_off, sb_off, part_off, red_off, red_rows, ring_off, sfa_off, stage_bytes, total;
+  int64_t rs_a, rs_s;  // bytes between the rows of a stage (A, sfa)
 };
 
 // ua: operands not 16-byte aligned; a stage then holds each tile's A and sfa bytes from the
 // 16-byte boundary at or below their first byte, plus the 16 bytes a lane's second aligned read
-// may reach past them: 32 bytes more for each.
+// may reach past them: 32 bytes more for each.  S > 1: K split over a cluster of S CTAs; a stage
+// holds one slice of each row (nseg / S segments), and the owner's partial sums of the cluster
+// (S x ceil(rows_cap / S) floats) follow the per-slot partials.
 TmaLayout tma_layout(bool rv, int64_t K, int64_t TR, int64_t NS, int64_t rows_cap, int64_t slots,
-                     bool ua = false) {
+                     bool ua = false, int64_t S = 1) {
   TmaLayout t;
+  const int64_t seg_s = S > 1 ? ceil_div(K, nvfp4::kStep) / S : 0;
+  t.rs_a = S > 1 ? seg_s * (nvfp4::kStep / 2) : K / 2;
+  t.rs_s = S > 1 ? seg_s * (nvfp4::kStep / 16) : K / 16;
   t.b_off = nvfp4::kTmaHeaderBytes;
   t.sb_off = t.b_off + (rv ? 0 : 2 * K);
   t.part_off = align_up(t.sb_off + (rv ? 0 : K / 4), 16);
-  t.ring_off = align_up(t.part_off + 4 * rows_cap * slots, 128);
+  t.red_off = align_up(t.part_off + 4 * rows_cap * slots, 16);
+  t.red_rows = S > 1 ? ceil_div(rows_cap, S) : 0;
+  t.ring_off = align_up(t.red_off + 4 * S * t.red_rows, 128);
   const int64_t slack = ua ? 32 : 0;
-  t.sfa_off = align_up(TR * (K / 2) + slack, 128);
-  t.stage_bytes = align_up(t.sfa_off + TR * (K / 16) + slack, 128);
+  t.sfa_off = align_up(TR * t.rs_a + slack, 128);
+  t.stage_bytes = align_up(t.sfa_off + TR * t.rs_s + slack, 128);
   t.total = t.ring_off + NS * t.stage_bytes;
   return t;
+}
+
+// Small calls: the register-vector ring on a grid sized by the bytes of the call, with K split
+// over a cluster only when a CTA would otherwise hold more than 32 segments.  Sweeps on GB300 of
+// K = 256 .. 65536 and M x L = 16 .. 2400 (us per call, early weights, graphs of 1000 calls):
+//   - the ring beats the stream kernel on every such shape, by 1.3-3x (512 x 16384: 2.31 us on
+//     152 CTAs against 5.5; 128 x 256 (18.8 KB): 1.95 against 2.82);
+//   - the best grid follows the bytes B of the call, not the rows: about 1.9 us + B / 2.5 TB/s
+//     on 76 CTAs, 2.1 us + B / 5.3 TB/s on 152 and 2.7 us + B / 7 TB/s on 304, so 76 CTAs below
+//     about 1.5 MB (2400 x 1024: 2.12 us, against 2.35 on 152 and 3.03 on 304), 152 up to about
+//     13 MB (2000 x 4096: 2.98; 400 x 7168: 1.75 against 2.29 on 76), 304 beyond (700 x 16384 x 3:
+//     5.19 against 6.50 on 152);
+//   - K = 32768 runs unsplit on at most 152 CTAs (1000 rows: 6.26 us, 8.05 on 304 CTAs, 6.60
+//     split in two); at K = 65536
+//     four slices of 16384 win (512 rows: 6.99 us on 57 x 4 CTAs, 7.32 with two slices);
+//   - clusters of 4 and 8 CTAs fit only about 3/4 of the 304 CTA slots at once (57 x 4 and
+//     28 x 8 run in one wave, 76 x 4 and 38 x 8 take twice as long), so split grids stop there.
+// The byte thresholds scale with the SM count (10 KB and 85 KB per SM).  Sets *S (1: unsplit) and
+// *P (CTAs per batch); *S = 0 when no split fits the segment count.
+constexpr int64_t kSmallCallBytesPerSm = 10 * 1024;
+constexpr int64_t kMidCallBytesPerSm = 85 * 1024;
+
+int64_t call_bytes(int64_t M, int64_t K, int64_t L) { return M * L * (K / 2 + K / 16); }
+
+bool small_call(const DeviceInfo& d, int64_t M, int64_t K, int64_t L) {
+  return call_bytes(M, K, L) < kMidCallBytesPerSm * d.sms;
+}
+
+void small_call_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, int64_t* S_out,
+                     int64_t* P_out) {
+  const int64_t nseg = ceil_div(K, nvfp4::kStep), slots = 2 * (int64_t)d.sms;
+  const int64_t B = call_bytes(M, K, L);
+  int64_t S = 1;
+  if (nseg > 32) {
+    S = 0;
+    for (int64_t s = 2; s <= nvfp4::kTmaMaxClusterK && !S; ++s)
+      if (nseg % s == 0 && nseg / s <= 16) S = s;
+  }
+  *S_out = S;
+  *P_out = 0;
+  if (!S) return;
+  int64_t G = B < kSmallCallBytesPerSm * d.sms ? slots / 4
+              : B < kMidCallBytesPerSm * d.sms ? slots / 2
+                                                : slots;  // CTAs of the launch
+  if (S > 1) G = std::min<int64_t>(G, slots * 3 / 4);
+  // more than 16 segments unsplit (K up to 32768): one CTA per SM (1000 x 32768: 6.26 us on 152
+  // CTAs, 8.05 on 304)
+  if (S == 1 && nseg > 16) G = std::min<int64_t>(G, slots / 2);
+  *P_out = std::min<int64_t>(M, std::max<int64_t>(1, G / (L * S)));
 }
 
 // Ring sizing, from sweeps on GB300 over the four large decode shapes: two stages of up to ~56 KiB
@@ -390,14 +455,25 @@ int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw, int64_t max_warps =
 }
 
 // ua: operands not 16-byte aligned (register-vector kernel only; stages carry 32 bytes of slack).
+// S: K slices over a cluster of S CTAs (register-vector kernel, aligned operands, S dividing the
+// 1024-element segment count, at most kTmaMaxClusterK).
 int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan& f, bool rv,
-             nvfp4_plan* pl, bool ua = false) {
+             nvfp4_plan* pl, bool ua = false, int64_t S = 1) {
   if (ua && !rv)
     return fail(NVFP4_ERR_MISALIGNED,
                 "the shared-memory-vector TMA kernel needs 16-byte aligned A, sfa, b and sfb");
   if (K % 256 != 0)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernels need K %% 256 == 0 (K=%lld)",
                 (long long)K);
+  if (S > 1) {
+    if (ua)
+      return fail(NVFP4_ERR_MISALIGNED, "split K over a cluster needs 16-byte aligned operands");
+    if (!rv || S > nvfp4::kTmaMaxClusterK || ceil_div(K, nvfp4::kStep) % S != 0)
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                  "split K: the register-vector kernel, k_slices <= %d dividing the %lld "
+                  "1024-element segments (k_slices=%lld)",
+                  nvfp4::kTmaMaxClusterK, (long long)ceil_div(K, nvfp4::kStep), (long long)S);
+  }
   if (f.warps_per_cta > 16)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "TMA kernels: at most 16 consumer warps");
   if (f.rows_per_warp && f.rows_per_warp != 4)
@@ -406,7 +482,7 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       f.stages > nvfp4::kTmaMaxStages)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tile_rows must be 1..256, stages 2..%d",
                 nvfp4::kTmaMaxStages);
-  const int64_t nseg = ceil_div(K, nvfp4::kStep);
+  const int64_t nseg = ceil_div(K, nvfp4::kStep) / S;  // segments of one CTA's slice
   int64_t Wc = f.warps_per_cta ? f.warps_per_cta : 8, nsw = 1;
   if (rv) {
     // the unaligned form needs more registers (about 88-96 a thread): at most 8 consumer warps
@@ -419,7 +495,8 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   }
   const int64_t slots = rv ? std::min(Wc, nseg) : Wc;
   const int64_t rg_step = (rv && nseg < Wc) ? Wc / nseg : 1;
-  const int64_t row_bytes = K / 2 + K / 16;
+  const TmaLayout one_row = tma_layout(rv, K, 1, 1, 1, slots, ua, S);
+  const int64_t row_bytes = one_row.rs_a + one_row.rs_s;
   const int64_t unit = 4 * rg_step;  // rows one round of the consumer warps covers
   // Tile rows and ring depth for P CTAs per batch within `budget` bytes of shared memory; false
   // if the partial sums and a two-stage ring do not fit.
@@ -434,21 +511,21 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       // at least ~4 tiles per CTA, so the last tile's compute is a small part of the CTA's time
       TR = std::min<int64_t>(TR, std::max<int64_t>(unit, align_up(ceil_div(rows_cap, 4), unit)));
       // shrink by whole rounds until two stages fit this occupancy's budget
-      while (TR > unit && tma_layout(rv, K, TR, 2, rows_cap, slots, ua).total > budget) TR -= unit;
-      while (TR > 4 && tma_layout(rv, K, TR, 2, rows_cap, slots, ua).total > budget) TR -= 4;
+      while (TR > unit && tma_layout(rv, K, TR, 2, rows_cap, slots, ua, S).total > budget) TR -= unit;
+      while (TR > 4 && tma_layout(rv, K, TR, 2, rows_cap, slots, ua, S).total > budget) TR -= 4;
     }
     int64_t NS = f.stages;
     if (NS == 0) {
-      const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots, ua).stage_bytes;
+      const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots, ua, S).stage_bytes;
       const int64_t want = stage < kTmaSmallStage ? 4 : 2;
       for (int64_t ns = want; ns >= 2; --ns)
-        if (tma_layout(rv, K, TR, ns, rows_cap, slots, ua).total <= budget) {
+        if (tma_layout(rv, K, TR, ns, rows_cap, slots, ua, S).total <= budget) {
           NS = ns;
           break;
         }
       if (NS == 0) return false;
     }
-    if (tma_layout(rv, K, TR, NS, rows_cap, slots, ua).total > d.max_smem_optin) return false;
+    if (tma_layout(rv, K, TR, NS, rows_cap, slots, ua, S).total > d.max_smem_optin) return false;
     *TR_out = TR;
     *NS_out = NS;
     return true;
@@ -457,6 +534,7 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   for (int occ = 2; occ >= 1; --occ) {
     const int64_t budget = std::min<int64_t>(d.max_smem_optin, d.max_smem_sm / occ - 1024);
     const int64_t slots_sm = (int64_t)d.sms * occ;
+    const int64_t LS = L * S;  // CTAs per row range: one per batch and slice
     int64_t P = 0, TR = 0, NS = 0;
     if (f.ctas_per_batch) {
       P = std::min<int64_t>(f.ctas_per_batch, M);
@@ -467,7 +545,7 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       // last wave at least 1% better.  Measured on GB300: a grid of 0.84 waves ran at 77% of the
       // bandwidth of four exact waves, and an 80-batch call (5.29 GB) ran at 2.1x the stream
       // kernel's rate.
-      const int64_t P0 = std::min<int64_t>(M, std::max<int64_t>(1, slots_sm / L));
+      const int64_t P0 = std::min<int64_t>(M, std::max<int64_t>(1, slots_sm / LS));
       // the smallest P >= P0 whose partial sums and two-stage ring fit: more CTAs per batch means
       // fewer rows per CTA, so whether a P fits is monotone in P (doubling, then bisection)
       int64_t P_fit = P0, tr = 0, ns = 0;
@@ -483,10 +561,11 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
         }
         P_fit = hi;
       }
-      const int64_t P_hi = std::min<int64_t>(M, P_fit + 8 * P0 + 8);
+      // (split K serves few rows: one wave of row ranges, no search over larger grids)
+      const int64_t P_hi = S > 1 ? P_fit : std::min<int64_t>(M, P_fit + 8 * P0 + 8);
       double best_fill = -1.0;
       for (int64_t p = P_fit; p <= P_hi; ++p) {
-        const int64_t grid = p * L;
+        const int64_t grid = p * LS;
         const double fill = (double)grid / (double)(ceil_div(grid, slots_sm) * slots_sm);
         if (fill <= best_fill + 0.01) continue;
         if (!shape(p, budget, &tr, &ns)) continue;
@@ -498,11 +577,12 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       }
       if (P == 0) continue;
     }
-    if (P * L > (int64_t(1) << 31) - 1)
+    if (P * LS > (int64_t(1) << 31) - 1)
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "grid too large");
     pl->kernel = rv ? NVFP4_KERNEL_TMA_RV : NVFP4_KERNEL_TMA;
     pl->rows_per_warp = 4;
     pl->k_split = (int32_t)nsw;
+    pl->k_slices = (int32_t)S;
     pl->ctas_per_batch = (int32_t)P;
     pl->warps_per_cta = (int32_t)Wc;
     pl->tile_rows = (int32_t)TR;
@@ -583,15 +663,20 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
                   NVFP4_FLAG_TEST_STALL))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown plan flags 0x%x", (unsigned)f.flags);
   if (f.warps_per_cta < 0 || f.rows_per_warp < 0 || f.k_split < 0 || f.ctas_per_batch < 0 ||
-      f.tile_rows < 0 || f.stages < 0)
+      f.tile_rows < 0 || f.stages < 0 || f.k_slices < 0)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "negative plan field");
+  if (f.k_slices > 1 && f.kernel != NVFP4_KERNEL_TMA_RV)
+    return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
+                "k_slices > 1 (split K over a cluster) needs the register-vector TMA kernel");
   memset(pl, 0, sizeof *pl);
   int st = NVFP4_OK;
   switch (f.kernel) {
     case NVFP4_KERNEL_SIMPLE: st = plan_simple(d, M, L, f, pl); break;
     case NVFP4_KERNEL_STREAM: st = plan_stream(d, M, K, L, f, pl); break;
     case NVFP4_KERNEL_TMA: st = plan_tma(d, M, K, L, f, false, pl); break;
-    case NVFP4_KERNEL_TMA_RV: st = plan_tma(d, M, K, L, f, true, pl, !aligned16); break;
+    case NVFP4_KERNEL_TMA_RV:
+      st = plan_tma(d, M, K, L, f, true, pl, !aligned16, f.k_slices > 1 ? f.k_slices : 1);
+      break;
     case NVFP4_KERNEL_TC: st = plan_tc(d, M, K, tc_groups, f, pl); break;
     case NVFP4_KERNEL_SHIFT: st = plan_shift(d, M, K, L, f, pl); break;
     case NVFP4_KERNEL_AUTO: {
@@ -601,6 +686,22 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
       // simple kernel
       const int64_t rows_per_cta = (M * L) / std::max<int64_t>(1, (int64_t)d.sms * 2);
       st = -1;
+      // small calls (few bytes, or few rows): the ring on a grid sized by the call's bytes
+      if (K % 256 == 0 && aligned16 && (rows_per_cta < 8 || small_call(d, M, K, L))) {
+        int64_t S = 0, P = 0;
+        small_call_plan(d, M, K, L, &S, &P);
+        if (S >= 1) {
+          nvfp4_plan f2 = f;
+          if (!f2.ctas_per_batch) f2.ctas_per_batch = (int32_t)P;
+          char saved[sizeof g_last_error];
+          memcpy(saved, g_last_error, sizeof saved);
+          st = plan_tma(d, M, K, L, f2, true, pl, false, S);
+          memcpy(g_last_error, saved, sizeof saved);
+          if (st == NVFP4_OK) break;
+          memset(pl, 0, sizeof *pl);
+        }
+        st = -1;
+      }
       if (K % 256 == 0 && rows_per_cta >= 8) {
         char saved[sizeof g_last_error];
         memcpy(saved, g_last_error, sizeof saved);
@@ -851,7 +952,17 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
       a.b_end = b + L * (K / 2);
       a.sfb_end = sfb + L * (K / 16);
     }
-    const TmaLayout t = tma_layout(rv, K, pl.tile_rows, pl.stages, a.rows_cap, a.slots, ua);
+    const int64_t S = pl.k_slices > 1 ? pl.k_slices : 1;
+    if (S > 1 && (!rv || ua))
+      return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "split K needs the aligned register-vector kernel");
+    if (S > 1) a.slots = (int32_t)std::min<int64_t>(pl.warps_per_cta, nseg / S);
+    const TmaLayout t = tma_layout(rv, K, pl.tile_rows, pl.stages, a.rows_cap, a.slots, ua, S);
+    a.k_slices = (int32_t)S;
+    a.slice_segs = (int32_t)(nseg / S);
+    a.rs_a = (uint32_t)t.rs_a;
+    a.rs_s = (uint32_t)t.rs_s;
+    a.red_off = (uint32_t)t.red_off;
+    a.red_rows = (int32_t)t.red_rows;
     a.stage_bytes = (uint32_t)t.stage_bytes;
     a.sfa_off = (uint32_t)t.sfa_off;
     a.b_off = (uint32_t)t.b_off;
@@ -870,7 +981,14 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
       a.b_out = fx->b_out;
       a.sfb_out = fx->sfb_out;
     }
-    if (rv) {
+    if (rv && S > 1) {
+      if (fx)
+        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, true, false, true>
+                               : nvfp4::gemv_tma_rv_kernel<1, true, false, true>;
+      else
+        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false, false, true>
+                               : nvfp4::gemv_tma_rv_kernel<1, false, false, true>;
+    } else if (rv) {
       if (fx)
         kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, true, false>
                                : nvfp4::gemv_tma_rv_kernel<1, true, false>;
@@ -883,15 +1001,26 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     }
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)(pl.ctas_per_batch * L));
+    cfg.gridDim = dim3((unsigned)(pl.ctas_per_batch * L * S));
     cfg.blockDim = dim3((unsigned)(threads + 32));
     cfg.dynamicSmemBytes = (size_t)t.total;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (!(pl.flags & NVFP4_FLAG_NO_PDL)) {
+      attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[na].val.programmaticStreamSerializationAllowed = 1;
+      ++na;
+    }
+    if (S > 1) {  // the S CTAs of a row range form one cluster (consecutive CTA indices)
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = (unsigned)S;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = (pl.flags & NVFP4_FLAG_NO_PDL) ? 0 : 1;
+    cfg.numAttrs = na;
     const cudaError_t le = cudaLaunchKernelEx(&cfg, kern, a);
     if (le != cudaSuccess) return cuda_fail(le, "kernel launch");
   }

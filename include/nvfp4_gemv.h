@@ -67,7 +67,7 @@
 extern "C" {
 #endif
 
-#define NVFP4_ABI_VERSION 6
+#define NVFP4_ABI_VERSION 7
 
 typedef enum nvfp4_status {
   NVFP4_OK = 0,
@@ -92,7 +92,10 @@ typedef enum nvfp4_kernel {
                                not 16-byte aligned take its unaligned form (bulk copies of each
                                tile's aligned interior, the buffers' first and last partial
                                16 bytes copied one by one, shifted out of shared memory; at most
-                               8 consumer warps) */
+                               8 consumer warps).  With k_slices = S > 1 (aligned operands, S
+                               dividing the 1024-element segment count, S <= 8) K is split over a
+                               thread-block cluster of S CTAs that reduce their partial sums in
+                               distributed shared memory, in slice order (no workspace) */
   NVFP4_KERNEL_TC = 5,      /* tensor cores (tcgen05.mma kind::mxf4nvf4, block scales applied by
                                the MMA, fp32 accumulator in tensor memory): 128-row tiles x up to
                                16 vectors, K split over a cluster of k_split (<= 8) CTAs with a
@@ -143,6 +146,11 @@ typedef struct nvfp4_plan {
   int32_t tile_rows;       /* TMA*: rows per ring stage (1 .. 256); TC: 128 (fixed) */
   int32_t stages;          /* TMA*: ring stages (2 .. 8); TC: 2 .. 6 stages of 256 elements */
   int32_t flags;           /* NVFP4_FLAG_* (honoured by the automatic plan too) */
+  int32_t k_slices;        /* TMA_RV: K slices over a thread-block cluster (0 or 1: no split;
+                              2 .. 8 dividing the 1024-element segment count).  The automatic
+                              plan splits K when one wave of CTA slots would give each CTA fewer
+                              than 8 rows; ctas_per_batch then counts row ranges (the grid is
+                              ctas_per_batch x L x k_slices CTAs) */
 } nvfp4_plan;
 
 /*

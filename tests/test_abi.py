@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_status_strings(lib):
     import decode_nvfp4_gemv_gb300 as pkg
 
-    assert pkg.nvfp4_abi_version() == 6
+    assert pkg.nvfp4_abi_version() == 7
     assert pkg.nvfp4_status_string(0) == "ok"
     assert pkg.nvfp4_status_string(2) == "misaligned pointer"
     assert pkg.nvfp4_status_string(99) == "unknown status"

@@ -35,7 +35,8 @@ def pkg():
     return p
 
 
-PLANS = [dict(kernel=4), dict(kernel=4, flags=1), dict(kernel=3), dict(kernel=5),
+PLANS = [dict(kernel=4), dict(kernel=4, flags=1), dict(kernel=4, k_slices=2),
+         dict(kernel=4, k_slices=2, flags=1), dict(kernel=3), dict(kernel=5),
          dict(kernel=5, k_split=2), dict(kernel=5, flags=1)]
 
 

@@ -62,15 +62,16 @@ def _fill(grid, slots):
 
 
 def test_automatic_plans_fill_their_waves():
-    """Every shape with at least 8 rows per CTA slot and K % 256 == 0 (K <= 16384, two CTAs per
-    SM) gets the register-vector kernel, a valid warp mapping and a last wave >= 95% full."""
+    """Every shape with at least 8 rows per CTA slot, at least 85 KB per SM and K % 256 == 0
+    (K <= 16384, two CTAs per SM) gets the register-vector kernel, a valid warp mapping and a last
+    wave >= 95% full."""
     n = 0
     for K in (256, 512, 1024, 2048, 3072, 4096, 6144, 7168, 16384):
         nseg = -(-K // 1024)
         for M in (256, 1000, 3584, 4096, 7168, 20000, 100000):
             for L in (1, 2, 3, 5, 7, 8, 16, 24, 33, 50, 64, 80, 100, 150, 304, 500):
-                if M * L < 8 * 304:
-                    continue
+                if M * L < 8 * 304 or M * L * (K // 2 + K // 16) < 85 * 1024 * 152:
+                    continue                              # small calls: sized by their bytes
                 p = plan(M, K, L)
                 n += 1
                 assert p["kernel"] == KERNEL_TMA_RV, (M, K, L, p)
@@ -98,8 +99,65 @@ def test_wide_k_keeps_two_ctas_per_sm():
     assert p["tile_rows"] < 4 and p["warps_per_cta"] == 16 and p["k_split"] == 2
 
 
+def _small_call_grid(M, K, L, slots=304):
+    """The grid the planner documents for small calls: 76, 152 or 304 CTAs by the call's bytes
+    (below 10 KB and 85 KB per SM), at most 152 for more than 16 segments unsplit, at most 3/4 of
+    the slots when K is split."""
+    sms = slots // 2
+    nbytes = M * L * (K // 2 + K // 16)
+    G = slots // 4 if nbytes < 10 * 1024 * sms else slots // 2 if nbytes < 85 * 1024 * sms \
+        else slots
+    return G
+
+
+def test_small_calls_take_the_ring_on_a_grid_sized_by_bytes():
+    """Few rows (below 8 per CTA slot) or few bytes (below 85 KB per SM), K % 256 == 0: the
+    register-vector kernel on 76 / 152 / 304 CTAs by the call's bytes; K split over a cluster
+    into slices of at most 16 segments only past 32 segments."""
+    n = 0
+    for K in (256, 1024, 2048, 4096, 7168, 8192, 16384, 32768, 65536, 131072):
+        nseg = -(-K // 1024)
+        for M in (1, 5, 16, 64, 128, 300, 512, 1000, 2000, 2432, 7168):
+            for L in (1, 2, 3):
+                rows = M * L
+                nbytes = rows * (K // 2 + K // 16)
+                if rows >= 8 * 304 and nbytes >= 85 * 1024 * 152:
+                    continue
+                p = plan(M, K, L)
+                S, P = p["k_slices"], p["ctas_per_batch"]
+                if nseg > 32 and not any(nseg % s == 0 and nseg // s <= 16 for s in range(2, 9)):
+                    assert p["kernel"] != KERNEL_TMA_RV or S <= 1, (M, K, L, p)
+                    continue
+                if nseg in (17, 19, 23, 29, 31):                 # no warp mapping: other kernels
+                    continue
+                n += 1
+                assert p["kernel"] == KERNEL_TMA_RV, (M, K, L, p)
+                G = _small_call_grid(M, K, L)
+                if nseg <= 32:
+                    assert S == 1, (M, K, L, p)
+                    if nseg > 16:
+                        G = min(G, 152)
+                else:
+                    assert S == min(s for s in range(2, 9) if nseg % s == 0 and nseg // s <= 16)
+                    G = min(G, 228)
+                assert P == min(M, max(1, G // (L * S))), (M, K, L, p, G)
+    assert n > 250
+
+
+def test_forced_k_slices():
+    p = plan(64, 16384, 1, forced={"kernel": KERNEL_TMA_RV, "k_slices": 2})
+    assert p["k_slices"] == 2 and p["kernel"] == KERNEL_TMA_RV
+    assert plan(64, 16384, 1, forced={"kernel": KERNEL_TMA_RV})["k_slices"] == 1
+    assert plan(7168, 16384, 1)["k_slices"] == 1
+    for forced in ({"kernel": KERNEL_TMA_RV, "k_slices": 3}, {"kernel": KERNEL_TMA_RV, "k_slices": 9},
+                   {"kernel": KERNEL_STREAM, "k_slices": 2}, {"kernel": KERNEL_TMA, "k_slices": 2},
+                   {"kernel": KERNEL_TMA_RV, "k_slices": -1}):
+        assert status_of(64, 16384, 1, forced=forced) == UNSUPPORTED, forced
+
+
 def test_planning_is_deterministic_and_forced_plans_are_echoed():
-    for shape in list(DECODE_PLANS) + [(20000, 4096, 33), (100000, 16384, 80)]:
+    for shape in list(DECODE_PLANS) + [(20000, 4096, 33), (100000, 16384, 80), (64, 16384, 1),
+                                       (512, 65536, 1), (100, 2304, 3)]:
         a = plan(*shape)
         assert plan(*shape) == a
         forced = {k: v for k, v in a.items()}
