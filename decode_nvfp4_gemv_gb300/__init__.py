@@ -26,6 +26,7 @@ from .build import LIB_PATH
 __all__ = [
     "NVFP4Error", "Plan", "KERNEL_AUTO", "KERNEL_SIMPLE", "KERNEL_STREAM", "KERNEL_TMA",
     "KERNEL_TMA_RV", "KERNEL_TC", "KERNEL_SHIFT", "nvfp4_gemm_small_n", "FLAG_EARLY_WEIGHTS", "FLAG_NO_PDL", "FLAG_QUANTIZE_IN_GEMV",
+    "FLAG_NO_L2_PREFETCH",
     "ROUND_HALF_STEP_TABLE",
     "ROUND_NEAREST_EVEN", "nvfp4_quantize_activation", "nvfp4_gemv_batched_bf16", "OUT_F16",
     "OUT_BF16", "nvfp4_gemv_grouped", "library_path",
@@ -37,6 +38,7 @@ __all__ = [
 KERNEL_AUTO, KERNEL_SIMPLE, KERNEL_STREAM, KERNEL_TMA, KERNEL_TMA_RV, KERNEL_TC, KERNEL_SHIFT = (
     0, 1, 2, 3, 4, 5, 6)
 FLAG_EARLY_WEIGHTS, FLAG_NO_PDL, FLAG_QUANTIZE_IN_GEMV, FLAG_TEST_STALL = 1, 2, 4, 8
+FLAG_NO_L2_PREFETCH = 16
 ROUND_HALF_STEP_TABLE, ROUND_NEAREST_EVEN = 0, 1
 OUT_F16, OUT_BF16 = 0, 1
 

@@ -37,6 +37,10 @@
 //   columns 48 + 32 s + 4 j + q   stage s, step j: the tokens' block scales, token r at lane r of
 //                                 every quadrant, all four q
 //
+// Signed block scales: the MMA reads scales as unsigned E4M3; the scale warps negate in place each
+// 16-element block whose scale is negative (its E2M1 sign bits flipped) and pass the magnitude, so
+// every E4M3FN scale, negative ones included, gives the definition's result.
+//
 // Bounded waits: every mbarrier wait gives up after one second; a CTA that gives up writes NaN for
 // its outputs (its partial, under split K).  Programmatic dependent launch as in the TMA kernels.
 #pragma once
@@ -164,6 +168,20 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t local_addr, uint32_t rank
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(a), "f"(b),
                "f"(c), "f"(d)
                : "memory");
+}
+
+// Negates, in a stage tile of 128-byte rows stored with the 128-byte swizzle (16-byte chunk c of
+// row r at chunk c ^ (r mod 8) of its 1024-byte atom), every 16-element block of row r whose
+// scale byte (sign bit 7 of byte j of the scale words) is negative: its 8 bytes XOR 0x88 flip
+// the sign bit of each E2M1 element.
+__device__ __forceinline__ void tc_negate_blocks(uint8_t* tile, int r, const uint32_t (&sc)[4]) {
+  uint8_t* row = tile + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if ((sc[j >> 2] >> (8 * (j & 3) + 7)) & 1u) {
+      uint64_t* blk = reinterpret_cast<uint64_t*>(row + (((j >> 1) ^ (r & 7)) << 4) + ((j & 1) << 3));
+      *blk ^= 0x8888888888888888ull;
+    }
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -381,11 +399,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
         if (lane == 0) *abort_flag = 1;
         break;
       }
-      const uint8_t* st = base + kTcHeaderBytes + rp.s * kTcStageBytes;
+      uint8_t* st = base + kTcHeaderBytes + rp.s * kTcStageBytes;
       uint4 rows[4];  // the 16 scale bytes of rows 32 c + lane, c = 0..3 (word j = MMA step j)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         rows[c] = *reinterpret_cast<const uint4*>(st + kTcOffSA + (32 * c + lane) * 16);
+      uint4 tb = make_uint4(0u, 0u, 0u, 0u);
+      if (lane < p.N) tb = *reinterpret_cast<const uint4*>(st + kTcOffSB + lane * 16);
+      // Signed scales.  The MMA reads block scales as unsigned E4M3, so a block whose scale is
+      // negative enters negated instead: XOR 0x88 on its 8 bytes flips the sign of each of its
+      // 16 elements (exact), and its scale enters as the magnitude (the sign bit cleared below;
+      // a NaN byte stays NaN).  Row 32 q + lane of A is this lane's to patch, the vectors' rows
+      // belong to the lanes of quadrant 0's warp.  Then the generic-proxy stores are made visible
+      // to the MMA's reads before the stage is handed over.
+      {
+        const uint4 own = q == 0 ? rows[0] : q == 1 ? rows[1] : q == 2 ? rows[2] : rows[3];
+        const uint32_t sa[4] = {own.x, own.y, own.z, own.w};
+        const uint32_t sb4[4] = {tb.x, tb.y, tb.z, tb.w};
+        const bool neg_a = ((own.x | own.y | own.z | own.w) & 0x80808080u) != 0;
+        const bool neg_b = q == 0 && ((tb.x | tb.y | tb.z | tb.w) & 0x80808080u) != 0;
+        if (__any_sync(0xffffffffu, neg_a || neg_b)) {
+          if (neg_a) tc_negate_blocks(st, 32 * q + lane, sa);
+          if (neg_b) tc_negate_blocks(st + kTcOffB, lane, sb4);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        rows[c].x &= 0x7F7F7F7Fu;
+        rows[c].y &= 0x7F7F7F7Fu;
+        rows[c].z &= 0x7F7F7F7Fu;
+        rows[c].w &= 0x7F7F7F7Fu;
+      }
+      tb.x &= 0x7F7F7F7Fu;
+      tb.y &= 0x7F7F7F7Fu;
+      tb.z &= 0x7F7F7F7Fu;
+      tb.w &= 0x7F7F7F7Fu;
       const uint4 own = q == 0 ? rows[0] : q == 1 ? rows[1] : q == 2 ? rows[2] : rows[3];
       uint32_t v[16];
 #pragma unroll
@@ -399,8 +448,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
         }
       }
       tc_st16(tmem + lane_addr + 32u + 32u * rp.s, v);
-      uint4 tb = make_uint4(0u, 0u, 0u, 0u);
-      if (lane < p.N) tb = *reinterpret_cast<const uint4*>(st + kTcOffSB + lane * 16);
       uint32_t u[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {

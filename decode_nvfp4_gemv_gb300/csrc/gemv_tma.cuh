@@ -113,6 +113,7 @@ struct TmaArgs {
   uint32_t rs_a, rs_s;
   uint32_t red_off;
   int32_t red_rows;
+  int32_t l2_prefetch;   // strict order: prefetch the first ring fill into L2 before the wait
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -194,7 +195,7 @@ template <bool L2 = false>
 __device__ __forceinline__ uint4 ld16_shifted(const uint8_t* p, uint32_t d, const uint8_t* start,
                                               const uint8_t* end) {
   const uint8_t* a = p - d;
-  if (a >= start && a + 32 <= end) {
+  if (a >= start && a + (d ? 32 : 16) <= end) {  // one aligned chunk when p is aligned
     const uint4 lo = L2 ? ld_l2_v4(a) : ld_l1_v4(a);
     if (d == 0) return lo;
     return shift16(lo, L2 ? ld_l2_v4(a + 16) : ld_l1_v4(a + 16), d);
@@ -302,6 +303,17 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
   __syncthreads();
   pdl_launch_dependents();
   return g;
+}
+
+// Strict stream order: the producer lane prefetches the CTA's first ring fill of A and sfa rows
+// (contiguous, so one prefetch each) into L2 before the launch wait.  A prefetch is a hint that
+// changes no value: every read of A still follows the wait and sees what the preceding work
+// wrote; the copies after the wait then find the bytes in L2.
+__device__ __forceinline__ void tma_prefetch_first_fill(const TmaArgs& p, const TmaCta& g) {
+  const int64_t K2 = p.K >> 1, K16 = p.K >> 4;
+  const int rows = min(g.n, p.stages * p.tile_rows);
+  bulk_prefetch_l2(p.A + (g.ea * p.M + g.m0) * K2, (uint32_t)(rows * K2));
+  bulk_prefetch_l2(p.sfa + (g.ea * p.M + g.m0) * K16, (uint32_t)(rows * K16));
 }
 
 // Grouped form, after the programmatic-launch wait: each warp finds token l's expert itself (all
@@ -522,7 +534,10 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   TmaCta g = tma_setup(p, bars, abort_flag);
-  if (!p.early_weights) pdl_wait();
+  if (!p.early_weights) {
+    if (p.l2_prefetch && warp == g.Wc && lane == 0) tma_prefetch_first_fill(p, g);
+    pdl_wait();
+  }
   tma_resolve_group(p, g, lane);
   if (g.skip) return;
   if (warp == g.Wc) {
@@ -680,7 +695,10 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   TmaCta g = tma_setup(p, bars, abort_flag);
-  if (!p.early_weights) pdl_wait();
+  if (!p.early_weights) {
+    if (p.l2_prefetch && warp == g.Wc && lane == 0) tma_prefetch_first_fill(p, g);
+    pdl_wait();
+  }
   tma_resolve_group(p, g, lane);
   if (g.skip) {
     if constexpr (CL) cluster_barrier();  // the one cluster barrier every CTA takes part in

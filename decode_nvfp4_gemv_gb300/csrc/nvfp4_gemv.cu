@@ -660,7 +660,7 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
                 "kernel %d needs 16-byte aligned A, sfa, b and sfb (TMA_RV, SHIFT and SIMPLE take "
                 "any)", f.kernel);
   if (f.flags & ~(NVFP4_FLAG_EARLY_WEIGHTS | NVFP4_FLAG_NO_PDL | NVFP4_FLAG_QUANTIZE_IN_GEMV |
-                  NVFP4_FLAG_TEST_STALL))
+                  NVFP4_FLAG_TEST_STALL | NVFP4_FLAG_NO_L2_PREFETCH))
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "unknown plan flags 0x%x", (unsigned)f.flags);
   if (f.warps_per_cta < 0 || f.rows_per_warp < 0 || f.k_split < 0 || f.ctas_per_batch < 0 ||
       f.tile_rows < 0 || f.stages < 0 || f.k_slices < 0)
@@ -963,6 +963,10 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     a.rs_s = (uint32_t)t.rs_s;
     a.red_off = (uint32_t)t.red_off;
     a.red_rows = (int32_t)t.red_rows;
+    // strict stream order: the first ring fill is prefetched into L2 before the launch wait
+    // (plain batched rows, aligned and unsplit; the grouped form learns its expert only after it)
+    a.l2_prefetch = !a.early_weights && G.E == 0 && !ua && S == 1 &&
+                    !(pl.flags & NVFP4_FLAG_NO_L2_PREFETCH);
     a.stage_bytes = (uint32_t)t.stage_bytes;
     a.sfa_off = (uint32_t)t.sfa_off;
     a.b_off = (uint32_t)t.b_off;

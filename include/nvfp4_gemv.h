@@ -99,8 +99,9 @@ typedef enum nvfp4_kernel {
   NVFP4_KERNEL_TC = 5,      /* tensor cores (tcgen05.mma kind::mxf4nvf4, block scales applied by
                                the MMA, fp32 accumulator in tensor memory): 128-row tiles x up to
                                16 vectors, K split over a cluster of k_split (<= 8) CTAs with a
-                               deterministic on-chip reduction; needs K % 256 == 0 and
-                               non-negative block scales (the MMA reads them as unsigned E4M3) */
+                               deterministic on-chip reduction; needs K % 256 == 0.  The MMA
+                               reads block scales as unsigned E4M3: a block whose scale is negative
+                               is negated in shared memory and enters with the scale's magnitude */
   NVFP4_KERNEL_SHIFT = 6    /* any K % 16 == 0 and any byte alignment of A, sfa, b, sfb: 16-byte
                                aligned loads around each lane's bytes, funnel-shifted into place,
                                vector staged in shared memory; needs the vector to fit there
@@ -124,7 +125,11 @@ enum {
      copies, so every wait for them gives up at its one-second limit and the launch writes NaN
      (0x7E00) to all of its outputs; nothing faults and the context stays usable.  The other
      kernels ignore it.  Never set in normal use. */
-  NVFP4_FLAG_TEST_STALL = 8
+  NVFP4_FLAG_TEST_STALL = 8,
+  /* Without NVFP4_FLAG_EARLY_WEIGHTS, the TMA kernels prefetch the first ring fill of A and sfa into
+     L2 before they wait for the preceding work (a hint: every read still follows the wait and sees
+     that work's writes).  This flag turns the prefetch off; the results are the same bits. */
+  NVFP4_FLAG_NO_L2_PREFETCH = 16
 };
 
 /*
@@ -287,8 +292,9 @@ int nvfp4_gemv_grouped(const uint8_t* A, const uint8_t* sfa, const float* g_a, c
  * The automatic plan is the tensor-core kernel (NVFP4_KERNEL_TC, groups of up to 16 vectors per
  * launch) when K % 256 == 0 and A, sfa, b, sfb are 16-byte aligned; otherwise, or with a forced
  * CUDA-core plan, the batched kernels run one vector per batch, all batches reading A (L2 serves
- * the repeats).  The TC kernel reads block scales as unsigned E4M3: they must be finite and
- * non-negative.  Checks, statuses and ownership as for nvfp4_gemv_batched_ex with L = N (A holds
+ * the repeats).  Every E4M3FN scale byte is taken as the format defines it on both paths (the TC
+ * kernel negates the blocks whose scales are negative, since its MMA reads scale magnitudes).
+ * Checks, statuses and ownership as for nvfp4_gemv_batched_ex with L = N (A holds
  * one matrix); M == 0 or N == 0 enqueues nothing.
  * ------------------------------------------------------------------------------------------ */
 int nvfp4_gemm_small_n(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,

@@ -270,6 +270,21 @@ def test_other_kernels_agree_at_full_size(pkg, workload, plan):
 
 # ------------------------------------------------------------------ invariants (bit for bit)
 
+@pytest.mark.parametrize("shape", [(7168, 16384, 1), (300, 4096, 3), (2432, 2048, 2)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_l2_prefetch_in_strict_order_changes_no_bit(pkg, shape):
+    """Strict stream order prefetches the first ring fill into L2 before the launch wait; the
+    flag that turns the prefetch off must give the same bits, on both ring kernels."""
+    M, K, L = shape
+    w = workloads.random_workload(M, K, L, seed=M + K + L, scale_bytes=workloads.pow2_scale_bytes(-3, 2),
+                                  g_a=0.25, g_b=0.5)
+    for kernel in (3, 4):
+        on = run(pkg, w, dict(kernel=kernel))
+        off = run(pkg, w, dict(kernel=kernel, flags=16))
+        assert np.array_equal(on.view(np.uint16), off.view(np.uint16)), kernel
+    check(w, on, f"{shape} strict order, prefetch")
+
+
 @pytest.fixture(scope="module")
 def mid():
     return workloads.random_workload(300, 5120, 3, seed=77,

@@ -5,8 +5,9 @@ GEMV with a forced tensor-core plan (N = 1 per batch).  Every output is compared
 (the batched definition, with A repeated for every vector) under the parity tolerance, across
 ragged M (partial 128-row tiles), N from 1 to 19 (19: two launches of at most 16 vectors), K
 splits over clusters of 1 to 8 CTAs (including splits that do not divide the K chunks), ring
-depths, the launch flags, the CUDA-core plans on the same inputs, and determinism.  Block scales
-are non-negative (the MMA reads them as unsigned E4M3).
+depths, the launch flags, the CUDA-core plans on the same inputs, and determinism.  The MMA reads
+block scales as unsigned E4M3; the kernel negates the blocks whose scales are negative, and the
+signed-scale tests check every finite E4M3FN byte, negative ones included, and NaN bytes.
 """
 import numpy as np
 import pytest
@@ -199,3 +200,72 @@ def test_tensor_cores_after_other_work_in_the_stream(pkg):
         g.replay()
     s.synchronize()
     assert np.array_equal(c.cpu().numpy().view(np.uint16), c2.cpu().numpy().view(np.uint16))
+
+
+# ------------------------------------------------------------------ signed and NaN block scales
+
+FINITE = [v for v in range(256) if v not in (0x7F, 0xFF)]
+SIGNED_SHAPES = [(128, 256, 1), (300, 1024, 5), (257, 2304, 16), (1000, 4096, 3)]
+
+
+@pytest.mark.parametrize("shape", SIGNED_SHAPES, ids=[f"{m}x{k}x{n}" for m, k, n in SIGNED_SHAPES])
+def test_signed_scales_on_the_automatic_small_n_path(pkg, shape):
+    """Block scales drawn from every finite E4M3FN byte (half of them negative) on both operands:
+    the automatic small-N plan takes the tensor cores and must give the oracle's result under
+    every split and ring depth."""
+    M, K, N = shape
+    w = workloads.random_workload(M, K, 1, seed=M + 3 * K, scale_bytes=FINITE, g_a=0.5, g_b=2.0)
+    v = workloads.random_workload(1, K, N, seed=M + 5 * K, scale_bytes=FINITE)
+    A, sfa = w.A[0], w.sfa[0]
+    assert (sfa & 0x80).any() and (v.sfb & 0x80).any()
+    ref, T = ref_small_n(A, sfa, v.b, v.sfb, w.g_a, w.g_b, M, K, N)
+    chunks = K // 256
+    plans = [None, dict(kernel=TC, stages=2), dict(kernel=TC, flags=1)]
+    plans += [dict(kernel=TC, k_split=s) for s in (2, 3) if s <= chunks]
+    for plan in plans:
+        c = small_n(pkg, A, sfa, v.b, v.sfb, w.g_a, w.g_b, M, K, N, plan)
+        assert not np.isnan(c).any(), plan
+        assert_parity(c, ref, T, f"signed scales {shape} {plan}")
+
+
+def test_one_negative_scale_negates_its_block(pkg):
+    """A single negative scale byte: flipping its sign bit changes the output by exactly minus two
+    times that block's contribution, as the oracle says."""
+    M, K, N = 128, 512, 2
+    A, sfa, b, sfb, g_a, g_b = make(M, K, N, seed=91)
+    sfa2 = sfa.copy()
+    sfa2[7, 5] |= 0x80
+    sfb2 = sfb.copy()
+    sfb2[1, 30] |= 0x80
+    for sa, sb in ((sfa2, sfb), (sfa, sfb2), (sfa2, sfb2)):
+        c = small_n(pkg, A, sa, b, sb, g_a, g_b, M, K, N)
+        ref, T = ref_small_n(A, sa, b, sb, g_a, g_b, M, K, N)
+        assert_parity(c, ref, T, "one negative scale")
+
+
+def test_nan_scale_bytes_give_nan_on_tensor_cores(pkg):
+    """E4M3 NaN bytes (0x7F, 0xFF) in a matrix row's scales make that row's outputs NaN for every
+    vector; in a vector's scales, that vector's outputs NaN: on the tensor cores as in the
+    oracle."""
+    M, K, N = 256, 1024, 4
+    A, sfa, b, sfb, g_a, g_b = make(M, K, N, seed=93)
+    sfa = sfa.copy()
+    sfb = sfb.copy()
+    sfa[17, 3] = 0x7F
+    sfa[200, 60] = 0xFF
+    sfb[2, 11] = 0x7F
+    c = small_n(pkg, A, sfa, b, sfb, g_a, g_b, M, K, N)
+    ref, T = ref_small_n(A, sfa, b, sfb, g_a, g_b, M, K, N)
+    assert np.isnan(ref[:, 17]).all() and np.isnan(ref[2]).all()
+    assert_parity(c, ref, T, "NaN scales on tensor cores")
+
+
+def test_batched_gemv_forced_onto_tensor_cores_with_signed_scales(pkg):
+    w = workloads.random_workload(200, 2048, 3, seed=95, scale_bytes=FINITE, g_a=0.25, g_b=4.0)
+    t = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (w.A, w.sfa, w.b, w.sfb)]
+    c = torch.full((w.L, w.M), float("nan"), dtype=torch.float16, device="cuda")
+    pkg.nvfp4_gemv_batched_ex(t[0], t[1], w.g_a, t[2], t[3], w.g_b, c, w.M, w.K, w.L,
+                              plan=dict(kernel=TC))
+    torch.cuda.synchronize()
+    ref, T = oracle.gemv(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, w.M, w.K, w.L)
+    assert_parity(c.cpu().numpy(), ref, T, "batched GEMV on tensor cores, signed scales")
