@@ -113,7 +113,9 @@ struct TmaArgs {
   uint32_t rs_a, rs_s;
   uint32_t red_off;
   int32_t red_rows;
-  int32_t l2_prefetch;   // strict order: prefetch the first ring fill into L2 before the wait
+  // rows [pf_row0, pf_row0 + pf_rows) of the CTA's rows are prefetched into L2 before the launch
+  // wait (pf_rows = 0: none); the host sets the first ring fill in strict stream order
+  int32_t pf_row0, pf_rows;
 };
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -305,15 +307,17 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
   return g;
 }
 
-// Strict stream order: the producer lane prefetches the CTA's first ring fill of A and sfa rows
+// The producer lane prefetches rows [pf_row0, pf_row0 + pf_rows) of the CTA's A and sfa rows
 // (contiguous, so one prefetch each) into L2 before the launch wait.  A prefetch is a hint that
-// changes no value: every read of A still follows the wait and sees what the preceding work
-// wrote; the copies after the wait then find the bytes in L2.
-__device__ __forceinline__ void tma_prefetch_first_fill(const TmaArgs& p, const TmaCta& g) {
+// changes no value: every read of A still follows the wait (strict stream order) and sees what
+// the preceding work wrote; the copies after the wait then find the bytes in L2.
+__device__ __forceinline__ void tma_prefetch_rows(const TmaArgs& p, const TmaCta& g) {
   const int64_t K2 = p.K >> 1, K16 = p.K >> 4;
-  const int rows = min(g.n, p.stages * p.tile_rows);
-  bulk_prefetch_l2(p.A + (g.ea * p.M + g.m0) * K2, (uint32_t)(rows * K2));
-  bulk_prefetch_l2(p.sfa + (g.ea * p.M + g.m0) * K16, (uint32_t)(rows * K16));
+  const int r0 = min(g.n, p.pf_row0), r1 = min(g.n, p.pf_row0 + p.pf_rows);
+  if (r1 <= r0) return;
+  const int64_t row = g.ea * p.M + g.m0 + r0;
+  bulk_prefetch_l2(p.A + row * K2, (uint32_t)((r1 - r0) * K2));
+  bulk_prefetch_l2(p.sfa + row * K16, (uint32_t)((r1 - r0) * K16));
 }
 
 // Grouped form, after the programmatic-launch wait: each warp finds token l's expert itself (all
@@ -408,6 +412,14 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
   int issued = 0;
   bool ok = true;
   if (p.test_stall) return;  // every consumer wait then runs out at its limit
+  // Early weights: the producer's first launch wait comes after its early copies; rows to
+  // prefetch into L2 (pf_rows) are requested just before it.
+  bool waited = false;
+  auto launch_wait = [&]() {
+    if (!waited && p.pf_rows) tma_prefetch_rows(p, g);
+    waited = true;
+    pdl_wait();
+  };
   RingPos rp;
   for (int T = 0; T < g.NT; ++T, rp.advance(NS)) {
     const int s = rp.s;
@@ -415,7 +427,7 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
     // the last tile of the first fill only once it has.  Requested early, that tile's bytes would
     // compete for HBM with the preceding call's last tiles: measured on GB300 against requesting
     // the whole ring early, c2 12.34 -> 11.50 us, c3 -3.6%, c4 -1.2%, c5 -1.3%.
-    if (p.early_weights && T == NS - 1) pdl_wait();
+    if (p.early_weights && T == NS - 1) launch_wait();
     // stage s was last filled in the previous round: wait until its consumers released it
     if (T >= NS && !mbar_wait_bounded(smem_addr(&bars[NS + s]), rp.phase ^ 1u, kWaitLimitNs)) {
       ok = false;
@@ -445,7 +457,7 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
           bulk_copy_g2s(smem_addr(st + r * p.rs_a), ga + (int64_t)r * K2, ra, full, pol);
       }
       if (hold) {
-        pdl_wait();
+        launch_wait();
         bulk_copy_g2s(smem_addr(st + (rows_t - 1) * p.rs_a), ga + (int64_t)(rows_t - 1) * K2, ra,
                       full, pol);
       }
@@ -474,7 +486,7 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
       bulk_copy_g2s(smem_addr(st), ga, bytesA - hold, full, pol);
       bulk_copy_g2s(smem_addr(st + p.sfa_off), S_c + (int64_t)T * TR * K16, bytesS, full, pol);
       if (hold) {
-        pdl_wait();
+        launch_wait();
         bulk_copy_g2s(smem_addr(st) + bytesA - hold, ga + (bytesA - hold), hold, full, pol);
       }
     }
@@ -535,7 +547,7 @@ __global__ void __launch_bounds__(544, 1) gemv_tma_kernel(const TmaArgs p) {
 
   TmaCta g = tma_setup(p, bars, abort_flag);
   if (!p.early_weights) {
-    if (p.l2_prefetch && warp == g.Wc && lane == 0) tma_prefetch_first_fill(p, g);
+    if (p.pf_rows && warp == g.Wc && lane == 0) tma_prefetch_rows(p, g);
     pdl_wait();
   }
   tma_resolve_group(p, g, lane);
@@ -696,7 +708,7 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
 
   TmaCta g = tma_setup(p, bars, abort_flag);
   if (!p.early_weights) {
-    if (p.l2_prefetch && warp == g.Wc && lane == 0) tma_prefetch_first_fill(p, g);
+    if (p.pf_rows && warp == g.Wc && lane == 0) tma_prefetch_rows(p, g);
     pdl_wait();
   }
   tma_resolve_group(p, g, lane);

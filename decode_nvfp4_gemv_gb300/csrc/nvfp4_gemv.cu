@@ -965,8 +965,22 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     a.red_rows = (int32_t)t.red_rows;
     // strict stream order: the first ring fill is prefetched into L2 before the launch wait
     // (plain batched rows, aligned and unsplit; the grouped form learns its expert only after it)
-    a.l2_prefetch = !a.early_weights && G.E == 0 && !ua && S == 1 &&
-                    !(pl.flags & NVFP4_FLAG_NO_L2_PREFETCH);
+    // The depth, from sweeps on GB300 of 1 to 8 tiles: the whole first fill (two tiles) for c2
+    // (13.36 -> 11.74 us) and c3 (23.58 -> 21.96), one tile for c4 (8.41 -> 7.44; 7.65 with two)
+    // and c5 (31.94 -> 30.04; 31.16 with two); deeper was slower everywhere.  The rule that fits:
+    // at most a third of a CTA's rows, and at most 7/8 of an SM's shared memory in prefetched bytes
+    // per SM (c3: 2 x 2 x 48 KB = 194 KB per SM; c5 would be 221 KB).
+    a.pf_row0 = 0;
+    a.pf_rows = 0;
+    if (!a.early_weights && G.E == 0 && !ua && S == 1 && !(pl.flags & NVFP4_FLAG_NO_L2_PREFETCH)) {
+      const int64_t grid = (int64_t)pl.ctas_per_batch * L;
+      const int64_t per_sm = std::max<int64_t>(1, ceil_div(grid, (int64_t)d.sms));
+      int64_t tiles = pl.stages;
+      while (tiles > 1 && (3 * tiles * pl.tile_rows > a.rows_cap ||
+                           8 * tiles * t.stage_bytes * per_sm > 7 * (int64_t)d.max_smem_sm))
+        --tiles;
+      a.pf_rows = (int32_t)(tiles * pl.tile_rows);
+    }
     a.stage_bytes = (uint32_t)t.stage_bytes;
     a.sfa_off = (uint32_t)t.sfa_off;
     a.b_off = (uint32_t)t.b_off;
