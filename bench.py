@@ -274,11 +274,17 @@ def recorded_traffic(workload_name: str):
 # ---------------------------------------------------------------------------- our arm
 
 def _device_inputs(w, n_copies, device):
+    """n_copies copies of the workload's inputs at distinct addresses: one pool allocation per
+    operand (copy i is row i of the pool), filled by one device copy each."""
     import torch
 
-    base = {k: torch.from_numpy(np.ascontiguousarray(getattr(w, k))).to(device)
-            for k in ("A", "sfa", "b", "sfb")}
-    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_copies - 1)]
+    sets = [{} for _ in range(n_copies)]
+    for k in ("A", "sfa", "b", "sfb"):
+        x = np.ascontiguousarray(getattr(w, k))
+        base = torch.from_numpy(x.reshape(1, -1)).to(device)
+        pool = base.expand(n_copies, -1).contiguous()
+        for i in range(n_copies):
+            sets[i][k] = pool[i].view(x.shape)
     return sets
 
 
