@@ -598,9 +598,10 @@ def time_general(pkg, w, stream, steps, warmup, dist, n_copies):
 
     peak, _ = measured_peak_gbs()
     out = {"inputs": "A, sfa, b, sfb each 1 byte past a 16-byte boundary"}
-    # the automatic plan (the shift kernel: aligned loads shifted into place), then the byte-load
-    # kernel forced on the same inputs
-    for name, plan in (("automatic", None), ("byte_loads", {"kernel": 1})):
+    # the automatic plan in strict order and with early weights, then the byte-load kernel forced
+    # on the same inputs
+    for name, plan in (("automatic", None), ("automatic_early_weights", {"flags": FLAG_EARLY_WEIGHTS}),
+                       ("byte_loads", {"kernel": 1})):
         def fn(i, plan=plan):
             s = sets[i % n_copies]
             pkg.nvfp4_gemv_batched_ex(s["A"], s["sfa"], w.g_a, s["b"], s["sfb"], w.g_b,
@@ -612,7 +613,7 @@ def time_general(pkg, w, stream, steps, warmup, dist, n_copies):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         auto = (KERNEL_NAMES[4] + " (unaligned form)"
                 if w.K % 256 == 0 and w.M * w.L // (2 * sms) >= 8 else KERNEL_NAMES[6])
-        out[name] = {"kernel": auto if plan is None else KERNEL_NAMES[1],
+        out[name] = {"kernel": KERNEL_NAMES[1] if plan and plan.get("kernel") == 1 else auto,
                      "us_per_call": round(sec / calls * 1e6, 3), "calls": calls,
                      "GB/s": round(tot / slow / 1e9, 2), "frac": round(tot / slow / 1e9 / peak, 4)}
     return out

@@ -211,26 +211,30 @@ __device__ __forceinline__ uint4 ld16_shifted(const uint8_t* p, uint32_t d, cons
   return ld16_bytes(p, start, end);
 }
 
-// One row group (4 rows) times one 32-element lane slice: decode, exact block partials, scale.
-// bw: the 16 vector words for this lane's 32 elements; sb: the two vector block scales.  acc[i]
-// holds row i's running sums of the lane's first and second blocks (added at the flush).
+// One row times one 32-element lane slice: decode, exact block partials, scale.  bw: the 16
+// vector words for this lane's 32 elements; sb: the two vector block scales.  acc holds the row's
+// running sums of the lane's first and second blocks (added at the flush).
+__device__ __forceinline__ void row_compute(const uint4& av, uint16_t sv, const uint32_t (&bw)[16],
+                                            float2 sb, float2& acc) {
+  uint32_t h[16];
+  e2m1x8_to_f16x2x4(av.x, h[0], h[1], h[2], h[3]);
+  e2m1x8_to_f16x2x4(av.y, h[4], h[5], h[6], h[7]);
+  e2m1x8_to_f16x2x4(av.z, h[8], h[9], h[10], h[11]);
+  e2m1x8_to_f16x2x4(av.w, h[12], h[13], h[14], h[15]);
+  uint32_t p0 = 0u, p1 = 0u;  // f16x2 zeros
+#pragma unroll
+  for (int q = 0; q < 8; ++q) hfma2(p0, h[q], bw[q]);
+#pragma unroll
+  for (int q = 8; q < 16; ++q) hfma2(p1, h[q], bw[q]);
+  ffma2(acc, scaled_block_pair(p0, p1, e4m3x2_to_f16x2(sv)), sb);
+}
+
+// One row group (4 rows) times one 32-element lane slice.
 __device__ __forceinline__ void item_compute4(const uint4 (&av)[4], const uint16_t (&sv)[4],
                                               const uint32_t (&bw)[16], float2 sb,
                                               float2 (&acc)[4]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t h[16];
-    e2m1x8_to_f16x2x4(av[i].x, h[0], h[1], h[2], h[3]);
-    e2m1x8_to_f16x2x4(av[i].y, h[4], h[5], h[6], h[7]);
-    e2m1x8_to_f16x2x4(av[i].z, h[8], h[9], h[10], h[11]);
-    e2m1x8_to_f16x2x4(av[i].w, h[12], h[13], h[14], h[15]);
-    uint32_t p0 = 0u, p1 = 0u;  // f16x2 zeros
-#pragma unroll
-    for (int q = 0; q < 8; ++q) hfma2(p0, h[q], bw[q]);
-#pragma unroll
-    for (int q = 8; q < 16; ++q) hfma2(p1, h[q], bw[q]);
-    ffma2(acc[i], scaled_block_pair(p0, p1, e4m3x2_to_f16x2(sv[i])), sb);
-  }
+  for (int i = 0; i < 4; ++i) row_compute(av[i], sv[i], bw, sb, acc[i]);
 }
 
 // Reduces the 4 row sums of a group across the warp and stores them to partial[row][slot].
@@ -307,19 +311,6 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
   return g;
 }
 
-// The producer lane prefetches rows [pf_row0, pf_row0 + pf_rows) of the CTA's A and sfa rows
-// (contiguous, so one prefetch each) into L2 before the launch wait.  A prefetch is a hint that
-// changes no value: every read of A still follows the wait (strict stream order) and sees what
-// the preceding work wrote; the copies after the wait then find the bytes in L2.
-__device__ __forceinline__ void tma_prefetch_rows(const TmaArgs& p, const TmaCta& g) {
-  const int64_t K2 = p.K >> 1, K16 = p.K >> 4;
-  const int r0 = min(g.n, p.pf_row0), r1 = min(g.n, p.pf_row0 + p.pf_rows);
-  if (r1 <= r0) return;
-  const int64_t row = g.ea * p.M + g.m0 + r0;
-  bulk_prefetch_l2(p.A + row * K2, (uint32_t)((r1 - r0) * K2));
-  bulk_prefetch_l2(p.sfa + row * K16, (uint32_t)((r1 - r0) * K16));
-}
-
 // Grouped form, after the programmatic-launch wait: each warp finds token l's expert itself (all
 // warps read the same offsets, so they agree).  A token without an expert gets zero outputs.
 __device__ __forceinline__ void tma_resolve_group(const TmaArgs& p, TmaCta& g, int lane) {
@@ -369,6 +360,19 @@ __device__ __forceinline__ USpan unaligned_span(const uint8_t* g0, const uint8_t
   sp.c1 = u1 < hi ? u1 : hi;
   sp.n = sp.c1 > sp.c0 ? (uint32_t)(sp.c1 - sp.c0) : 0u;
   return sp;
+}
+
+// The producer lane prefetches rows [pf_row0, pf_row0 + pf_rows) of the CTA's A and sfa rows
+// (contiguous, so one prefetch each; 16-byte aligned operands only) into L2 before the launch wait.  A prefetch is a hint that
+// changes no value: every read of A still follows the wait (strict stream order) and sees what
+// the preceding work wrote; the copies after the wait then find the bytes in L2.
+__device__ __forceinline__ void tma_prefetch_rows(const TmaArgs& p, const TmaCta& g) {
+  const int64_t K2 = p.K >> 1, K16 = p.K >> 4;
+  const int r0 = min(g.n, p.pf_row0), r1 = min(g.n, p.pf_row0 + p.pf_rows);
+  if (r1 <= r0) return;
+  const int64_t row = g.ea * p.M + g.m0 + r0;
+  bulk_prefetch_l2(p.A + row * K2, (uint32_t)((r1 - r0) * K2));
+  bulk_prefetch_l2(p.sfa + row * K16, (uint32_t)((r1 - r0) * K16));
 }
 
 __device__ __forceinline__ void stage_unaligned(uint8_t* st, const uint8_t* g0, const uint8_t* g1,
@@ -819,22 +823,29 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
 #pragma unroll
       for (int j = 0; j < NSW; ++j) {
         if (live[j]) {
-          uint4 av[4];
-          uint16_t sv[4];
+          if constexpr (UA) {
+            // one row at a time: the shift needs two 16-byte words a row, and holding all four
+            // rows' words at once spilled registers in the two-segment form
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if constexpr (UA) {
+            for (int i = 0; i < 4; ++i) {
               const uint32_t o = aoff[i] + lane_a[j];
               const uint4 lo = lds_v4(o);
-              av[i] = dA ? shift16(lo, lds_v4(o + 16), dA) : lo;
+              const uint4 a = dA ? shift16(lo, lds_v4(o + 16), dA) : lo;
               const uint32_t so = soff[i] + lane_s[j];
-              sv[i] = (dS & 1u) ? (uint16_t)(lds_u8(so) | (lds_u8(so + 1) << 8)) : lds_u16(so);
-            } else {
+              const uint16_t sv =
+                  (dS & 1u) ? (uint16_t)(lds_u8(so) | (lds_u8(so + 1) << 8)) : lds_u16(so);
+              row_compute(a, sv, bw[j], sb[j], acc[i]);
+            }
+          } else {
+            uint4 av[4];
+            uint16_t sv[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
               av[i] = lds_v4(aoff[i] + lane_a[j]);
               sv[i] = lds_u16(soff[i] + lane_s[j]);
             }
+            item_compute4(av, sv, bw[j], sb[j], acc);
           }
-          item_compute4(av, sv, bw[j], sb[j], acc);
         }
       }
       tma_flush(acc, lane, 4 * rg, rows_t, part_tile, p.slots, slot);

@@ -964,7 +964,8 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     a.red_off = (uint32_t)t.red_off;
     a.red_rows = (int32_t)t.red_rows;
     // strict stream order: the first ring fill is prefetched into L2 before the launch wait
-    // (plain batched rows, aligned and unsplit; the grouped form learns its expert only after it)
+    // (batched rows, aligned and unsplit; the grouped form learns its expert only after it; for
+    // the unaligned form the prefetch measured 18.6 -> 17.9 us on c2 but 12.1 -> 13.0 us on c4)
     // The depth, from sweeps on GB300 of 1 to 8 tiles: the whole first fill (two tiles) for c2
     // (13.36 -> 11.74 us) and c3 (23.58 -> 21.96), one tile for c4 (8.41 -> 7.44; 7.65 with two)
     // and c5 (31.94 -> 30.04; 31.16 with two); deeper was slower everywhere.  The rule that fits:
