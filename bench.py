@@ -296,6 +296,23 @@ def _copies_for(bytes_per_call, device):
     return max(2, -(-3 * l2 // bytes_per_call) + 1), l2
 
 
+def workload_config(w, name, world):
+    """The `config` object both arms print: the workload, and how the GPU arm keeps each call's
+    inputs out of L2 (rotated copies larger than 3x L2)."""
+    import torch
+
+    bytes_call = w.algorithmic_bytes
+    if torch.cuda.is_available():
+        n_copies, l2 = _copies_for(bytes_call, torch.device("cuda", torch.cuda.current_device()))
+        l2_text = (f"GPU arm: inputs rotated over {n_copies} copies "
+                   f"({n_copies * bytes_call / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)")
+    else:
+        l2_text = "GPU arm: inputs rotated over copies larger than 3x L2 (no GPU on this host)"
+    return {"workload": f"NVFP4 decode GEMV M={w.M} K={w.K} L={w.L} ({name})",
+            "M": w.M, "K": w.K, "L": w.L, "bytes_per_call": bytes_call, "l2": l2_text,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def _preroll():
     """A spin kernel on the current stream ahead of a start event: while it runs, the host queues
     the start event and the timed graphs, so the device-timed region starts with the first call
@@ -878,16 +895,9 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "e2m1/e4m3 in, f16x2 block sums, f32 accumulate, f16 out",
             "data": "synthetic (seeded splitmix64; " + w.recipe + ")",
-            "config": {
-                "workload": f"NVFP4 decode GEMV M={w.M} K={w.K} L={w.L} ({args.config})",
-                "M": w.M, "K": w.K, "L": w.L,
-                "bytes_per_call": bytes_call,
-                "l2": f"inputs rotated over {n_copies} copies "
-                      f"({n_copies * bytes_call / 1e6:.0f} MB > 3x L2 {l2 / 1e6:.0f} MB)",
-                "plan": used_plan,
-                "launch": f"CUDA graphs of {chunk} calls after a spin-kernel pre-roll",
-                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            },
+            "config": workload_config(w, args.config, world),
+            "plan": used_plan,
+            "launch": f"CUDA graphs of {chunk} calls after a spin-kernel pre-roll",
             "roofline": {
                 "bound": "hbm",
                 "kernel": KERNEL_NAMES.get(used_plan.get("kernel"), "?"),
@@ -1077,8 +1087,7 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"NVFP4 decode GEMV M={w.M} K={w.K} L={w.L} ({args.config})",
-                       "M": w.M, "K": w.K, "L": w.L},
+            "config": workload_config(w, args.config, world),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": sample, "host_cpus": cpus,
                              "host_cpu_model": model},
