@@ -59,9 +59,12 @@ constexpr int kTcChunkBytes = 128;    // bytes of a row per ring stage (256 elem
 constexpr int kTcMaxStages = 6;
 constexpr int kTcThreads = 320;       // producer, MMA, 4 scale warps, 4 epilogue warps
 constexpr uint32_t kTcTmemCols = 256;
-// stage layout (bytes, every part 1024-aligned): A 128 x 128, tokens 16 x 128, sfa 128 x 16,
-// sfb 16 x 16
-constexpr uint32_t kTcOffB = 16384, kTcOffSA = 18432, kTcOffSB = 20480, kTcStageBytes = 21504;
+// stage layout (bytes, every part 1024-aligned): A 128 x 128, tokens 16 x 128, sfa 128 x 16.
+// The tokens' scales (16 x 16 bytes a stage) sit in a small array after the ring: inside a stage
+// they would round it up to the next 1024 bytes, and five stages of 21504 bytes leave no room for
+// a second CTA on the SM under split K.
+constexpr uint32_t kTcOffB = 16384, kTcOffSA = 18432, kTcStageBytes = 20480;
+constexpr uint32_t kTcSbBytes = 256;
 constexpr uint32_t kTcHeaderBytes = 1024;  // barriers, TMEM address, abort flag
 constexpr uint32_t kTcRedBytes = 9216;     // split-K partials: S x ceil(128 / S) rows x 16 fp32
 
@@ -244,6 +247,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
   const uint32_t ring32 = base32 + kTcHeaderBytes;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int NS = p.stages;
+  const uint32_t sb_off = kTcHeaderBytes + (uint32_t)NS * kTcStageBytes;  // stage s: + 256 s
   const TcWork w = tc_work(p);
   const int npairs = w.ntiles * w.nloc;  // (tile, chunk) pairs this CTA streams
   const uint32_t stage_tx = kTcRows * kTcChunkBytes + (uint32_t)p.N * kTcChunkBytes +
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
         tc_rows(p, w.u0 + k * w.ustep, l, tile, ar, br);
         const uint32_t st = ring32 + g * kTcStageBytes, full = smem_addr(&h->full[g]);
         tma_load_2d(st + kTcOffB, &mB, (w.c0 + i) * kTcChunkBytes, br, full);
-        tma_load_2d(st + kTcOffSB, &mSB, (w.c0 + i) * 16, br, full);
+        tma_load_2d(base32 + sb_off + g * kTcSbBytes, &mSB, (w.c0 + i) * 16, br, full);
       }
       RingPos rp;
       int issued = 0;
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
           tma_load_2d(st, &mA, x, ar, full);
           tma_load_2d(st + kTcOffB, &mB, x, br, full);
           tma_load_2d(st + kTcOffSA, &mSA, xs, ar, full);
-          tma_load_2d(st + kTcOffSB, &mSB, xs, br, full);
+          tma_load_2d(base32 + sb_off + rp.s * kTcSbBytes, &mSB, xs, br, full);
         }
         issued = g + 1;
         if (++i == w.nloc) {
@@ -405,7 +409,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemv_tc_kernel(
       for (int c = 0; c < 4; ++c)
         rows[c] = *reinterpret_cast<const uint4*>(st + kTcOffSA + (32 * c + lane) * 16);
       uint4 tb = make_uint4(0u, 0u, 0u, 0u);
-      if (lane < p.N) tb = *reinterpret_cast<const uint4*>(st + kTcOffSB + lane * 16);
+      if (lane < p.N)
+        tb = *reinterpret_cast<const uint4*>(base + sb_off + rp.s * kTcSbBytes + lane * 16);
       // Signed scales.  The MMA reads block scales as unsigned E4M3, so a block whose scale is
       // negative enters negated instead: XOR 0x88 on its 8 bytes flips the sign of each of its
       // 16 elements (exact), and its scale enters as the magnitude (the sign bit cleared below;

@@ -101,7 +101,10 @@ void init_device(int dev) {
       (e = cudaFuncSetAttribute(nvfp4::gemv_shift_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin)) ||
       (e = cudaFuncSetAttribute(nvfp4::gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                d.max_smem_optin))) {
+                                d.max_smem_optin)) ||
+      (e = cudaFuncSetAttribute(nvfp4::gemv_tc_kernel,
+                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                (int)cudaSharedmemCarveoutMaxShared))) {
     d.err = e;
     return;
   }
@@ -602,7 +605,8 @@ constexpr int kTcDefaultStages = 5;
 // S > 1; at least 80 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM (a
 // third would wait in its TMEM allocation).
 int64_t tc_smem_bytes(int64_t NS, int64_t S) {
-  return std::max<int64_t>(80 * 1024, 1024 + nvfp4::kTcHeaderBytes + NS * nvfp4::kTcStageBytes +
+  return std::max<int64_t>(80 * 1024, 1024 + nvfp4::kTcHeaderBytes +
+                                          NS * (nvfp4::kTcStageBytes + nvfp4::kTcSbBytes) +
                                           (S > 1 ? nvfp4::kTcRedBytes : 0));
 }
 
@@ -627,7 +631,12 @@ int plan_tc(const DeviceInfo& d, int64_t M, int64_t K, int64_t groups, const nvf
                 (long long)S);
   const int64_t per = ceil_div(chunks, S);
   S = ceil_div(chunks, per);  // every slice gets at least one chunk
-  const int64_t NS = f.stages ? f.stages : (S > 1 ? 4 : kTcDefaultStages);
+  // default ring depth: the deepest up to kTcDefaultStages that still lets two CTAs share an SM
+  int64_t NS = f.stages;
+  if (NS == 0) {
+    NS = kTcDefaultStages;
+    while (NS > 2 && 2 * (tc_smem_bytes(NS, S) + 1024) > d.max_smem_sm) --NS;
+  }
   if (NS < 2 || NS > nvfp4::kTcMaxStages || tc_smem_bytes(NS, S) > d.max_smem_optin)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                 "tensor-core kernel: stages must be 2..%d within shared memory",
@@ -800,7 +809,8 @@ int launch_tc(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const
   a.early_weights = (pl.flags & NVFP4_FLAG_EARLY_WEIGHTS) ? 1 : 0;
   a.test_stall = (pl.flags & NVFP4_FLAG_TEST_STALL) ? 1 : 0;
   a.total_tiles = (int32_t)(groups * a.tiles);
-  a.red_off = nvfp4::kTcHeaderBytes + (uint32_t)pl.stages * nvfp4::kTcStageBytes;
+  a.red_off = nvfp4::kTcHeaderBytes +
+              (uint32_t)pl.stages * (nvfp4::kTcStageBytes + nvfp4::kTcSbBytes);
   const int64_t smem = tc_smem_bytes(pl.stages, a.S);
   // S == 1: persistent CTAs, as many as fit at once (at most two per SM); S > 1: one per
   // (tile, slice)
