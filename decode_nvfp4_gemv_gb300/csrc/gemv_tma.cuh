@@ -316,7 +316,7 @@ __device__ __forceinline__ TmaCta tma_setup(const TmaArgs& p, uint64_t* bars,
 __device__ __forceinline__ void tma_resolve_group(const TmaArgs& p, TmaCta& g, int lane) {
   if (p.G.E <= 0) return;
   const int e = group_of_batch(p.G, g.l, lane);
-  // one verdict for the whole CTA (called by every thread), so no warp can be left waiting at a
+  // one decision for the whole CTA (called by every thread), so no warp can be left waiting at a
   // barrier for warps that skipped, even if the routing changed under a misbehaving writer
   g.skip = __syncthreads_or(e < 0) != 0;
   if (g.skip) {
@@ -504,7 +504,7 @@ __device__ __forceinline__ void tma_produce(const TmaArgs& p, const TmaCta& g, u
   }
 }
 
-// Consumer wait for the tile at ring position r; the verdict is voted so the whole warp leaves
+// Consumer wait for the tile at ring position r; the outcome is voted so the whole warp leaves
 // together.
 __device__ __forceinline__ bool tma_consume_wait(const TmaArgs& p, uint64_t* bars,
                                                  volatile int* abort_flag, const RingPos& r,

@@ -92,7 +92,7 @@ def test_grid_values_round_trip(rounding):
         assert np.allclose(deq, x, rtol=1e-6, atol=0), (rounding, sf_byte)
 
 
-def test_lut_and_rne_disagree_where_the_survey_says():
+def test_lut_and_rne_disagree_at_the_half_steps():
     mags = np.float32([0.2, 0.25, 0.75, 1.25, 1.3, 2.5, 2.6, 3.6, 5.1, 5.6])
     lut = [GRID[c] for c in Q.e2m1_code_lut(mags)]
     rne = [GRID[c] for c in Q.e2m1_code_rne(mags)]
