@@ -210,6 +210,18 @@ def test_tensor_core_plans():
     assert status_of(7168, 512, 1, forced={"kernel": KERNEL_TC, "k_split": 3}) == UNSUPPORTED
 
 
+def test_tensor_core_ring_keeps_two_ctas_per_sm():
+    # five stages of 20,480 bytes plus the tokens' scales and the split-K partials: 114,944 bytes,
+    # two CTAs in the 228 KB of an SM
+    p = plan(7168, 16384, 1, forced={"kernel": KERNEL_TC})
+    assert (p["k_split"], p["stages"]) == (5, 5)
+    assert plan(7168, 16384, 16, forced={"kernel": KERNEL_TC})["stages"] == 5
+    # with less shared memory per SM the ring gets shallower instead of leaving one CTA per SM
+    r = plan(7168, 16384, 1, forced={"kernel": KERNEL_TC}, max_smem_sm=200 * 1024,
+             max_smem_optin=199 * 1024)
+    assert (r["k_split"], r["stages"]) == (5, 4)
+
+
 @pytest.mark.parametrize("lim", [dict(sms=0), dict(max_smem_optin=512),
                                  dict(max_smem_sm=1000, max_smem_optin=2000)],
                          ids=["no SMs", "tiny smem", "sm smem below cta smem"])
