@@ -893,7 +893,9 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "e2m1/e4m3 in, f16x2 block sums, f32 accumulate, f16 out",
+            "dtype": "f32",
+            "dtype_detail": "e2m1 / e4m3 inputs, exact f16x2 block sums, f32 scaling and "
+                            "accumulation, f16 output",
             "data": "synthetic (seeded splitmix64; " + w.recipe + ")",
             "config": workload_config(w, args.config, world),
             "plan": used_plan,
