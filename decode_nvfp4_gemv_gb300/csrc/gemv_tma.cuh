@@ -180,12 +180,21 @@ __device__ __forceinline__ uint4 shift16(const uint4& lo, const uint4& hi, uint3
 }
 
 // The 16 bytes at p read one by one, those outside [start, end) taken as zero (the first and the
-// last chunk of a buffer).
+// last chunk of a buffer).  All sixteen loads are issued before the first is used, so the bytes
+// cost one memory round trip, not sixteen.  L2 = true reads through L2 only (.cg).
+template <bool L2 = false>
 __device__ __forceinline__ uint4 ld16_bytes(const uint8_t* p, const uint8_t* start,
                                             const uint8_t* end) {
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
-  for (uint32_t j = 0; j < 16u; ++j)
-    if (p + j >= start && p + j < end) w[j >> 2] |= (uint32_t)p[j] << (8u * (j & 3u));
+  uint32_t v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint8_t* q = p + j;
+    v[j] = (q >= start && q < end) ? (uint32_t)(L2 ? __ldcg(q) : *q) : 0u;
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = v[4 * i] | (v[4 * i + 1] << 8) | (v[4 * i + 2] << 16) | (v[4 * i + 3] << 24);
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
@@ -202,13 +211,7 @@ __device__ __forceinline__ uint4 ld16_shifted(const uint8_t* p, uint32_t d, cons
     if (d == 0) return lo;
     return shift16(lo, L2 ? ld_l2_v4(a + 16) : ld_l1_v4(a + 16), d);
   }
-  if constexpr (L2) {
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    for (uint32_t j = 0; j < 16u; ++j)
-      if (p + j >= start && p + j < end) w[j >> 2] |= (uint32_t)__ldcg(p + j) << (8u * (j & 3u));
-    return make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  return ld16_bytes(p, start, end);
+  return ld16_bytes<L2>(p, start, end);
 }
 
 // One row times one 32-element lane slice: decode, exact block partials, scale.  bw: the 16
@@ -708,9 +711,11 @@ __device__ __forceinline__ void tma_cluster_reduce(const TmaArgs& p, const TmaCt
 // Vector slice in registers (W_c divides the segment count, or the segment count divides W_c).
 // QX: the vector is bf16 and is quantized to NVFP4 here (see quantize.cuh); its bytes feed the same
 // decode as packed input would.  CL: split K over a cluster (the CTA's segments are those of its
-// slice; rows of a stage lie rs_a / rs_s bytes apart).
+// slice; rows of a stage lie rs_a / rs_s bytes apart).  VA: A and sfa aligned, b or sfb not: the
+// vector is staged by shifted loads (a separate instantiation; a run-time switch there slowed
+// the aligned kernels' main loop by 0.5-1.3%).
 // ------------------------------------------------------------------------------------------------
-template <int NSW, bool QX, bool UA, bool CL = false>
+template <int NSW, bool QX, bool UA, bool CL = false, bool VA = false>
 __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel(const TmaArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
@@ -752,15 +757,24 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
   uint32_t bw[NSW][16];
   float2 sb[NSW];
 #pragma unroll
+  // the vector slice: every segment's loads go out before the first is decoded (one L2 round
+  // trip, not NSW; with a branch between them they went out one after another: c2 11.3 ->
+  // 12.3 us)
+  int64_t kks[NSW];
+  uint4 vv[NSW];
+  uint16_t ss[NSW];
+#pragma unroll
   for (int j = 0; j < NSW; ++j) {
     seg[j] = many ? warp + j * Wc : warp % nseg;
     const int64_t k = (int64_t)seg[j] * kStep + 32 * lane;  // inside the slice
     live[j] = k < g.kz;
     // lanes past the slice's end read its first element and never use it
-    const int64_t kk = g.k0 + (live[j] ? k : 0);
-    uint4 v;
-    uint16_t s2;
-    if constexpr (QX) {
+    kks[j] = g.k0 + (live[j] ? k : 0);
+  }
+  if constexpr (QX) {
+#pragma unroll
+    for (int j = 0; j < NSW; ++j) {
+      const int64_t kk = kks[j];
       const uint16_t* xs = p.x + g.l * K + kk;
       uint32_t xv[16];
 #pragma unroll
@@ -772,28 +786,108 @@ __global__ void __launch_bounds__(UA ? 288 : 544, UA ? 2 : 1) gemv_tma_rv_kernel
         xv[4 * q + 3] = t.w;
       }
       uint32_t pk[4];
-      quantize_blocks2(xv, p.x_gs, p.rounding, pk, s2);
-      v = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      quantize_blocks2(xv, p.x_gs, p.rounding, pk, ss[j]);
+      vv[j] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       // one writer per segment: the first CTA of the batch, and (when several warps share a
       // segment) the warps of the first row-group round
       if (live[j] && g.pi == 0 && rg_first == 0) {
-        *reinterpret_cast<uint4*>(p.b_out + g.l * K2 + (kk >> 1)) = v;
-        *reinterpret_cast<uint16_t*>(p.sfb_out + g.l * K16 + (kk >> 4)) = s2;
+        *reinterpret_cast<uint4*>(p.b_out + g.l * K2 + (kk >> 1)) = vv[j];
+        *reinterpret_cast<uint16_t*>(p.sfb_out + g.l * K16 + (kk >> 4)) = ss[j];
       }
-    } else if constexpr (UA) {  // any alignment, through L2
-      const uint8_t* bp = p.b + g.l * K2 + (kk >> 1);
-      v = ld16_shifted<true>(bp, (uint32_t)((uintptr_t)bp & 15u), p.b, p.b_end);
-      const uint8_t* sp = p.sfb + g.l * K16 + (kk >> 4);
-      s2 = (uint16_t)((uint32_t)__ldcg(sp) | ((uint32_t)__ldcg(sp + 1) << 8));
-    } else {
-      v = ld_l2_v4(p.b + g.l * K2 + (kk >> 1));
-      s2 = ld_l2_u16(p.sfb + g.l * K16 + (kk >> 4));
     }
-    e2m1x8_to_f16x2x4(v.x, bw[j][0], bw[j][1], bw[j][2], bw[j][3]);
-    e2m1x8_to_f16x2x4(v.y, bw[j][4], bw[j][5], bw[j][6], bw[j][7]);
-    e2m1x8_to_f16x2x4(v.z, bw[j][8], bw[j][9], bw[j][10], bw[j][11]);
-    e2m1x8_to_f16x2x4(v.w, bw[j][12], bw[j][13], bw[j][14], bw[j][15]);
-    sb[j] = f16x2_to_f32x2(e4m3x2_to_f16x2(s2));
+  } else if constexpr (UA || VA) {  // any alignment, through L2
+    // A lane reads the two aligned 16-byte chunks around its 16 bytes and shifts them; only at the
+    // buffer's first and last bytes (nothing outside [b, b_end) is read) does it read byte by byte.
+    // The usual case is one warp-uniform block with all the loads in flight at once.
+    const uint8_t* bps[NSW];
+    uint32_t dd[NSW];
+    bool fast = true;
+#pragma unroll
+    for (int j = 0; j < NSW; ++j) {
+      bps[j] = p.b + g.l * K2 + (kks[j] >> 1);
+      dd[j] = (uint32_t)((uintptr_t)bps[j] & 15u);
+      const uint8_t* a = bps[j] - dd[j];
+      fast = fast && a >= p.b && a + (dd[j] ? 32 : 16) <= p.b_end;
+    }
+    const bool sfb_even = (((uintptr_t)p.sfb) & 1u) == 0;  // K/16 is even: the grid's parity
+    if (__all_sync(0xffffffffu, fast)) {
+      // consecutive live lanes hold consecutive 16-byte chunks: a lane's second chunk is the
+      // next lane's first; lane 31, and a lane whose neighbour does not hold the next chunk (the
+      // last live lane of a partial segment), loads its own
+      uint4 lo[NSW], hi[NSW];
+      bool own[NSW];
+#pragma unroll
+      for (int j = 0; j < NSW; ++j) {
+        const unsigned long long nxt =
+            __shfl_down_sync(0xffffffffu, reinterpret_cast<unsigned long long>(bps[j]), 1);
+        own[j] = lane == 31 || nxt != reinterpret_cast<unsigned long long>(bps[j] + 16);
+        lo[j] = ld_l2_v4(bps[j] - dd[j]);
+        hi[j] = (own[j] && dd[j]) ? ld_l2_v4(bps[j] - dd[j] + 16) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      // the scale bytes go out before the shuffles below wait for the chunks
+      if (sfb_even) {
+#pragma unroll
+        for (int j = 0; j < NSW; ++j) ss[j] = ld_l2_u16(p.sfb + g.l * K16 + (kks[j] >> 4));
+      } else {
+#pragma unroll
+        for (int j = 0; j < NSW; ++j) {
+          const uint8_t* sp = p.sfb + g.l * K16 + (kks[j] >> 4);
+          ss[j] = (uint16_t)((uint32_t)__ldcg(sp) | ((uint32_t)__ldcg(sp + 1) << 8));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NSW; ++j) {
+        const uint4 nx = make_uint4(__shfl_down_sync(0xffffffffu, lo[j].x, 1),
+                                    __shfl_down_sync(0xffffffffu, lo[j].y, 1),
+                                    __shfl_down_sync(0xffffffffu, lo[j].z, 1),
+                                    __shfl_down_sync(0xffffffffu, lo[j].w, 1));
+        if (!own[j]) hi[j] = nx;
+      }
+#pragma unroll
+      for (int j = 0; j < NSW; ++j) vv[j] = dd[j] ? shift16(lo[j], hi[j], dd[j]) : lo[j];
+    } else {  // a warp holding the buffer's first or last bytes
+#pragma unroll
+      for (int j = 0; j < NSW; ++j) {
+        const uint8_t* a = bps[j] - dd[j];
+        const bool ok = a >= p.b && a + (dd[j] ? 32 : 16) <= p.b_end;
+        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+        if (ok) {
+          lo = ld_l2_v4(a);
+          if (dd[j]) hi = ld_l2_v4(a + 16);
+        }
+        const uint8_t* sp = p.sfb + g.l * K16 + (kks[j] >> 4);
+        ss[j] = (uint16_t)((uint32_t)__ldcg(sp) | ((uint32_t)__ldcg(sp + 1) << 8));
+        // the lanes whose chunks reach past the buffer: lanes 0..15 of the warp load one byte each
+        // of such a lane's 16 bytes (one request), which then collects them by shuffles
+        uint4 vb = make_uint4(0u, 0u, 0u, 0u);
+        for (uint32_t need = __ballot_sync(0xffffffffu, !ok); need; need &= need - 1u) {
+          const int e = __ffs((int)need) - 1;
+          const uint8_t* base = reinterpret_cast<const uint8_t*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(bps[j]), e));
+          const uint8_t* q = base + (lane & 15);
+          const uint32_t byte = (lane < 16 && q >= p.b && q < p.b_end) ? (uint32_t)__ldcg(q) : 0u;
+          uint32_t w4[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int t = 0; t < 16; ++t) w4[t >> 2] |= __shfl_sync(0xffffffffu, byte, t) << (8 * (t & 3));
+          if (lane == e) vb = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        vv[j] = !ok ? vb : dd[j] ? shift16(lo, hi, dd[j]) : lo;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NSW; ++j) {
+      vv[j] = ld_l2_v4(p.b + g.l * K2 + (kks[j] >> 1));
+      ss[j] = ld_l2_u16(p.sfb + g.l * K16 + (kks[j] >> 4));
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NSW; ++j) {
+    e2m1x8_to_f16x2x4(vv[j].x, bw[j][0], bw[j][1], bw[j][2], bw[j][3]);
+    e2m1x8_to_f16x2x4(vv[j].y, bw[j][4], bw[j][5], bw[j][6], bw[j][7]);
+    e2m1x8_to_f16x2x4(vv[j].z, bw[j][8], bw[j][9], bw[j][10], bw[j][11]);
+    e2m1x8_to_f16x2x4(vv[j].w, bw[j][12], bw[j][13], bw[j][14], bw[j][15]);
+    sb[j] = f16x2_to_f32x2(e4m3x2_to_f16x2(ss[j]));
   }
   for (int i = threadIdx.x; i < p.rows_cap * p.slots; i += cthreads) part[i] = 0.f;
   named_barrier(1, (uint32_t)cthreads);

@@ -98,6 +98,14 @@ void init_device(int dev) {
                               d.max_smem_optin)) ||
       (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, true, false, true>,
                               d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, false, false, false, true>,
+                              d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false, false, false, true>,
+                              d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<1, false, false, true, true>,
+                              d.max_smem_optin)) ||
+      (e = prepare_tma_kernel(nvfp4::gemv_tma_rv_kernel<2, false, false, true, true>,
+                              d.max_smem_optin)) ||
       (e = cudaFuncSetAttribute(nvfp4::gemv_shift_kernel,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem_optin)) ||
       (e = cudaFuncSetAttribute(nvfp4::gemv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -137,6 +145,10 @@ int current_device(const DeviceInfo** out) {
 bool overlaps(const void* a, int64_t na, const void* b, int64_t nb) {
   const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
   return x < y + (uintptr_t)nb && y < x + (uintptr_t)na;
+}
+
+bool matrix_aligned16(const void* A, const void* sfa) {
+  return (((uintptr_t)A | (uintptr_t)sfa) & 15u) == 0;
 }
 
 // n_mats: matrices in A and sfa (L for the batched form, E for the grouped form).
@@ -470,7 +482,7 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
                 (long long)K);
   if (S > 1) {
     if (ua)
-      return fail(NVFP4_ERR_MISALIGNED, "split K over a cluster needs 16-byte aligned operands");
+      return fail(NVFP4_ERR_MISALIGNED, "split K over a cluster needs 16-byte aligned A and sfa");
     if (!rv || S > nvfp4::kTmaMaxClusterK || ceil_div(K, nvfp4::kStep) % S != 0)
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                   "split K: the register-vector kernel, k_slices <= %d dividing the %lld "
@@ -657,8 +669,10 @@ int plan_tc(const DeviceInfo& d, int64_t M, int64_t K, int64_t groups, const nvf
   return NVFP4_OK;
 }
 
+// aligned16: A, sfa, b and sfb all 16-byte aligned; mat16: A and sfa 16-byte aligned (the
+// register-vector kernel's aligned form takes a vector at any alignment).
 int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan* forced,
-              nvfp4_plan* pl, bool aligned16 = true, int64_t tc_groups = -1) {
+              nvfp4_plan* pl, bool aligned16, bool mat16, int64_t tc_groups = -1) {
   if (tc_groups < 0) tc_groups = L;
   nvfp4_plan f;
   memset(&f, 0, sizeof f);
@@ -684,7 +698,7 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
     case NVFP4_KERNEL_STREAM: st = plan_stream(d, M, K, L, f, pl); break;
     case NVFP4_KERNEL_TMA: st = plan_tma(d, M, K, L, f, false, pl); break;
     case NVFP4_KERNEL_TMA_RV:
-      st = plan_tma(d, M, K, L, f, true, pl, !aligned16, f.k_slices > 1 ? f.k_slices : 1);
+      st = plan_tma(d, M, K, L, f, true, pl, !mat16, f.k_slices > 1 ? f.k_slices : 1);
       break;
     case NVFP4_KERNEL_TC: st = plan_tc(d, M, K, tc_groups, f, pl); break;
     case NVFP4_KERNEL_SHIFT: st = plan_shift(d, M, K, L, f, pl); break;
@@ -696,7 +710,7 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
       const int64_t rows_per_cta = (M * L) / std::max<int64_t>(1, (int64_t)d.sms * 2);
       st = -1;
       // small calls (few bytes, or few rows): the ring on a grid sized by the call's bytes
-      if (K % 256 == 0 && aligned16 && (rows_per_cta < 8 || small_call(d, M, K, L))) {
+      if (K % 256 == 0 && mat16 && (rows_per_cta < 8 || small_call(d, M, K, L))) {
         int64_t S = 0, P = 0;
         small_call_plan(d, M, K, L, &S, &P);
         if (S >= 1) {
@@ -716,7 +730,7 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
         memcpy(saved, g_last_error, sizeof saved);
         for (bool rv : {true, false}) {
           if (!aligned16 && !rv) break;  // unaligned operands: the register-vector kernel only
-          if (plan_tma(d, M, K, L, f, rv, pl, !aligned16) == NVFP4_OK) {
+          if (plan_tma(d, M, K, L, f, rv, pl, rv && !mat16) == NVFP4_OK) {
             st = NVFP4_OK;
             break;
           }
@@ -941,12 +955,19 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     a.slots = (int32_t)(rv ? std::min<int64_t>(pl.warps_per_cta, nseg) : pl.warps_per_cta);
     a.early_weights = (pl.flags & NVFP4_FLAG_EARLY_WEIGHTS) ? 1 : 0;
     a.test_stall = (pl.flags & NVFP4_FLAG_TEST_STALL) ? 1 : 0;
-    // operands not 16-byte aligned (the register-vector kernel's unaligned form): the aligned
-    // interiors of A and sfa and the ends of b and sfb bound every read
-    const bool ua = (((uintptr_t)A | (uintptr_t)sfa | (uintptr_t)b | (uintptr_t)sfb) & 15u) != 0;
-    if (ua && (!rv || fx))
+    // A or sfa not 16-byte aligned: the register-vector kernel's unaligned form, the aligned
+    // interiors of A and sfa and the ends of b and sfb bounding every read.  Only b or sfb not
+    // aligned: the aligned form, its vector loaded once per CTA with shifted loads inside [b,
+    // b_end) and [sfb, sfb_end).
+    const bool ua = !matrix_aligned16(A, sfa);
+    const bool va = (((uintptr_t)b | (uintptr_t)sfb) & 15u) != 0;
+    if ((ua || va) && (!rv || fx))
       return fail(NVFP4_ERR_MISALIGNED, "this TMA plan needs 16-byte aligned operands");
     a.A_lo = a.A_hi = a.S_lo = a.S_hi = a.b_end = a.sfb_end = nullptr;
+    if (va) {
+      a.b_end = b + L * (K / 2);
+      a.sfb_end = sfb + L * (K / 16);
+    }
     if (ua) {
       const int64_t n_mats = G.E > 0 ? (int64_t)G.E : (G.shared_a ? 1 : L);  // matrices in A
       auto up16 = [](const uint8_t* q) {
@@ -1014,6 +1035,9 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
       if (fx)
         kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, true, false, true>
                                : nvfp4::gemv_tma_rv_kernel<1, true, false, true>;
+      else if (va)
+        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false, false, true, true>
+                               : nvfp4::gemv_tma_rv_kernel<1, false, false, true, true>;
       else
         kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false, false, true>
                                : nvfp4::gemv_tma_rv_kernel<1, false, false, true>;
@@ -1024,6 +1048,9 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
       else if (ua)
         kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false, true>
                                : nvfp4::gemv_tma_rv_kernel<1, false, true>;
+      else if (va)
+        kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false, false, false, true>
+                               : nvfp4::gemv_tma_rv_kernel<1, false, false, false, true>;
       else
         kern = pl.k_split == 2 ? nvfp4::gemv_tma_rv_kernel<2, false, false>
                                : nvfp4::gemv_tma_rv_kernel<1, false, false>;
@@ -1074,7 +1101,8 @@ int gemv_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t* b,
   if (forced && (forced->flags & NVFP4_FLAG_QUANTIZE_IN_GEMV))
     return fail(NVFP4_ERR_INVALID_VALUE, "NVFP4_FLAG_QUANTIZE_IN_GEMV needs a bf16 vector");
   nvfp4_plan pl;
-  if ((st = make_plan(*d, M, K, L, forced, &pl, aligned16)) != NVFP4_OK) return st;
+  if ((st = make_plan(*d, M, K, L, forced, &pl, aligned16, matrix_aligned16(A, sfa))) != NVFP4_OK)
+    return st;
   return launch(*d, pl, A, sfa, g_a, b, sfb, g_b, c, M, K, L, (cudaStream_t)stream);
 }
 
@@ -1160,7 +1188,8 @@ int gemv_bf16_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint16
       (st = check_access(*d, sfb_out, "sfb_out")) || (st = check_access(*d, c, "c")))
     return st;
   nvfp4_plan pl;
-  if ((st = make_plan(*d, M, K, L, forced, &pl, aligned16)) != NVFP4_OK) return st;
+  if ((st = make_plan(*d, M, K, L, forced, &pl, aligned16, matrix_aligned16(A, sfa))) != NVFP4_OK)
+    return st;
   if (pl.flags & NVFP4_FLAG_QUANTIZE_IN_GEMV) {  // quantize inside the GEMV's vector staging
     if (pl.kernel != NVFP4_KERNEL_TMA_RV)
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
@@ -1216,7 +1245,8 @@ int grouped_impl(const uint8_t* A, const uint8_t* sfa, const float* g_a, const u
       (st = check_access(*d, g_b, "g_b")) || (st = check_access(*d, idx, "expert indices")))
     return st;
   nvfp4_plan pl;
-  if ((st = make_plan(*d, M, K, T, forced, &pl, aligned16)) != NVFP4_OK) return st;
+  if ((st = make_plan(*d, M, K, T, forced, &pl, aligned16, matrix_aligned16(A, sfa))) != NVFP4_OK)
+    return st;
   GroupedOut go;
   go.G.offsets = offsets;
   go.G.expert_of = expert_of;
@@ -1254,11 +1284,14 @@ int small_n_impl(const uint8_t* A, const uint8_t* sfa, float g_a, const uint8_t*
     f.kernel = NVFP4_KERNEL_TC;
     char saved[sizeof g_last_error];
     memcpy(saved, g_last_error, sizeof saved);
-    tc = make_plan(*d, M, K, std::min<int64_t>(N, nvfp4::kTcCols), &f, &pl, true, 1) == NVFP4_OK;
+    tc = make_plan(*d, M, K, std::min<int64_t>(N, nvfp4::kTcCols), &f, &pl, true, true, 1) ==
+         NVFP4_OK;
     memcpy(g_last_error, saved, sizeof saved);
   }
   if (!tc) {
-    if ((st = make_plan(*d, M, K, N, forced, &pl, aligned16, 1)) != NVFP4_OK) return st;
+    if ((st = make_plan(*d, M, K, N, forced, &pl, aligned16, matrix_aligned16(A, sfa), 1)) !=
+        NVFP4_OK)
+      return st;
     tc = pl.kernel == NVFP4_KERNEL_TC;
   }
   if (tc) {  // groups of up to 16 vectors, one launch each
@@ -1314,7 +1347,7 @@ int nvfp4_gemv_plan(int64_t M, int64_t K, int64_t L, nvfp4_plan* out) {
   const DeviceInfo* d = nullptr;
   int st = current_device(&d);
   if (st != NVFP4_OK) return st;
-  return make_plan(*d, M, K, L, nullptr, out);
+  return make_plan(*d, M, K, L, nullptr, out, true, true);
 }
 
 int nvfp4_plan_for_limits(const nvfp4_device_limits* lim, int64_t M, int64_t K, int64_t L,
@@ -1333,7 +1366,7 @@ int nvfp4_plan_for_limits(const nvfp4_device_limits* lim, int64_t M, int64_t K, 
   d.sms = lim->sms;
   d.max_smem_optin = lim->max_smem_optin;
   d.max_smem_sm = lim->max_smem_sm;
-  return make_plan(d, M, K, L, forced, out);
+  return make_plan(d, M, K, L, forced, out, true, true);
 }
 
 int64_t nvfp4_max_stream_k(void) {

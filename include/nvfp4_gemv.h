@@ -49,10 +49,12 @@
  *   NVFP4_ERR_UNSUPPORTED_SHAPE  M, L or K/2 above 2^31 - 1, or an invalid forced plan
  *   NVFP4_ERR_MISALIGNED      c not 2-byte aligned, or a forced plan other than TMA_RV, SHIFT or
  *                             SIMPLE while A, sfa, b or sfb is not 16-byte aligned
- *   Any alignment of A, sfa, b and sfb is accepted.  When one of them is not 16-byte aligned the
- *   automatic plan is TMA_RV's unaligned form if K % 256 == 0 and every CTA gets 8 rows; else
- *   (and for aligned operands with K % 32 != 0) the SHIFT kernel (aligned 16-byte loads shifted
- *   into place), or the SIMPLE kernel (byte loads) when the vector does not fit shared memory.
+ *   Any alignment of A, sfa, b and sfb is accepted.  When only b or sfb is not 16-byte aligned,
+ *   TMA_RV keeps the plan aligned operands get and loads the vector with shifted loads.  When A or
+ *   sfa is not, the automatic plan is TMA_RV's unaligned form if K % 256 == 0 and every CTA gets 8
+ *   rows; else (and for aligned operands with K % 32 != 0) the SHIFT kernel (aligned 16-byte
+ *   loads shifted into place), or the SIMPLE kernel (byte loads) when the vector does not fit
+ *   shared memory.
  *   NVFP4_ERR_ARCH            the current device is not compute capability 10.3 (GB300)
  *   NVFP4_ERR_CUDA            a CUDA runtime call or the launch failed (nvfp4_last_error() has
  *                             the runtime's message)
@@ -88,11 +90,12 @@ typedef enum nvfp4_kernel {
                                (TMA) and mbarriers, vector in shared memory; needs K % 256 == 0 */
   NVFP4_KERNEL_TMA_RV = 4,  /* as TMA with each consumer warp's vector slice held in registers;
                                needs K % 256 == 0 and the warp count to divide the number of
-                               1024-element K segments (or be a multiple of it).  Operands that are
-                               not 16-byte aligned take its unaligned form (bulk copies of each
+                               1024-element K segments (or be a multiple of it).  A vector (b,
+                               sfb) not 16-byte aligned is loaded with shifted loads; A or sfa not
+                               16-byte aligned take its unaligned form (bulk copies of each
                                tile's aligned interior, the buffers' first and last partial
                                16 bytes copied one by one, shifted out of shared memory; at most
-                               8 consumer warps).  With k_slices = S > 1 (aligned operands, S
+                               8 consumer warps).  With k_slices = S > 1 (A and sfa aligned, S
                                dividing the 1024-element segment count, S <= 8) K is split over a
                                thread-block cluster of S CTAs that reduce their partial sums in
                                distributed shared memory, in slice order (no workspace) */

@@ -174,7 +174,8 @@ def test_shift_kernel_grouped_forms(pkg):
         assert_parity(out, ref, T, f"grouped unaligned {plan}")
 
 
-RING_SHAPES = [(2432, 2048, 1), (300, 4096, 9), (97, 1024, 3), (1000, 16384, 1)]
+RING_SHAPES = [(2432, 2048, 1), (300, 4096, 9), (97, 1024, 3), (1000, 16384, 1),
+               (600, 4352, 2)]                                # a partial last segment
 
 
 @pytest.mark.parametrize("shape", RING_SHAPES, ids=[f"{m}x{k}x{l}" for m, k, l in RING_SHAPES])
@@ -208,6 +209,43 @@ def test_unaligned_operands_on_the_tma_ring(pkg, shape, offsets):
             ring = out
         elif plan is not None and plan.get("kernel") == 4 and "tile_rows" not in plan:
             assert np.array_equal(out.view(np.uint16), ring.view(np.uint16)), plan
+
+
+VEC_SHAPES = [(2432, 2048, 1), (300, 4096, 9), (64, 65536, 1), (40, 16384, 3),
+              (700, 2304, 2), (1500, 1280, 1)]                # partial last segments
+
+
+@pytest.mark.parametrize("shape", VEC_SHAPES, ids=[f"{m}x{k}x{l}" for m, k, l in VEC_SHAPES])
+@pytest.mark.parametrize("offsets", [(0, 0, 1, 0), (0, 0, 0, 3), (0, 0, 9, 5), (0, 0, 15, 15)])
+def test_unaligned_vector_keeps_the_aligned_ring(pkg, shape, offsets):
+    """Only b or sfb off a 16-byte boundary: the aligned ring form with its usual plan (split K
+    and small-call grids included), the vector loaded with shifted loads.  The outputs are the
+    oracle's and bit-identical to the same call on aligned copies, for the automatic plan and with
+    early weights."""
+    M, K, L = shape
+    w = workloads.random_workload(M, K, L, seed=M + K + L + sum(offsets),
+                                  scale_bytes=workloads.pow2_scale_bytes(-4, 3), g_a=0.5, g_b=1.5)
+    ref, T = oracle.gemv(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, M, K, L)
+    keep = []
+
+    def run(offs, plan):
+        args = []
+        for name, off in zip(("A", "sfa", "b", "sfb"), offs):
+            v, raw = placed(getattr(w, name), off)
+            keep.append(raw)
+            args.append(v)
+        c = torch.full((L, M), float("nan"), dtype=torch.float16, device="cuda")
+        pkg.nvfp4_gemv_batched_ex(args[0], args[1], w.g_a, args[2], args[3], w.g_b, c, M, K, L,
+                                  plan=plan)
+        torch.cuda.synchronize()
+        return c.cpu().numpy()
+
+    for plan in (None, dict(flags=1)):
+        aligned = run((0, 0, 0, 0), plan)
+        out = run(offsets, plan)
+        assert not np.isnan(out).any(), plan
+        assert_parity(out, ref, T, f"{shape} {offsets} {plan}")
+        assert np.array_equal(out.view(np.uint16), aligned.view(np.uint16)), plan
 
 
 def test_unaligned_grouped_on_the_tma_ring(pkg):
