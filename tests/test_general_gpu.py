@@ -248,6 +248,32 @@ def test_unaligned_vector_keeps_the_aligned_ring(pkg, shape, offsets):
         assert np.array_equal(out.view(np.uint16), aligned.view(np.uint16)), plan
 
 
+def test_unaligned_vector_grouped_keeps_the_aligned_ring(pkg):
+    """The grouped form with aligned experts and token vectors off 16-byte boundaries: the aligned
+    ring form, bit-identical to the same call on aligned vectors."""
+    w = workloads.make_grouped("g0")
+    A = torch.from_numpy(w.A).cuda()
+    sfa = torch.from_numpy(w.sfa).cuda()
+    g_a = torch.from_numpy(np.ascontiguousarray(w.g_a)).cuda()
+    g_b = torch.from_numpy(np.ascontiguousarray(w.g_b)).cuda()
+    emap = torch.from_numpy(np.ascontiguousarray(w.expert_of, dtype=np.int32)).cuda()
+    from oracle import grouped as G
+    ref, T = G.gemv_grouped(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, w.expert_of, w.M, w.K)
+    outs = []
+    for ob, osb in ((0, 0), (3, 0), (0, 5), (11, 7)):
+        b, rb = placed(w.b, ob)
+        sfb, rsb = placed(w.sfb, osb)
+        c = torch.full((w.T, w.M), float("nan"), dtype=torch.float16, device="cuda")
+        pkg.nvfp4_gemv_grouped(A, sfa, g_a, b, sfb, g_b, c, w.M, w.K, w.E, w.T,
+                               expert_of_token=emap, plan=dict(kernel=4))
+        torch.cuda.synchronize()
+        out = c.cpu().numpy()
+        assert_parity(out, ref, T, f"grouped vector +{ob}/+{osb}")
+        outs.append(out)
+    for out in outs[1:]:
+        assert np.array_equal(out.view(np.uint16), outs[0].view(np.uint16))
+
+
 def test_unaligned_grouped_on_the_tma_ring(pkg):
     """The grouped form with unaligned experts on the register-vector TMA kernel."""
     w = workloads.make_grouped("g0")
