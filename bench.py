@@ -421,9 +421,22 @@ def _gemv_caller(pkg, w, sets, outs, plan, stream):
     return call
 
 
+def plan_with_flags(pkg, M, K, L, plan):
+    """The automatic plan a call with these forced fields (flags included) gets on the current
+    device: the planner's choice depends on the flags (three CTAs per SM need early weights)."""
+    import torch
+
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    lim = dict(sms=props.multi_processor_count)
+    if hasattr(props, "shared_memory_per_block_optin"):
+        lim["max_smem_optin"] = props.shared_memory_per_block_optin
+    if hasattr(props, "shared_memory_per_multiprocessor"):
+        lim["max_smem_sm"] = props.shared_memory_per_multiprocessor
+    return pkg.nvfp4_plan_for_limits(M, K, L, plan=plan, **lim).as_dict()
+
+
 def _plan_name(pkg, w, flags):
-    p = pkg.nvfp4_gemv_plan(w.M, w.K, w.L).as_dict()
-    p["flags"] = flags
+    p = plan_with_flags(pkg, w.M, w.K, w.L, {"flags": flags})
     return KERNEL_NAMES.get(p["kernel"], "?"), p
 
 
@@ -458,6 +471,10 @@ def time_per_config(pkg, device, stream, steps, warmup, dist, names=("c1", "c2",
             gbs = tot / slow / 1e9
             row[key] = {"us_per_call": round(sec / n * 1e6, 3), "calls": n,
                         "GB/s": round(gbs, 2), "frac": round(gbs / peak, 4)}
+            if flags != FLAG_EARLY_WEIGHTS:
+                sp = _plan_name(pkg, w, flags)[1]
+                if any(sp[k] != plan[k] for k in sp if k != "flags"):
+                    row[key]["plan"] = sp
             del t
         assert not torch.isnan(outs[0]).any().item()
         out[name] = row
@@ -790,8 +807,7 @@ def run_ours(args):
     stream = torch.cuda.Stream(device)
     timer = GraphTimer(_gemv_caller(pkg, w, sets, outs, plan, stream), args.steps, args.warmup,
                        stream)
-    used_plan = pkg.nvfp4_gemv_plan(w.M, w.K, w.L).as_dict()
-    used_plan.update({k: v for k, v in plan.items() if v})
+    used_plan = plan_with_flags(pkg, w.M, w.K, w.L, plan)
     uuid = str(torch.cuda.get_device_properties(device).uuid)
     gpu_id = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
 

@@ -45,8 +45,15 @@ struct DeviceInfo {
   int max_smem_optin = 0;   // bytes of shared memory one CTA may opt into
   int max_smem_sm = 0;      // bytes of shared memory per SM
   int pageable_access = 0;  // the device can read pageable host memory
+  // registers a thread of the one-segment register-vector kernel takes (its three-CTA plans
+  // assume at most kRv1RegsForThreeCtas); the design value when no device is queried
+  int rv1_regs = 65;
   PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;  // driver's tensor-map encoder
 };
+
+// Three CTAs of at most 8 warps (7 consumers and the producer) fit an SM's 64 K registers at up to
+// 72 registers a thread, also within each of the four schedulers' 16 K (6 warps x 72 x 32).
+constexpr int kRv1RegsForThreeCtas = 72;
 
 std::once_flag g_dev_once[kMaxDevices];
 DeviceInfo g_dev[kMaxDevices];
@@ -115,6 +122,13 @@ void init_device(int dev) {
                                 (int)cudaSharedmemCarveoutMaxShared))) {
     d.err = e;
     return;
+  }
+  {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, nvfp4::gemv_tma_rv_kernel<1, false, false>) == cudaSuccess)
+      d.rv1_regs = fa.numRegs;
+    else
+      cudaGetLastError();
   }
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -515,6 +529,7 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   const int64_t unit = 4 * rg_step;  // rows one round of the consumer warps covers
   // Tile rows and ring depth for P CTAs per batch within `budget` bytes of shared memory; false
   // if the partial sums and a two-stage ring do not fit.
+  int occ_try = 2;  // the occupancy being tried (set by the loop below)
   auto shape = [&](int64_t P, int64_t budget, int64_t* TR_out, int64_t* NS_out) -> bool {
     const int64_t rows_cap = ceil_div(M, P);
     int64_t TR = f.tile_rows;
@@ -532,7 +547,8 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
     int64_t NS = f.stages;
     if (NS == 0) {
       const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots, ua, S).stage_bytes;
-      const int64_t want = stage < kTmaSmallStage ? 4 : 2;
+      // three CTAs per SM keep two stages (4-stage rings of small tiles measured 5-10% slower)
+      const int64_t want = stage < kTmaSmallStage && occ_try < 3 ? 4 : 2;
       for (int64_t ns = want; ns >= 2; --ns)
         if (tma_layout(rv, K, TR, ns, rows_cap, slots, ua, S).total <= budget) {
           NS = ns;
@@ -545,8 +561,19 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
     *NS_out = NS;
     return true;
   };
-  // two CTAs per SM if the ring fits, else one
-  for (int occ = 2; occ >= 1; --occ) {
+  // Two CTAs per SM if the ring fits, else one.  With at most 7 consumer warps of one segment each,
+  // three CTAs per SM first: more warps to hide the decode's latency and fewer rows per CTA.
+  // Measured on GB300 (K = 7168, 7 warps, early weights; us per call, automatic two-CTA plan
+  // against three CTAs with 8-row tiles, 4-row where a CTA has few rows): 7168 x 7168 x 1 7.97 ->
+  // 6.50, 4096 x 7168 x 8 (c3) 21.21 -> 20.63, 7168 x 7168 x 4 19.09 -> 18.31, 2048 x 7168 x 8
+  // 12.22 -> 11.64, 16384 x 7168 x 1 12.23 -> 11.73, 1536 x 7168 x 16 16.51 -> 16.01.  Plans
+  // with 12 warps (c4, c5) did not gain from three CTAs of 8 warps.
+  // In strict stream order the three-CTA plans lost as often as they won (4096 x 7168 x 8 21.5 ->
+  // 22.5 us, 16384 x 7168 x 1 13.0 -> 12.7), so they are for calls with early weights only.
+  const bool three = rv && !ua && S == 1 && nsw == 1 && Wc + 1 <= 8 &&
+                     (f.flags & NVFP4_FLAG_EARLY_WEIGHTS) && d.rv1_regs <= kRv1RegsForThreeCtas;
+  for (int occ = three ? 3 : 2; occ >= 1; --occ) {
+    occ_try = occ;
     const int64_t budget = std::min<int64_t>(d.max_smem_optin, d.max_smem_sm / occ - 1024);
     const int64_t slots_sm = (int64_t)d.sms * occ;
     const int64_t LS = L * S;  // CTAs per row range: one per batch and slice

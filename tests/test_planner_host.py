@@ -38,12 +38,12 @@ def status_of(M, K, L, forced=None, **lim):
 
 
 # (M, K, L): kernel, CTAs per batch, consumer warps, 1024-element segments per warp, tile rows,
-# ring stages -- one wave of 304 CTAs (two per SM) for each workload
+# ring stages, CTAs per SM -- one wave of CTAs for each workload, with early weights
 DECODE_PLANS = {
-    (7168, 16384, 1): (KERNEL_TMA_RV, 304, 8, 2, 4, 2),
-    (4096, 7168, 8): (KERNEL_TMA_RV, 38, 7, 1, 12, 2),
-    (7168, 2048, 4): (KERNEL_TMA_RV, 76, 12, 1, 24, 2),
-    (3584, 6144, 16): (KERNEL_TMA_RV, 19, 12, 1, 16, 2),
+    (7168, 16384, 1): (KERNEL_TMA_RV, 304, 8, 2, 4, 2, 2),
+    (4096, 7168, 8): (KERNEL_TMA_RV, 57, 7, 1, 8, 2, 3),    # 7 warps of one segment: 3 per SM
+    (7168, 2048, 4): (KERNEL_TMA_RV, 76, 12, 1, 24, 2, 2),
+    (3584, 6144, 16): (KERNEL_TMA_RV, 19, 12, 1, 16, 2, 2),
 }
 
 
@@ -52,9 +52,22 @@ def test_decode_workload_plans_on_gb300(shape):
     p = plan(*shape, forced={"flags": 1})
     got = (p["kernel"], p["ctas_per_batch"], p["warps_per_cta"], p["k_split"], p["tile_rows"],
            p["stages"])
-    assert got == DECODE_PLANS[shape]
+    assert got == DECODE_PLANS[shape][:6]
     assert p["flags"] == 1 and p["rows_per_warp"] == 4
-    assert p["ctas_per_batch"] * shape[2] == 2 * 152
+    assert p["ctas_per_batch"] * shape[2] == DECODE_PLANS[shape][6] * 152
+
+
+def test_three_ctas_per_sm_only_with_early_weights():
+    # in strict stream order the 7-warp plans keep two CTAs per SM
+    p = plan(4096, 7168, 8, forced={"flags": 0})
+    assert (p["ctas_per_batch"], p["warps_per_cta"], p["tile_rows"], p["stages"]) == (38, 7, 12, 2)
+    # with early weights, three; a CTA with few rows keeps 4-row tiles and two stages
+    q = plan(7168, 7168, 1, forced={"flags": 1})
+    assert (q["ctas_per_batch"], q["tile_rows"], q["stages"]) == (456, 4, 2)
+    # 8 or more consumer warps never take three CTAs per SM
+    for shape in ((7168, 16384, 1), (7168, 8192, 1), (7168, 2048, 4)):
+        r = plan(*shape, forced={"flags": 1})
+        assert r["ctas_per_batch"] * shape[2] <= 2 * 152, shape
 
 
 def _fill(grid, slots):
