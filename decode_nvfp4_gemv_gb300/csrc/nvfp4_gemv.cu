@@ -48,12 +48,22 @@ struct DeviceInfo {
   // registers a thread of the one-segment register-vector kernel takes (its three-CTA plans
   // assume at most kRv1RegsForThreeCtas); the design value when no device is queried
   int rv1_regs = 65;
+  int rv2_regs = 90;  // the same for the two-segment kernel
   PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;  // driver's tensor-map encoder
 };
 
 // Three CTAs of at most 8 warps (7 consumers and the producer) fit an SM's 64 K registers at up to
 // 72 registers a thread, also within each of the four schedulers' 16 K (6 warps x 72 x 32).
 constexpr int kRv1RegsForThreeCtas = 72;
+
+// CTAs of the aligned register-vector kernel (Wc consumer warps and the producer) that an SM's
+// registers hold: each of the four schedulers owns a quarter (16 K) of the register file, and a
+// warp takes its registers in units of 8 a thread.
+int64_t rv_ctas_by_regs(const DeviceInfo& d, int64_t Wc, int64_t nsw) {
+  const int64_t regs = ((nsw == 2 ? d.rv2_regs : d.rv1_regs) + 7) / 8 * 8;
+  const int64_t warps_per_scheduler = 16384 / (regs * 32);
+  return std::max<int64_t>(1, 4 * warps_per_scheduler / (Wc + 1));
+}
 
 std::once_flag g_dev_once[kMaxDevices];
 DeviceInfo g_dev[kMaxDevices];
@@ -127,6 +137,10 @@ void init_device(int dev) {
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, nvfp4::gemv_tma_rv_kernel<1, false, false>) == cudaSuccess)
       d.rv1_regs = fa.numRegs;
+    else
+      cudaGetLastError();
+    if (cudaFuncGetAttributes(&fa, nvfp4::gemv_tma_rv_kernel<2, false, false>) == cudaSuccess)
+      d.rv2_regs = fa.numRegs;
     else
       cudaGetLastError();
   }
@@ -547,8 +561,9 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
     int64_t NS = f.stages;
     if (NS == 0) {
       const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots, ua, S).stage_bytes;
-      // three CTAs per SM keep two stages (4-stage rings of small tiles measured 5-10% slower)
-      const int64_t want = stage < kTmaSmallStage && occ_try < 3 ? 4 : 2;
+      // three CTAs per SM keep two stages (4-stage rings of small tiles measured 5-10% slower);
+      // one CTA per SM (where the registers allow no more) takes four, the bytes in flight of two
+      const int64_t want = (stage < kTmaSmallStage && occ_try < 3) || occ_try == 1 ? 4 : 2;
       for (int64_t ns = want; ns >= 2; --ns)
         if (tma_layout(rv, K, TR, ns, rows_cap, slots, ua, S).total <= budget) {
           NS = ns;
@@ -572,7 +587,12 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   // 22.5 us, 16384 x 7168 x 1 13.0 -> 12.7), so they are for calls with early weights only.
   const bool three = rv && !ua && S == 1 && nsw == 1 && Wc + 1 <= 8 &&
                      (f.flags & NVFP4_FLAG_EARLY_WEIGHTS) && d.rv1_regs <= kRv1RegsForThreeCtas;
-  for (int occ = three ? 3 : 2; occ >= 1; --occ) {
+  // and never more CTAs than the registers hold: 11 or more warps of two segments (K of 20 to 32
+  // segments unsplit) take one CTA per SM; planned as two they ran as a second wave (8192 x 24576:
+  // 22.97 us on 304 CTAs, 20.54 on 152)
+  const int occ_max = (int)std::min<int64_t>(three ? 3 : 2,
+                                             rv && !ua ? rv_ctas_by_regs(d, Wc, nsw) : 2);
+  for (int occ = occ_max; occ >= 1; --occ) {
     occ_try = occ;
     const int64_t budget = std::min<int64_t>(d.max_smem_optin, d.max_smem_sm / occ - 1024);
     const int64_t slots_sm = (int64_t)d.sms * occ;
@@ -755,7 +775,35 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
       if (K % 256 == 0 && rows_per_cta >= 8) {
         char saved[sizeof g_last_error];
         memcpy(saved, g_last_error, sizeof saved);
+        // Wide K whose unsplit warps hold only one CTA per SM: when half of K runs on two-segment
+        // warps that fit two CTAs, split K over clusters of 2.  Measured on GB300 (early weights,
+        // us per call, one CTA per SM with a four-stage ring against the split): 8192 x 28672 x 1
+        // 25.87 -> 23.74, 4096 x 28672 x 4 47.28 -> 42.56, 8192 x 32768 x 1 27.01 -> 25.80,
+        // 4096 x 32768 x 4 49.39 -> 46.05.  Where the halves take one-segment warps (K of 20 to 24
+        // segments) the split lost (8192 x 24576 x 1: 19.41 unsplit, 21.21 split).
+        // Beyond 32 segments no warp mapping holds the whole vector: split K over the smallest
+        // cluster whose slices it holds (two for K up to 65536).  Against the shared-memory-vector
+        // kernel these shapes used to take: 8192 x 40960 x 1 60.8 -> 38.2 us, 8192 x 65536 x 1
+        // 169.8 -> 56.9 us.
+        if (mat16 && f.k_slices == 0 && st != NVFP4_OK) {
+          const int64_t nseg = ceil_div(K, nvfp4::kStep);
+          int64_t nsw1 = 1, nsw2 = 1;
+          const int64_t W1 = rv_warps(nseg, f.warps_per_cta, &nsw1);
+          int64_t S = 0;
+          if (W1 && rv_ctas_by_regs(d, W1, nsw1) < 2 && nseg % 2 == 0) {
+            const int64_t W2 = rv_warps(nseg / 2, f.warps_per_cta, &nsw2);
+            if (W2 && nsw2 == 2 && rv_ctas_by_regs(d, W2, nsw2) >= 2) S = 2;
+          } else if (!W1) {
+            for (int64_t s2 = 2; s2 <= nvfp4::kTmaMaxClusterK && !S; ++s2)
+              if (nseg % s2 == 0 && rv_warps(nseg / s2, f.warps_per_cta, &nsw2)) S = s2;
+          }
+          if (S && plan_tma(d, M, K, L, f, true, pl, false, S) == NVFP4_OK)
+            st = NVFP4_OK;
+          else
+            memset(pl, 0, sizeof *pl);
+        }
         for (bool rv : {true, false}) {
+          if (st == NVFP4_OK) break;
           if (!aligned16 && !rv) break;  // unaligned operands: the register-vector kernel only
           if (plan_tma(d, M, K, L, f, rv, pl, rv && !mat16) == NVFP4_OK) {
             st = NVFP4_OK;

@@ -104,12 +104,34 @@ def test_plans_follow_the_sm_count():
     assert plan(4096, 7168, 8, **half)["ctas_per_batch"] == 19
 
 
-def test_wide_k_keeps_two_ctas_per_sm():
-    """K = 32768 (18 KB per row): tiles shrink below four rows so that two CTAs still share an
-    SM, and 16 warps take two 1024-element segments each."""
-    p = plan(7168, 32768, 1)
-    assert p["kernel"] == KERNEL_TMA_RV and p["ctas_per_batch"] == 304
-    assert p["tile_rows"] < 4 and p["warps_per_cta"] == 16 and p["k_split"] == 2
+def test_register_capped_rings_take_one_wave():
+    """K of 20-24 segments unsplit: 10-12 consumer warps of two segments each hold ~90 registers a
+    thread, so the register file takes one CTA per SM; the grid is one wave of 152 CTAs, with a
+    four-stage ring to keep the SM's loads in flight."""
+    for M, K, L in ((8192, 20480, 1), (8192, 24576, 1), (4096, 24576, 4)):
+        p = plan(M, K, L, forced={"flags": 1})
+        assert p["kernel"] == KERNEL_TMA_RV and p["k_slices"] == 1, (M, K, L, p)
+        assert p["ctas_per_batch"] * L == 152 and p["stages"] == 4, (M, K, L, p)
+        assert p["k_split"] == 2 and p["warps_per_cta"] == K // 2048, (M, K, L, p)
+
+
+def test_wide_k_splits_over_a_cluster_of_two():
+    """K of 28-32 segments: split over a cluster of two CTAs, each slice on 7-8 warps of two
+    segments, two clusters' CTAs per SM -- instead of one 14-16 warp CTA per SM."""
+    for M, K in ((7168, 32768), (8192, 28672)):
+        p = plan(M, K, 1, forced={"flags": 1})
+        assert p["kernel"] == KERNEL_TMA_RV and p["k_slices"] == 2, (M, K, p)
+        assert p["ctas_per_batch"] * 2 == 304 and p["k_split"] == 2, (M, K, p)
+        assert p["warps_per_cta"] == K // 4096, (M, K, p)
+
+
+@pytest.mark.parametrize("K,S", [(40960, 2), (65536, 2), (98304, 3), (131072, 4), (262144, 8)])
+def test_huge_k_splits_into_the_fewest_slices(K, S):
+    """Past 32 segments no single CTA holds the vector slice: K splits over the fewest CTAs of a
+    cluster (at most 8) that divide the segments into slices of at most 32."""
+    p = plan(8192, K, 1, forced={"flags": 1})
+    assert p["kernel"] == KERNEL_TMA_RV and p["k_slices"] == S, p
+    assert -(-K // 1024) // S <= 32
 
 
 def _small_call_grid(M, K, L, slots=304):
