@@ -49,6 +49,9 @@ struct DeviceInfo {
   // assume at most kRv1RegsForThreeCtas); the design value when no device is queried
   int rv1_regs = 65;
   int rv2_regs = 90;  // the same for the two-segment kernel
+  // thread-block clusters of S CTAs resident at once at occ CTAs per SM ([occ - 1][S]), from the
+  // occupancy query; 0 where not queried
+  int cluster_cap[2][9] = {};
   PFN_cuTensorMapEncodeTiled_v12000 encode_tiled = nullptr;  // driver's tensor-map encoder
 };
 
@@ -63,6 +66,19 @@ int64_t rv_ctas_by_regs(const DeviceInfo& d, int64_t Wc, int64_t nsw) {
   const int64_t regs = ((nsw == 2 ? d.rv2_regs : d.rv1_regs) + 7) / 8 * 8;
   const int64_t warps_per_scheduler = 16384 / (regs * 32);
   return std::max<int64_t>(1, 4 * warps_per_scheduler / (Wc + 1));
+}
+
+// The same counts on GB300 (152 SMs), for planning without a device.  A cluster's CTAs share one
+// GPC, so past two CTAs a cluster the GPCs' SM counts leave CTA slots empty: 36 clusters of 4 at
+// one CTA per SM hold 144 of the 152 slots, 36 of 8 at two per SM 288 of 304.
+constexpr int kClusterCapGb300[2][9] = {{0, 152, 76, 46, 36, 28, 23, 15, 15},
+                                        {0, 304, 152, 97, 74, 58, 46, 38, 36}};
+
+// Clusters of S CTAs (2 <= S <= 8) the device holds at once at occ (1 or 2) CTAs per SM.
+int64_t clusters_resident(const DeviceInfo& d, int occ, int64_t S) {
+  occ = std::min(std::max(occ, 1), 2);
+  if (d.cluster_cap[occ - 1][S] > 0) return d.cluster_cap[occ - 1][S];
+  return std::max<int64_t>(1, (int64_t)kClusterCapGb300[occ - 1][S] * d.sms / 152);
 }
 
 std::once_flag g_dev_once[kMaxDevices];
@@ -144,6 +160,29 @@ void init_device(int dev) {
     else
       cudaGetLastError();
   }
+  // clusters resident at once, for one and two CTAs per SM (shared memory sized to allow exactly
+  // that many; 128 threads keep the registers out of the answer)
+  for (int occ = 1; occ <= 2; ++occ)
+    for (int S = 2; S <= nvfp4::kTmaMaxClusterK; ++S) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)S);
+      cfg.blockDim = dim3(128);
+      cfg.dynamicSmemBytes = (size_t)std::min(d.max_smem_optin, d.max_smem_sm / occ - 1024);
+      cudaLaunchAttribute a[1];
+      a[0].id = cudaLaunchAttributeClusterDimension;
+      a[0].val.clusterDim.x = (unsigned)S;
+      a[0].val.clusterDim.y = 1;
+      a[0].val.clusterDim.z = 1;
+      cfg.attrs = a;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, nvfp4::gemv_tma_rv_kernel<1, false, false, true>,
+                                         &cfg) == cudaSuccess &&
+          n > 0)
+        d.cluster_cap[occ - 1][S] = n;
+      else
+        cudaGetLastError();
+    }
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
@@ -420,6 +459,28 @@ TmaLayout tma_layout(bool rv, int64_t K, int64_t TR, int64_t NS, int64_t rows_ca
   return t;
 }
 
+// Consumer warps for the register-vector variant: they must divide the K-segment count (NSW = 1
+// or 2 segments per warp) or be a multiple of it.  Returns 0 if no such count fits.
+int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw, int64_t max_warps = 16) {
+  auto ok = [&](int64_t w) -> bool {
+    if (w < 1 || w > max_warps) return false;
+    if (nseg >= w) {
+      if (nseg % w || nseg / w > 2) return false;
+      *nsw = nseg / w;
+      return true;
+    }
+    if (w % nseg) return false;
+    *nsw = 1;
+    return true;
+  };
+  if (forced) return ok(forced) ? forced : 0;
+  // preference from sweeps: 12 warps when the mapping allows, else 8, then the nearest counts
+  // (16 would need <= 60 registers per thread for two CTAs per SM)
+  for (int64_t w : {12, 8, 7, 6, 14, 10, 9, 5, 4, 11, 13, 3, 2, 1, 15, 16})
+    if (ok(w)) return w;
+  return 0;
+}
+
 // Small calls: the register-vector ring on a grid sized by the bytes of the call, with K split
 // over a cluster only when a CTA would otherwise hold more than 32 segments.  Sweeps on GB300 of
 // K = 256 .. 65536 and M x L = 16 .. 2400 (us per call, early weights, graphs of 1000 calls):
@@ -433,8 +494,9 @@ TmaLayout tma_layout(bool rv, int64_t K, int64_t TR, int64_t NS, int64_t rows_ca
 //   - K = 32768 runs unsplit on at most 152 CTAs (1000 rows: 6.26 us, 8.05 on 304 CTAs, 6.60
 //     split in two); at K = 65536
 //     four slices of 16384 win (512 rows: 6.99 us on 57 x 4 CTAs, 7.32 with two slices);
-//   - clusters of 4 and 8 CTAs fit only about 3/4 of the 304 CTA slots at once (57 x 4 and
-//     28 x 8 run in one wave, 76 x 4 and 38 x 8 take twice as long), so split grids stop there.
+//   - clusters of 4 and 8 CTAs fit only 74 x 4 and 36 x 8 of the 304 CTA slots at once (57 x 4
+//     and 28 x 8 run in one wave, 76 x 4 and 38 x 8 take twice as long), so split grids stop at
+//     3/4 of the slots and at the clusters resident at the slice's CTAs per SM.
 // The byte thresholds scale with the SM count (10 KB and 85 KB per SM).  Sets *S (1: unsplit) and
 // *P (CTAs per batch); *S = 0 when no split fits the segment count.
 constexpr int64_t kSmallCallBytesPerSm = 10 * 1024;
@@ -462,7 +524,13 @@ void small_call_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, int64
   int64_t G = B < kSmallCallBytesPerSm * d.sms ? slots / 4
               : B < kMidCallBytesPerSm * d.sms ? slots / 2
                                                 : slots;  // CTAs of the launch
-  if (S > 1) G = std::min<int64_t>(G, slots * 3 / 4);
+  if (S > 1) {
+    // no more clusters than the GPU holds at once, at the CTAs per SM the slice's warps allow
+    int64_t nsw = 1;
+    const int64_t W = rv_warps(nseg / S, 0, &nsw);
+    const int occ = W ? (int)std::min<int64_t>(2, rv_ctas_by_regs(d, W, nsw)) : 1;
+    G = std::min<int64_t>({G, slots * 3 / 4, clusters_resident(d, occ, S) * S});
+  }
   // more than 16 segments unsplit (K up to 32768): one CTA per SM (1000 x 32768: 6.26 us on 152
   // CTAs, 8.05 on 304)
   if (S == 1 && nseg > 16) G = std::min<int64_t>(G, slots / 2);
@@ -474,28 +542,6 @@ void small_call_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, int64
 // ring that leaves room for only one CTA per SM was much slower.
 constexpr int64_t kTmaStageTarget = 57344;  // stage bytes (A + sfa rows) the planner aims for
 constexpr int64_t kTmaSmallStage = 24576;   // stages below this get up to 4 ring slots
-
-// Consumer warps for the register-vector variant: they must divide the K-segment count (NSW = 1
-// or 2 segments per warp) or be a multiple of it.  Returns 0 if no such count fits.
-int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw, int64_t max_warps = 16) {
-  auto ok = [&](int64_t w) -> bool {
-    if (w < 1 || w > max_warps) return false;
-    if (nseg >= w) {
-      if (nseg % w || nseg / w > 2) return false;
-      *nsw = nseg / w;
-      return true;
-    }
-    if (w % nseg) return false;
-    *nsw = 1;
-    return true;
-  };
-  if (forced) return ok(forced) ? forced : 0;
-  // preference from sweeps: 12 warps when the mapping allows, else 8, then the nearest counts
-  // (16 would need <= 60 registers per thread for two CTAs per SM)
-  for (int64_t w : {12, 8, 7, 6, 14, 10, 9, 5, 4, 11, 13, 3, 2, 1, 15, 16})
-    if (ok(w)) return w;
-  return 0;
-}
 
 // ua: operands not 16-byte aligned (register-vector kernel only; stages carry 32 bytes of slack).
 // S: K slices over a cluster of S CTAs (register-vector kernel, aligned operands, S dividing the
@@ -607,7 +653,11 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       // last wave at least 1% better.  Measured on GB300: a grid of 0.84 waves ran at 77% of the
       // bandwidth of four exact waves, and an 80-batch call (5.29 GB) ran at 2.1x the stream
       // kernel's rate.
-      const int64_t P0 = std::min<int64_t>(M, std::max<int64_t>(1, slots_sm / LS));
+      // A wave is the CTA slots, or under split K the clusters the GPCs hold at once (fewer than
+      // the slots past S = 2); P CTAs (clusters) per batch take P * L of it.
+      const int64_t wave = S > 1 ? clusters_resident(d, occ, S) : slots_sm;
+      const int64_t per_p = S > 1 ? L : LS;
+      const int64_t P0 = std::min<int64_t>(M, std::max<int64_t>(1, wave / per_p));
       // the smallest P >= P0 whose partial sums and two-stage ring fit: more CTAs per batch means
       // fewer rows per CTA, so whether a P fits is monotone in P (doubling, then bisection)
       int64_t P_fit = P0, tr = 0, ns = 0;
@@ -623,12 +673,11 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
         }
         P_fit = hi;
       }
-      // (split K serves few rows: one wave of row ranges, no search over larger grids)
-      const int64_t P_hi = S > 1 ? P_fit : std::min<int64_t>(M, P_fit + 8 * P0 + 8);
+      const int64_t P_hi = std::min<int64_t>(M, P_fit + 8 * P0 + 8);
       double best_fill = -1.0;
       for (int64_t p = P_fit; p <= P_hi; ++p) {
-        const int64_t grid = p * LS;
-        const double fill = (double)grid / (double)(ceil_div(grid, slots_sm) * slots_sm);
+        const int64_t grid = p * per_p;
+        const double fill = (double)grid / (double)(ceil_div(grid, wave) * wave);
         if (fill <= best_fill + 0.01) continue;
         if (!shape(p, budget, &tr, &ns)) continue;
         P = p;
@@ -782,9 +831,15 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
         // 4096 x 32768 x 4 49.39 -> 46.05.  Where the halves take one-segment warps (K of 20 to 24
         // segments) the split lost (8192 x 24576 x 1: 19.41 unsplit, 21.21 split).
         // Beyond 32 segments no warp mapping holds the whole vector: split K over the smallest
-        // cluster whose slices it holds (two for K up to 65536).  Against the shared-memory-vector
-        // kernel these shapes used to take: 8192 x 40960 x 1 60.8 -> 38.2 us, 8192 x 65536 x 1
-        // 169.8 -> 56.9 us.
+        // cluster whose slices are at most 24 segments (12 warps of two), else the smallest whose
+        // slices fit.  Slices of 26-32 segments (13-16 warps of two, one CTA per SM) streamed
+        // 5-15% slower than smaller slices at two CTAs per SM.  Sweep on GB300, 8192 rows, grids
+        // of the resident clusters (us per call, early weights; slices in brackets): K = 36-48
+        // segments take 2 (48: 35.3 us, 95% of the copy peak), 52 4 (45.9; 47.4 on 2), 64 4
+        // (47.8; 52.0 on 2), 96 4 (68.7; 82.7 on 3), 112 7 (88.7; 95.1 on 4), 128 8 (99.7; 103.0
+        // on 4); 60 and 72 segments lose 4-5% against the best (2 and 4 slices).  The
+        // shared-memory-vector kernel these shapes used to take ran 8192 x 40960 x 1 in 60.8 us
+        // (32.7 now) and 8192 x 65536 x 1 in 169.8.
         if (mat16 && f.k_slices == 0 && st != NVFP4_OK) {
           const int64_t nseg = ceil_div(K, nvfp4::kStep);
           int64_t nsw1 = 1, nsw2 = 1;
@@ -794,8 +849,11 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
             const int64_t W2 = rv_warps(nseg / 2, f.warps_per_cta, &nsw2);
             if (W2 && nsw2 == 2 && rv_ctas_by_regs(d, W2, nsw2) >= 2) S = 2;
           } else if (!W1) {
-            for (int64_t s2 = 2; s2 <= nvfp4::kTmaMaxClusterK && !S; ++s2)
-              if (nseg % s2 == 0 && rv_warps(nseg / s2, f.warps_per_cta, &nsw2)) S = s2;
+            for (int64_t most : {24, 32})
+              for (int64_t s2 = 2; s2 <= nvfp4::kTmaMaxClusterK && !S; ++s2)
+                if (nseg % s2 == 0 && nseg / s2 <= most &&
+                    rv_warps(nseg / s2, f.warps_per_cta, &nsw2))
+                  S = s2;
           }
           if (S && plan_tma(d, M, K, L, f, true, pl, false, S) == NVFP4_OK)
             st = NVFP4_OK;

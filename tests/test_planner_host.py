@@ -125,13 +125,49 @@ def test_wide_k_splits_over_a_cluster_of_two():
         assert p["warps_per_cta"] == K // 4096, (M, K, p)
 
 
-@pytest.mark.parametrize("K,S", [(40960, 2), (65536, 2), (98304, 3), (131072, 4), (262144, 8)])
-def test_huge_k_splits_into_the_fewest_slices(K, S):
+# Thread-block clusters of S CTAs a GB300 holds at once, at one and at two CTAs per SM (the
+# occupancy query's answers on a 152-SM GB300; a cluster's CTAs share one GPC)
+CLUSTERS_RESIDENT = {1: {2: 76, 3: 46, 4: 36, 5: 28, 6: 23, 7: 15, 8: 15},
+                     2: {2: 152, 3: 97, 4: 74, 5: 58, 6: 46, 7: 38, 8: 36}}
+
+
+def _ctas_per_sm_by_regs(p):
+    """CTAs per SM the register file holds: 96 (two segments a warp) or 72 (one) registers a
+    thread, a quarter of the SM's 64 K registers per scheduler."""
+    per_scheduler = 16384 // ((96 if p["k_split"] == 2 else 72) * 32)
+    return max(1, 4 * per_scheduler // (p["warps_per_cta"] + 1))
+
+
+def test_split_grids_fit_the_resident_clusters():
+    """Every automatic split-K plan launches at most the clusters the GPU holds at once (small
+    calls fewer, by their bytes), or, where the rows do not fit one wave's CTAs, waves at least 95%
+    full."""
+    n = 0
+    for nseg in range(28, 129):
+        for M, L in ((8192, 1), (2048, 4), (512, 1), (100000, 1)):
+            p = plan(M, nseg * 1024, L, forced={"flags": 1})
+            if p["k_slices"] < 2:
+                continue
+            n += 1
+            occ = min(2, _ctas_per_sm_by_regs(p))
+            cap = CLUSTERS_RESIDENT[occ][p["k_slices"]]
+            grid = p["ctas_per_batch"] * L
+            assert grid <= cap or _fill(grid, cap) >= 0.95, (M, nseg, L, p)
+    assert n > 100
+
+
+@pytest.mark.parametrize("K,S", [(36864, 2), (49152, 2), (53248, 4), (65536, 4), (98304, 4),
+                                 (114688, 7), (131072, 8), (262144, 8), (33792, 3)])
+def test_huge_k_splits_into_slices_of_at_most_24_segments(K, S):
     """Past 32 segments no single CTA holds the vector slice: K splits over the fewest CTAs of a
-    cluster (at most 8) that divide the segments into slices of at most 32."""
+    cluster (at most 8) that divide the segments into slices of at most 24 (12 warps of two
+    segments), else of at most 32; the grid is the clusters the GPU holds at once."""
     p = plan(8192, K, 1, forced={"flags": 1})
     assert p["kernel"] == KERNEL_TMA_RV and p["k_slices"] == S, p
-    assert -(-K // 1024) // S <= 32
+    nseg = -(-K // 1024)
+    assert nseg // S <= (24 if any(nseg % s == 0 and nseg // s <= 24 for s in range(2, 9)) else 32)
+    occ = min(2, _ctas_per_sm_by_regs(p))
+    assert p["ctas_per_batch"] == min(CLUSTERS_RESIDENT[occ][S], 8192)
 
 
 def _small_call_grid(M, K, L, slots=304):

@@ -3,7 +3,8 @@ k_slices > 1), through the C ABI, against the oracle.
 
 Few output rows (M * L far below 8 rows per CTA slot) with long K: each cluster of S CTAs shares a
 row range, CTA z streams K slice z and the partial sums meet in the owner CTA's shared memory.
-Covered: the automatic plan on M * L in {16, 64, 128, 512} at K = 16384 and 65536, forced slice
+Covered: the automatic plan on M * L in {16, 64, 128, 512} at K = 16384 and 65536, the automatic
+plan on wide K (24576 to 131072) with many rows, forced slice
 counts (2, 3, 4, 7, 8; a last slice shorter than the others), batches, one row range per batch,
 tile and ring shapes, the launch flags (bit-identical with and without early weights),
 determinism, NaN pre-fill and guard bands, the grouped, small-N and bf16-vector entry points on
@@ -84,6 +85,27 @@ def test_automatic_plan_for_few_rows(pkg, shape):
     c_ew = run(pkg, w, {"flags": 1})
     assert np.array_equal(c.view(np.uint16), c_ew.view(np.uint16)), "early weights changed bits"
     assert np.array_equal(run(pkg, w).view(np.uint16), c.view(np.uint16)), "not deterministic"
+
+
+# (M, K, L) -> K slices of the automatic plan: wide K on enough rows for the full grid
+WIDE_K = {(2432, 24576, 1): 1, (2560, 28672, 1): 2, (2560, 33792, 1): 3, (2560, 36864, 1): 2,
+          (2560, 53248, 1): 4, (1280, 65536, 2): 4, (2560, 98304, 1): 4, (2560, 114688, 1): 7,
+          (2560, 131072, 1): 8}
+
+
+@pytest.mark.parametrize("shape", list(WIDE_K), ids=lambda s: "x".join(map(str, s)))
+def test_automatic_plan_for_wide_k(pkg, shape):
+    """Wide K on many rows: one CTA per SM where the registers hold no more (24576), split over
+    clusters of two for 28 segments, past 32 segments over the fewest CTAs whose slices are at most
+    24 segments; grids of the clusters the GPU holds at once."""
+    M, K, L = shape
+    w = small(M, K, L, seed=11)
+    p = pkg.nvfp4_gemv_plan(M, K, L)
+    assert p.kernel == TMA_RV and max(1, p.k_slices) == WIDE_K[shape], p
+    c = run(pkg, w, guard=64)
+    check(w, c, f"{shape} auto {p}")
+    c_ew = run(pkg, w, {"flags": 1})
+    assert np.array_equal(c.view(np.uint16), c_ew.view(np.uint16)), "early weights changed bits"
 
 
 FORCED = [
