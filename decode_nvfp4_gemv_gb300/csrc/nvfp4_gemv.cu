@@ -435,15 +435,22 @@ struct TmaLayout {
   int64_t rs_a, rs_s;  // bytes between the rows of a stage (A, sfa)
 };
 
+// Split K into S slices of whole 1024-element segments: ceil(nseg / S) each, the last slice the
+// rest (shorter when S does not divide nseg); every slice must hold at least one segment.
+int64_t slice_segs(int64_t nseg, int64_t S) { return S > 1 ? ceil_div(nseg, S) : nseg; }
+bool slices_valid(int64_t nseg, int64_t S) {
+  return S >= 2 && S <= nvfp4::kTmaMaxClusterK && (S - 1) * ceil_div(nseg, S) < nseg;
+}
+
 // ua: operands not 16-byte aligned; a stage then holds each tile's A and sfa bytes from the
 // 16-byte boundary at or below their first byte, plus the 16 bytes a lane's second aligned read
 // may reach past them: 32 bytes more for each.  S > 1: K split over a cluster of S CTAs; a stage
-// holds one slice of each row (nseg / S segments), and the owner's partial sums of the cluster
+// holds one slice of each row (slice_segs segments), and the owner's partial sums of the cluster
 // (S x ceil(rows_cap / S) floats) follow the per-slot partials.
 TmaLayout tma_layout(bool rv, int64_t K, int64_t TR, int64_t NS, int64_t rows_cap, int64_t slots,
                      bool ua = false, int64_t S = 1) {
   TmaLayout t;
-  const int64_t seg_s = S > 1 ? ceil_div(K, nvfp4::kStep) / S : 0;
+  const int64_t seg_s = S > 1 ? slice_segs(ceil_div(K, nvfp4::kStep), S) : 0;
   t.rs_a = S > 1 ? seg_s * (nvfp4::kStep / 2) : K / 2;
   t.rs_s = S > 1 ? seg_s * (nvfp4::kStep / 16) : K / 16;
   t.b_off = nvfp4::kTmaHeaderBytes;
@@ -459,8 +466,11 @@ TmaLayout tma_layout(bool rv, int64_t K, int64_t TR, int64_t NS, int64_t rows_ca
   return t;
 }
 
-// Consumer warps for the register-vector variant: they must divide the K-segment count (NSW = 1
-// or 2 segments per warp) or be a multiple of it.  Returns 0 if no such count fits.
+// Consumer warps for the register-vector variant: they divide the K-segment count (NSW = 1 or 2
+// segments per warp) or are a multiple of it; an automatic choice for a count with no such
+// divisor (an odd count past 16) takes warps of two segments with the last warp's second segment
+// past the end (idle: the kernel skips segments that start at or past K).  Returns 0 if nothing
+// fits.
 int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw, int64_t max_warps = 16) {
   auto ok = [&](int64_t w) -> bool {
     if (w < 1 || w > max_warps) return false;
@@ -478,6 +488,11 @@ int64_t rv_warps(int64_t nseg, int64_t forced, int64_t* nsw, int64_t max_warps =
   // (16 would need <= 60 registers per thread for two CTAs per SM)
   for (int64_t w : {12, 8, 7, 6, 14, 10, 9, 5, 4, 11, 13, 3, 2, 1, 15, 16})
     if (ok(w)) return w;
+  const int64_t w = (nseg + 1) / 2;
+  if (nseg > 2 && w <= max_warps) {
+    *nsw = 2;
+    return w;
+  }
   return 0;
 }
 
@@ -515,8 +530,10 @@ void small_call_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, int64
   int64_t S = 1;
   if (nseg > 32) {
     S = 0;
-    for (int64_t s = 2; s <= nvfp4::kTmaMaxClusterK && !S; ++s)
-      if (nseg % s == 0 && nseg / s <= 16) S = s;
+    for (bool exact : {true, false})  // slices that divide the segments first
+      for (int64_t s = 2; s <= nvfp4::kTmaMaxClusterK && !S; ++s)
+        if (slices_valid(nseg, s) && (!exact || nseg % s == 0) && slice_segs(nseg, s) <= 16)
+          S = s;
   }
   *S_out = S;
   *P_out = 0;
@@ -527,7 +544,7 @@ void small_call_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, int64
   if (S > 1) {
     // no more clusters than the GPU holds at once, at the CTAs per SM the slice's warps allow
     int64_t nsw = 1;
-    const int64_t W = rv_warps(nseg / S, 0, &nsw);
+    const int64_t W = rv_warps(slice_segs(nseg, S), 0, &nsw);
     const int occ = W ? (int)std::min<int64_t>(2, rv_ctas_by_regs(d, W, nsw)) : 1;
     G = std::min<int64_t>({G, slots * 3 / 4, clusters_resident(d, occ, S) * S});
   }
@@ -544,8 +561,8 @@ constexpr int64_t kTmaStageTarget = 57344;  // stage bytes (A + sfa rows) the pl
 constexpr int64_t kTmaSmallStage = 24576;   // stages below this get up to 4 ring slots
 
 // ua: operands not 16-byte aligned (register-vector kernel only; stages carry 32 bytes of slack).
-// S: K slices over a cluster of S CTAs (register-vector kernel, aligned operands, S dividing the
-// 1024-element segment count, at most kTmaMaxClusterK).
+// S: K slices over a cluster of S CTAs (register-vector kernel, aligned operands, at most
+// kTmaMaxClusterK slices, each with at least one 1024-element segment).
 int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_plan& f, bool rv,
              nvfp4_plan* pl, bool ua = false, int64_t S = 1) {
   if (ua && !rv)
@@ -557,10 +574,10 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   if (S > 1) {
     if (ua)
       return fail(NVFP4_ERR_MISALIGNED, "split K over a cluster needs 16-byte aligned A and sfa");
-    if (!rv || S > nvfp4::kTmaMaxClusterK || ceil_div(K, nvfp4::kStep) % S != 0)
+    if (!rv || !slices_valid(ceil_div(K, nvfp4::kStep), S))
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
-                  "split K: the register-vector kernel, k_slices <= %d dividing the %lld "
-                  "1024-element segments (k_slices=%lld)",
+                  "split K: the register-vector kernel, k_slices <= %d, each slice at least one "
+                  "of the %lld 1024-element segments (k_slices=%lld)",
                   nvfp4::kTmaMaxClusterK, (long long)ceil_div(K, nvfp4::kStep), (long long)S);
   }
   if (f.warps_per_cta > 16)
@@ -571,7 +588,7 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       f.stages > nvfp4::kTmaMaxStages)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "tile_rows must be 1..256, stages 2..%d",
                 nvfp4::kTmaMaxStages);
-  const int64_t nseg = ceil_div(K, nvfp4::kStep) / S;  // segments of one CTA's slice
+  const int64_t nseg = slice_segs(ceil_div(K, nvfp4::kStep), S);  // segments of a CTA's slice
   int64_t Wc = f.warps_per_cta ? f.warps_per_cta : 8, nsw = 1;
   if (rv) {
     // the unaligned form needs more registers (about 88-96 a thread): at most 8 consumer warps
@@ -830,29 +847,30 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
         // 25.87 -> 23.74, 4096 x 28672 x 4 47.28 -> 42.56, 8192 x 32768 x 1 27.01 -> 25.80,
         // 4096 x 32768 x 4 49.39 -> 46.05.  Where the halves take one-segment warps (K of 20 to 24
         // segments) the split lost (8192 x 24576 x 1: 19.41 unsplit, 21.21 split).
-        // Beyond 32 segments no warp mapping holds the whole vector: split K over the smallest
-        // cluster whose slices are at most 24 segments (12 warps of two), else the smallest whose
-        // slices fit.  Slices of 26-32 segments (13-16 warps of two, one CTA per SM) streamed
-        // 5-15% slower than smaller slices at two CTAs per SM.  Sweep on GB300, 8192 rows, grids
-        // of the resident clusters (us per call, early weights; slices in brackets): K = 36-48
-        // segments take 2 (48: 35.3 us, 95% of the copy peak), 52 4 (45.9; 47.4 on 2), 64 4
-        // (47.8; 52.0 on 2), 96 4 (68.7; 82.7 on 3), 112 7 (88.7; 95.1 on 4), 128 8 (99.7; 103.0
-        // on 4); 60 and 72 segments lose 4-5% against the best (2 and 4 slices).  The
-        // shared-memory-vector kernel these shapes used to take ran 8192 x 40960 x 1 in 60.8 us
-        // (32.7 now) and 8192 x 65536 x 1 in 169.8.
+        // Beyond 32 segments no warp mapping holds the whole vector: split K over 2, 4 or 8 CTAs
+        // (the first whose slices are at most 24 segments, 12 warps of two), else 3, 5, 6 or 7,
+        // else the first whose slices fit (at most 32); slices are ceil(segments / S) each, the
+        // last the rest.  Slices of 26-32 segments (13-16 warps of two, one CTA per SM) streamed
+        // 5-15% slower than smaller ones, and clusters of 3, 5 and 6 CTAs were 5-20% slower than
+        // 2 or 4 on the same K.  Sweep on GB300, 8192 rows, grids of the resident clusters (us
+        // per call, early weights): K of 33-48 segments take 2 (33: 27.0, 30.5 on 3; 48: 35.3,
+        // 95% of the copy peak), 52-96 take 4 (53: 43.0, 50.9 on 3; 64: 47.8, 52.0 on 2; 67:
+        // 50.5, 55.4 on 3; 96: 68.7, 82.7 on 3), 128 takes 8 (99.7, 103.0 on 4); 60 and 112 lose
+        // 4-5% against 2 and 7.  The shared-memory-vector kernel these shapes used to take ran
+        // 8192 x 40960 x 1 in 60.8 us (32.7 now) and 8192 x 65536 x 1 in 169.8.
         if (mat16 && f.k_slices == 0 && st != NVFP4_OK) {
           const int64_t nseg = ceil_div(K, nvfp4::kStep);
           int64_t nsw1 = 1, nsw2 = 1;
           const int64_t W1 = rv_warps(nseg, f.warps_per_cta, &nsw1);
           int64_t S = 0;
-          if (W1 && rv_ctas_by_regs(d, W1, nsw1) < 2 && nseg % 2 == 0) {
-            const int64_t W2 = rv_warps(nseg / 2, f.warps_per_cta, &nsw2);
+          if (W1 && rv_ctas_by_regs(d, W1, nsw1) < 2) {
+            const int64_t W2 = rv_warps(slice_segs(nseg, 2), f.warps_per_cta, &nsw2);
             if (W2 && nsw2 == 2 && rv_ctas_by_regs(d, W2, nsw2) >= 2) S = 2;
           } else if (!W1) {
             for (int64_t most : {24, 32})
-              for (int64_t s2 = 2; s2 <= nvfp4::kTmaMaxClusterK && !S; ++s2)
-                if (nseg % s2 == 0 && nseg / s2 <= most &&
-                    rv_warps(nseg / s2, f.warps_per_cta, &nsw2))
+              for (int64_t s2 : {2, 4, 8, 3, 5, 6, 7})
+                if (!S && slices_valid(nseg, s2) && slice_segs(nseg, s2) <= most &&
+                    rv_warps(slice_segs(nseg, s2), f.warps_per_cta, &nsw2))
                   S = s2;
           }
           if (S && plan_tma(d, M, K, L, f, true, pl, false, S) == NVFP4_OK)
@@ -1119,10 +1137,10 @@ int launch(const DeviceInfo& d, const nvfp4_plan& pl, const uint8_t* A, const ui
     const int64_t S = pl.k_slices > 1 ? pl.k_slices : 1;
     if (S > 1 && (!rv || ua))
       return fail(NVFP4_ERR_UNSUPPORTED_SHAPE, "split K needs the aligned register-vector kernel");
-    if (S > 1) a.slots = (int32_t)std::min<int64_t>(pl.warps_per_cta, nseg / S);
+    if (S > 1) a.slots = (int32_t)std::min<int64_t>(pl.warps_per_cta, slice_segs(nseg, S));
     const TmaLayout t = tma_layout(rv, K, pl.tile_rows, pl.stages, a.rows_cap, a.slots, ua, S);
     a.k_slices = (int32_t)S;
-    a.slice_segs = (int32_t)(nseg / S);
+    a.slice_segs = (int32_t)slice_segs(nseg, S);
     a.rs_a = (uint32_t)t.rs_a;
     a.rs_s = (uint32_t)t.rs_s;
     a.red_off = (uint32_t)t.red_off;

@@ -89,14 +89,17 @@ typedef enum nvfp4_kernel {
   NVFP4_KERNEL_TMA = 3,     /* row tiles streamed into a shared-memory ring by bulk async copies
                                (TMA) and mbarriers, vector in shared memory; needs K % 256 == 0 */
   NVFP4_KERNEL_TMA_RV = 4,  /* as TMA with each consumer warp's vector slice held in registers;
-                               needs K % 256 == 0 and the warp count to divide the number of
-                               1024-element K segments (or be a multiple of it).  A vector (b,
+                               needs K % 256 == 0 and a forced warp count to divide the number of
+                               1024-element K segments (or be a multiple of it); the automatic
+                               count for an odd number past 16 takes warps of two segments with
+                               one idle.  A vector (b,
                                sfb) not 16-byte aligned is loaded with shifted loads; A or sfa not
                                16-byte aligned take its unaligned form (bulk copies of each
                                tile's aligned interior, the buffers' first and last partial
                                16 bytes copied one by one, shifted out of shared memory; at most
-                               8 consumer warps).  With k_slices = S > 1 (A and sfa aligned, S
-                               dividing the 1024-element segment count, S <= 8) K is split over a
+                               8 consumer warps).  With k_slices = S > 1 (A and sfa aligned,
+                               S <= 8; slices of ceil(segments / S) 1024-element segments, the
+                               last one the rest and not empty) K is split over a
                                thread-block cluster of S CTAs that reduce their partial sums in
                                distributed shared memory, in slice order (no workspace) */
   NVFP4_KERNEL_TC = 5,      /* tensor cores (tcgen05.mma kind::mxf4nvf4, block scales applied by
@@ -155,10 +158,12 @@ typedef struct nvfp4_plan {
   int32_t stages;          /* TMA*: ring stages (2 .. 8); TC: 2 .. 6 stages of 256 elements */
   int32_t flags;           /* NVFP4_FLAG_* (honoured by the automatic plan too) */
   int32_t k_slices;        /* TMA_RV: K slices over a thread-block cluster (0 or 1: no split;
-                              2 .. 8 dividing the 1024-element segment count).  The automatic
-                              plan splits K when one wave of CTA slots would give each CTA fewer
-                              than 8 rows; ctas_per_batch then counts row ranges (the grid is
-                              ctas_per_batch x L x k_slices CTAs) */
+                              2 .. 8, each slice at least one 1024-element segment).  The
+                              automatic plan splits K when one wave of CTA slots would give each
+                              CTA fewer than 8 rows, when K is too long for one CTA's registers
+                              (past 32 segments) and for 27-32 segments; ctas_per_batch then
+                              counts row ranges (the grid is ctas_per_batch x L x k_slices CTAs,
+                              at most the clusters the GPU holds at once per wave) */
 } nvfp4_plan;
 
 /*

@@ -175,7 +175,8 @@ def test_shift_kernel_grouped_forms(pkg):
 
 
 RING_SHAPES = [(2432, 2048, 1), (300, 4096, 9), (97, 1024, 3), (1000, 16384, 1),
-               (600, 4352, 2)]                                # a partial last segment
+               (600, 4352, 2),                                # a partial last segment
+               (400, 11264, 2)]                               # 11 segments: 6 warps, one idle
 
 
 @pytest.mark.parametrize("shape", RING_SHAPES, ids=[f"{m}x{k}x{l}" for m, k, l in RING_SHAPES])
@@ -212,7 +213,9 @@ def test_unaligned_operands_on_the_tma_ring(pkg, shape, offsets):
 
 
 VEC_SHAPES = [(2432, 2048, 1), (300, 4096, 9), (64, 65536, 1), (40, 16384, 3),
-              (700, 2304, 2), (1500, 1280, 1)]                # partial last segments
+              (700, 2304, 2), (1500, 1280, 1),                # partial last segments
+              (2560, 17408, 1),                               # 17 segments: 9 warps, one idle
+              (700, 37888, 1)]                                # 37: slices of 13, 13 and 11
 
 
 @pytest.mark.parametrize("shape", VEC_SHAPES, ids=[f"{m}x{k}x{l}" for m, k, l in VEC_SHAPES])

@@ -115,6 +115,21 @@ def test_register_capped_rings_take_one_wave():
         assert p["k_split"] == 2 and p["warps_per_cta"] == K // 2048, (M, K, L, p)
 
 
+def test_odd_segment_counts_take_warps_of_two_with_one_idle():
+    """An odd segment count past 16 has no warp count that divides it: ceil(segments / 2) warps of
+    two segments, the last warp's second one idle (unsplit, or over clusters of two)."""
+    for nseg in (17, 19, 21, 23, 25, 29):
+        p = plan(8192, nseg * 1024, 1, forced={"flags": 1})
+        assert p["kernel"] == KERNEL_TMA_RV and p["k_slices"] == 1, (nseg, p)
+        assert p["warps_per_cta"] == (nseg + 1) // 2 and p["k_split"] == 2, (nseg, p)
+    for nseg in (27, 31):
+        p = plan(8192, nseg * 1024, 1, forced={"flags": 1})
+        assert p["k_slices"] == 2 and p["warps_per_cta"] == (nseg + 3) // 4, (nseg, p)
+    # a forced warp count must still divide the segments (or be a multiple of them)
+    assert status_of(8192, 17 * 1024, 1, forced={"kernel": KERNEL_TMA_RV, "warps_per_cta": 9}) \
+        == UNSUPPORTED
+
+
 def test_wide_k_splits_over_a_cluster_of_two():
     """K of 28-32 segments: split over a cluster of two CTAs, each slice on 7-8 warps of two
     segments, two clusters' CTAs per SM -- instead of one 14-16 warp CTA per SM."""
@@ -157,15 +172,20 @@ def test_split_grids_fit_the_resident_clusters():
 
 
 @pytest.mark.parametrize("K,S", [(36864, 2), (49152, 2), (53248, 4), (65536, 4), (98304, 4),
-                                 (114688, 7), (131072, 8), (262144, 8), (33792, 3)])
+                                 (114688, 8), (131072, 8), (262144, 8), (33792, 2), (37888, 2),
+                                 (52224, 4), (54272, 4), (99328, 8), (61440, 4)])
 def test_huge_k_splits_into_slices_of_at_most_24_segments(K, S):
-    """Past 32 segments no single CTA holds the vector slice: K splits over the fewest CTAs of a
-    cluster (at most 8) that divide the segments into slices of at most 24 (12 warps of two
-    segments), else of at most 32; the grid is the clusters the GPU holds at once."""
+    """Past 32 segments no single CTA holds the vector slice: K splits over 2, 4 or 8 CTAs of a
+    cluster, the first whose slices (ceil(segments / S) each, the last the rest) are at most 24
+    segments (12 warps of two), else over 3, 5, 6 or 7, else the first whose slices are at most 32.
+    The grid is the clusters the GPU holds at once."""
     p = plan(8192, K, 1, forced={"flags": 1})
     assert p["kernel"] == KERNEL_TMA_RV and p["k_slices"] == S, p
     nseg = -(-K // 1024)
-    assert nseg // S <= (24 if any(nseg % s == 0 and nseg // s <= 24 for s in range(2, 9)) else 32)
+    sl = lambda s: -(-nseg // s)
+    order = [s for most in (24, 32) for s in (2, 4, 8, 3, 5, 6, 7)
+             if (s - 1) * sl(s) < nseg and sl(s) <= most]
+    assert S == order[0]
     occ = min(2, _ctas_per_sm_by_regs(p))
     assert p["ctas_per_batch"] == min(CLUSTERS_RESIDENT[occ][S], 8192)
 
@@ -220,10 +240,12 @@ def test_forced_k_slices():
     assert p["k_slices"] == 2 and p["kernel"] == KERNEL_TMA_RV
     assert plan(64, 16384, 1, forced={"kernel": KERNEL_TMA_RV})["k_slices"] == 1
     assert plan(7168, 16384, 1)["k_slices"] == 1
-    for forced in ({"kernel": KERNEL_TMA_RV, "k_slices": 3}, {"kernel": KERNEL_TMA_RV, "k_slices": 9},
+    for forced in ({"kernel": KERNEL_TMA_RV, "k_slices": 7}, {"kernel": KERNEL_TMA_RV, "k_slices": 9},
                    {"kernel": KERNEL_STREAM, "k_slices": 2}, {"kernel": KERNEL_TMA, "k_slices": 2},
                    {"kernel": KERNEL_TMA_RV, "k_slices": -1}):
         assert status_of(64, 16384, 1, forced=forced) == UNSUPPORTED, forced
+    # slices need not divide the segments: 16 segments in three slices of 6, 6 and 4
+    assert plan(64, 16384, 1, forced={"kernel": KERNEL_TMA_RV, "k_slices": 3})["k_slices"] == 3
 
 
 def test_planning_is_deterministic_and_forced_plans_are_echoed():

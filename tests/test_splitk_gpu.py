@@ -88,9 +88,12 @@ def test_automatic_plan_for_few_rows(pkg, shape):
 
 
 # (M, K, L) -> K slices of the automatic plan: wide K on enough rows for the full grid
-WIDE_K = {(2432, 24576, 1): 1, (2560, 28672, 1): 2, (2560, 33792, 1): 3, (2560, 36864, 1): 2,
-          (2560, 53248, 1): 4, (1280, 65536, 2): 4, (2560, 98304, 1): 4, (2560, 114688, 1): 7,
-          (2560, 131072, 1): 8}
+WIDE_K = {(2432, 24576, 1): 1, (2560, 28672, 1): 2, (2560, 33792, 1): 2, (2560, 36864, 1): 2,
+          (2560, 53248, 1): 4, (1280, 65536, 2): 4, (2560, 98304, 1): 4, (2560, 114688, 1): 8,
+          (2560, 131072, 1): 8,
+          # odd and prime segment counts: warps of two with one idle, slices with a shorter last
+          (2560, 17408, 1): 1, (2560, 25600, 1): 1, (2560, 31744, 1): 2, (2560, 37888, 1): 2,
+          (2560, 61440 + 1024, 1): 4}
 
 
 @pytest.mark.parametrize("shape", list(WIDE_K), ids=lambda s: "x".join(map(str, s)))
@@ -125,6 +128,10 @@ FORCED = [
     (300, 4096, 2, dict(k_slices=2, flags=2)),
     (5, 32768, 1, dict(k_slices=8, flags=1)),                 # more CTAs than rows in a cluster
     (1, 16384, 3, dict(k_slices=8)),
+    (100, 16384, 1, dict(k_slices=3)),                        # slices of 6, 6 and 4 segments
+    (97, 37888, 1, dict(k_slices=2)),                         # 19 + 18: 10 warps, one idle
+    (64, 10240, 2, dict(k_slices=4)),                         # 3, 3, 3 and 1
+    (50, 9472, 1, dict(k_slices=3, flags=1)),                 # 4, 4 and a partial 2
 ]
 
 
@@ -154,10 +161,10 @@ def test_nan_scale_poisons_only_its_row_under_split(pkg):
     assert_parity(c, ref, T, "NaN scale under split K")
 
 
-@pytest.mark.parametrize("plan", [dict(kernel=TMA_RV, k_slices=3), dict(kernel=TMA_RV, k_slices=9),
+@pytest.mark.parametrize("plan", [dict(kernel=TMA_RV, k_slices=7), dict(kernel=TMA_RV, k_slices=9),
                                   dict(kernel=2, k_slices=2), dict(kernel=3, k_slices=2),
                                   dict(kernel=TMA_RV, k_slices=-1)],
-                         ids=["3-does-not-divide-16", "9-too-many", "stream", "smem-vector",
+                         ids=["7-leaves-a-slice-empty", "9-too-many", "stream", "smem-vector",
                               "negative"])
 def test_plans_the_split_cannot_take_are_refused(pkg, plan):
     w = small(64, 16384)
@@ -238,6 +245,30 @@ def test_bf16_vector_on_the_split_kernel(pkg, flags):
     assert np.array_equal(s.cpu().numpy(), sr.ravel()), "sfb_out"
     ref, T = oracle.gemv(w.A, w.sfa, w.g_a, pr, sr, gs, M, K, L)
     assert_parity(c.cpu().numpy(), ref, T, f"bf16 vector, split K, flags {flags}")
+
+
+@pytest.mark.parametrize("flags", [1, 1 | 4], ids=["quantizer-then-gemv", "in-gemv"])
+def test_bf16_vector_with_an_idle_segment(pkg, flags):
+    """17 segments on 9 warps of two, the last warp's second segment idle: the in-GEMV form still
+    writes every segment of the packed vector once."""
+    M, K, L = 2560, 17408, 1
+    w = small(M, K, L, seed=73)
+    x = workloads.normal_bf16(74, "x", K * L).reshape(L, K)
+    gs = float(np.abs(x).max() / 2688.0)
+    pr, sr = Q.quantize_activation(x, gs, "lut")
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16).view(np.int16)
+    b = torch.full((L * K // 2,), 0xA5, dtype=torch.uint8, device="cuda")
+    s = torch.full((L * K // 16,), 0x5A, dtype=torch.uint8, device="cuda")
+    c = torch.full((L, M), float("nan"), dtype=torch.float16, device="cuda")
+    p = pkg.nvfp4_gemv_plan(M, K, L)
+    assert (p.kernel, p.warps_per_cta, p.k_split, max(1, p.k_slices)) == (TMA_RV, 9, 2, 1), p
+    pkg.nvfp4_gemv_batched_bf16(dev(w.A), dev(w.sfa), w.g_a, dev(bits), gs, b, s, c, M, K, L,
+                                plan={"flags": flags})
+    torch.cuda.synchronize()
+    assert np.array_equal(b.cpu().numpy(), pr.ravel()), "b_out"
+    assert np.array_equal(s.cpu().numpy(), sr.ravel()), "sfb_out"
+    ref, T = oracle.gemv(w.A, w.sfa, w.g_a, pr, sr, gs, M, K, L)
+    assert_parity(c.cpu().numpy(), ref, T, f"bf16 vector, 17 segments, flags {flags}")
 
 
 def test_graph_replays_of_split_calls(pkg):
