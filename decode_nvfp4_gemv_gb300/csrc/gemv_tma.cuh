@@ -28,11 +28,12 @@
 //   gemv_tma_kernel        b[l] decoded into shared memory (one f16x2 word per packed byte,
 //                          swizzled as in the stream kernel) and sfb[l] as fp32; item i goes to
 //                          warp i mod W_c.  Any K % 256 == 0 within the shared-memory budget.
-//   gemv_tma_rv_kernel<NSW> when W_c divides the segment count nseg (each warp owns NSW = nseg/W_c
-//                          segments, for every row group) or nseg divides W_c (each warp owns one
-//                          segment and every (W_c/nseg)-th row group): a warp touches the same
-//                          segments in every tile, so it decodes its slice of b into registers once.
-//                          No vector reads in the inner loop, and the ring gets the shared memory.
+//   gemv_tma_rv_kernel<NSW> when W_c NSW >= nseg > W_c (NSW = 1 or 2 segments per warp, for every
+//                          row group; a warp's segments are warp + j W_c, and one that starts past
+//                          K is idle) or nseg divides W_c (each warp owns one segment and every
+//                          (W_c/nseg)-th row group): a warp touches the same segments in every
+//                          tile, so it decodes its slice of b into registers once.  No vector reads
+//                          in the inner loop, and the ring gets the shared memory.
 //
 // Split K over a cluster (register-vector kernel, `CL`).  When the rows of a call are too few to
 // give every CTA slot of one wave enough work, K is cut into S slices of whole 1024-element
@@ -708,7 +709,8 @@ __device__ __forceinline__ void tma_cluster_reduce(const TmaArgs& p, const TmaCt
 }
 
 // ------------------------------------------------------------------------------------------------
-// Vector slice in registers (W_c divides the segment count, or the segment count divides W_c).
+// Vector slice in registers (W_c NSW segment slots cover the segment count, or the segment count
+// divides W_c).
 // QX: the vector is bf16 and is quantized to NVFP4 here (see quantize.cuh); its bytes feed the same
 // decode as packed input would.  CL: split K over a cluster (the CTA's segments are those of its
 // slice; rows of a stage lie rs_a / rs_s bytes apart).  VA: A and sfa aligned, b or sfb not: the
