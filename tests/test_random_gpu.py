@@ -2,7 +2,7 @@
 every output checked against the oracle under the parity tolerance, for the batched GEMV (below),
 the small-N entry point and the grouped form (their own tests at the end).
 
-Each case draws M in [1, 300], K in 16..4096 (multiples of 16, with K % 32, K % 256 and
+Each batched case draws M in [1, 300], K in 16..4096 (multiples of 16, with K % 32, K % 256 and
 K % 1024 each varied), L in [1, 4]; each of A, sfa, b, sfb lands 0 to 15 bytes past a 16-byte
 boundary (aligned half of the time); the plan is automatic or forces a kernel with random fields.
 A forced plan the planner refuses for that shape (UNSUPPORTED_SHAPE or MISALIGNED) is skipped: the
@@ -99,6 +99,50 @@ def test_random_case(pkg, case):
         torch.cuda.synchronize()
         out = c.cpu().numpy()
         what = f"case {case}: M={M} K={K} L={L} offsets={offsets} plan={p}"
+        assert not np.isnan(out).any(), what
+        assert_parity(out, ref, T, what)
+
+
+@pytest.mark.parametrize("case", list(range(40)))
+def test_random_wide_k(pkg, case):
+    """Wide K on the register-vector ring: 17 to 96 segments (odd and prime counts, a partial last
+    segment a quarter of the time), M up to 3000, L up to 2, the vector aligned or not (A aligned,
+    as split K needs); the automatic plan, and forced K slices 2 to 8 (equal slices and a shorter
+    last one; a split that leaves a slice empty or a slice past 32 segments is refused)."""
+    rng = np.random.default_rng(9000 + case)
+    nseg = int(rng.integers(17, 97))
+    K = nseg * 1024 - (256 * int(rng.integers(1, 4)) if rng.random() < 0.25 else 0)
+    M = int(rng.integers(1, 3001))
+    L = int(rng.integers(1, 3))
+    offsets = (0, 0, 0, 0) if rng.random() < 0.5 else \
+        (0, 0, int(rng.integers(0, 16)), int(rng.integers(0, 16)))
+    w = workloads.random_workload(M, K, L, seed=60_000 + case,
+                                  scale_bytes=workloads.pow2_scale_bytes(-4, 3), g_a=0.75,
+                                  g_b=1.25)
+    keep, args = [], []
+    for name, off in zip(("A", "sfa", "b", "sfb"), offsets):
+        v, raw = placed(getattr(w, name), off)
+        keep.append(raw)
+        args.append(v)
+    ref, T = oracle.gemv(w.A, w.sfa, w.g_a, w.b, w.sfb, w.g_b, M, K, L)
+    plans = [None]
+    if rng.random() < 0.5:
+        plans.append({"kernel": 4, "k_slices": int(rng.integers(2, 9)),
+                      "flags": int(rng.choice([0, 1]))})
+    for p in plans:
+        c = torch.full((L, M), float("nan"), dtype=torch.float16, device="cuda")
+        try:
+            pkg.nvfp4_gemv_batched_ex(args[0], args[1], w.g_a, args[2], args[3], w.g_b, c, M, K,
+                                      L, plan=p)
+        except pkg.NVFP4Error as e:
+            # refused: a slice left empty, or slices too long for one CTA's warps
+            assert p is not None and e.status == 3, (p, e)
+            nsl, S = -(-K // 1024), p["k_slices"]
+            assert (S - 1) * -(-nsl // S) >= nsl or -(-nsl // S) > 32, (p, e)
+            continue
+        torch.cuda.synchronize()
+        out = c.cpu().numpy()
+        what = f"wide case {case}: M={M} K={K} L={L} offsets={offsets} plan={p}"
         assert not np.isnan(out).any(), what
         assert_parity(out, ref, T, what)
 
