@@ -271,6 +271,28 @@ def recorded_traffic(workload_name: str):
         return None
 
 
+def headline_workload(args):
+    """The timed workload and its name: a named decode config, or any M x K x L (--shape) drawn
+    like c5 (uniform packed bytes, block scales of powers of two from 2^-3 to 2^2)."""
+    if not args.shape:
+        return workloads.make(args.config), args.config
+    M, K, L = parse_shape(args.shape)
+    name = f"{M}x{K}x{L}"
+    return workloads.random_workload(M, K, L, seed=M + K + L,
+                                     scale_bytes=workloads.pow2_scale_bytes(-3, 2), g_a=0.5,
+                                     g_b=1.0, name=name), name
+
+
+def parse_shape(text):
+    """'MxKxL' (or 'MxK', L = 1) -> (M, K, L); K a positive multiple of 16."""
+    parts = [int(v) for v in text.lower().split("x")]
+    if len(parts) == 2:
+        parts.append(1)
+    if len(parts) != 3 or min(parts) < 1 or parts[1] % 16:
+        raise ValueError(f"--shape wants MxKxL with K a multiple of 16, not {text!r}")
+    return tuple(parts)
+
+
 # ---------------------------------------------------------------------------- our arm
 
 def _device_inputs(w, n_copies, device):
@@ -795,7 +817,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     pkg.load_library()
-    w = workloads.make(args.config)
+    w, name = headline_workload(args)
     bytes_call = w.algorithmic_bytes
     n_copies, l2 = _copies_for(bytes_call, device)
     sets = _device_inputs(w, n_copies, device)
@@ -821,7 +843,7 @@ def run_ours(args):
     per_call_s = seconds / args.steps
     achieved = bytes_call / per_call_s / 1e9
     peak, peak_kind = measured_peak_gbs()
-    traffic = recorded_traffic(args.config)
+    traffic = recorded_traffic(name)
 
     # correctness spot check of the timed launches' last output (NaN would mean an unwritten c)
     assert not torch.isnan(outs[(args.steps - 1) % n_copies]).any().item()
@@ -913,7 +935,7 @@ def run_ours(args):
             "dtype_detail": "e2m1 / e4m3 inputs, exact f16x2 block sums, f32 scaling and "
                             "accumulation, f16 output",
             "data": "synthetic (seeded splitmix64; " + w.recipe + ")",
-            "config": workload_config(w, args.config, world),
+            "config": workload_config(w, name, world),
             "plan": used_plan,
             "launch": f"CUDA graphs of {chunk} calls after a spin-kernel pre-roll",
             "roofline": {
@@ -1082,7 +1104,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    w = workloads.make(args.config)
+    w, name = headline_workload(args)
     total = w.M * w.L
     threads = cref.max_threads()
     per_step_budget = args.reference_seconds / max(1, args.steps + args.warmup)
@@ -1105,7 +1127,7 @@ def run_reference(args):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, args.config, world),
+            "config": workload_config(w, name, world),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": sample, "host_cpus": cpus,
                              "host_cpu_model": model},
@@ -1120,6 +1142,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50000)
     ap.add_argument("--warmup", type=int, default=1000)
     ap.add_argument("--config", default="c2", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--shape", default="",
+                    help="time any M x K x L instead of --config (e.g. 8192x65536x1)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--plan", default="", help="JSON plan fields forced on every call")
     ap.add_argument("--no-e2e", action="store_true")
@@ -1150,6 +1174,11 @@ def main():
         ap.error("--steps must be at least 1")
     if args.gpus < 1:
         ap.error("--gpus must be at least 1")
+    if args.shape:
+        try:
+            parse_shape(args.shape)
+        except ValueError as e:
+            ap.error(str(e))
     world_env = os.environ.get("WORLD_SIZE")
     if world_env is not None and int(world_env) != args.gpus:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world_env}: launch one rank per GPU")

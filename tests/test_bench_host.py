@@ -54,6 +54,23 @@ def test_reference_arm_json_line():
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
 
 
+def test_shape_flag_times_any_workload():
+    """--shape MxKxL replaces the named config: the reference arm's line names it, and a K that is
+    not a multiple of 16 is rejected before anything runs."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--shape", "96x17408x2", "--steps", "3", "--warmup", "3",
+                          "--reference-seconds", "2"], capture_output=True, text=True,
+                         timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    d = json.loads([ln for ln in out.stdout.splitlines() if ln.strip()][-1])
+    cfg = d["config"]
+    assert (cfg["M"], cfg["K"], cfg["L"]) == (96, 17408, 2) and "96x17408x2" in cfg["workload"]
+    assert cfg["bytes_per_call"] == 96 * 17408 * 2 * 9 // 16 + 17408 * 2 * 9 // 16 + 2 * 96 * 2
+    bad = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--shape", "96x100x1"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert bad.returncode != 0 and "multiple of 16" in bad.stderr
+
+
 def test_warmup_below_three_is_rejected():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"],
                          capture_output=True, text=True, timeout=120, cwd=ROOT)
