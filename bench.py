@@ -61,6 +61,7 @@ KERNEL_NAMES = {1: "gemv_simple_kernel", 2: "gemv_stream_kernel", 3: "gemv_tma_k
                 4: "gemv_tma_rv_kernel", 5: "gemv_tc_kernel", 6: "gemv_shift_kernel"}
 DEFAULT_PEAK_GBS = 6800.0   # only if MEASURED_PEAKS.json is absent
 PREROLL_CYCLES = 200_000    # spin kernel ahead of every start event (~0.1 ms at 2 GHz)
+NOMINAL_HBM_GBS = 7900.0    # GB300's nominal HBM3e rate, reported beside the measured-peak fraction
 
 
 # ---------------------------------------------------------------------------- distributed helpers
@@ -928,6 +929,7 @@ def run_ours(args):
             "us_per_call": round(per_call_s * 1e6, 3),
             "us_per_call_spread": spread,
             "pct_of_peak": round(100.0 * achieved / peak, 2),
+            "pct_of_nominal_hbm": round(100.0 * achieved / NOMINAL_HBM_GBS, 2),
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
