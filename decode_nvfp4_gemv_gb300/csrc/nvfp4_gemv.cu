@@ -746,10 +746,13 @@ int plan_tc(const DeviceInfo& d, int64_t M, int64_t K, int64_t groups, const nvf
   const int64_t tiles = ceil_div(M, (int64_t)nvfp4::kTcRows), chunks = K / 256;
   const int64_t total = groups * tiles, slots = 2 * (int64_t)d.sms;
   int64_t S = f.k_split;
-  if (S == 0)  // split K only while the tiles leave at least half of the CTA slots empty
+  if (S == 0) {  // split K only while the tiles leave at least half of the CTA slots empty
     S = 2 * total >= slots ? 1
                            : std::min<int64_t>(std::min<int64_t>(8, chunks),
                                                std::max<int64_t>(1, slots / total));
+    // and in one wave: no more clusters than the GPCs hold at once (two CTAs per SM)
+    while (S > 1 && total > clusters_resident(d, 2, S)) --S;
+  }
   if (S < 1 || S > 8 || S > chunks)
     return fail(NVFP4_ERR_UNSUPPORTED_SHAPE,
                 "tensor-core kernel: K slices must be 1..8 and at most K/256 (S=%lld)",

@@ -315,6 +315,25 @@ def test_tensor_core_ring_keeps_two_ctas_per_sm():
     assert (r["k_split"], r["stages"]) == (5, 4)
 
 
+def test_tensor_core_split_runs_in_one_wave_of_clusters():
+    """The tensor-core kernel splits K over clusters of S CTAs, one cluster per 128-row tile: S is
+    the largest (up to 8, and while the tiles leave half the CTA slots empty) whose clusters the
+    GPU holds at once, so no tile waits for a second wave."""
+    n = 0
+    for M in range(128, 19 * 1024, 128):
+        for L in (1, 2):
+            p = plan(M, 16384, L, forced={"kernel": KERNEL_TC})
+            tiles, S = -(-M // 128) * L, p["k_split"]
+            if S > 1:
+                n += 1
+                assert tiles <= CLUSTERS_RESIDENT[2][S], (M, L, p)
+                if S < 8 and 2 * tiles * (S + 1) <= 2 * 304:
+                    assert tiles > CLUSTERS_RESIDENT[2][S + 1], (M, L, p)   # the largest that fits
+    assert n > 100
+    # 60 tiles: five slices would be 60 clusters of 5 where 58 fit; four it is
+    assert plan(7680, 16384, 1, forced={"kernel": KERNEL_TC})["k_split"] == 4
+
+
 @pytest.mark.parametrize("lim", [dict(sms=0), dict(max_smem_optin=512),
                                  dict(max_smem_sm=1000, max_smem_optin=2000)],
                          ids=["no SMs", "tiny smem", "sm smem below cta smem"])
