@@ -9,6 +9,11 @@ if ROOT not in sys.path:
 
 
 def pytest_configure(config):
+    # temporary files of the tests (tmp_path) stay inside the checkout, in a git-ignored folder
+    # that pytest clears at the start of each session
+    if getattr(config.option, "basetemp", None) is None:
+        os.makedirs(os.path.join(ROOT, "_build"), exist_ok=True)
+        config.option.basetemp = os.path.join(ROOT, "_build", "pytest-tmp")
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: generates full-size workloads on the host")
 
