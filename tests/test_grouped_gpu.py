@@ -128,17 +128,23 @@ def test_tokens_without_an_expert_get_zeros(pkg, g0):
         assert_parity(c, ref, T, f"map with holes {plan}")
 
 
-def test_identity_routing_equals_the_batched_call(pkg):
+@pytest.mark.parametrize("shape", [(300, 1024, 4), (2600, 17408, 2), (96, 37888, 3)],
+                         ids=["300x1024x4", "17-segments-one-idle", "37-segments-split"])
+def test_identity_routing_equals_the_batched_call(pkg, shape):
     """E experts, one token each, equal global scales: the same kernel and plan as the batched
-    entry point with L = E, so the same bits."""
-    M, K, L = 300, 1024, 4
+    entry point with L = E, so the same bits (also with an idle segment, and with K split over a
+    cluster into slices of 13, 13 and 11 segments)."""
+    M, K, L = shape
     w = workloads.random_workload(M, K, L, seed=21, scale_bytes=workloads.pow2_scale_bytes(-3, 3),
                                   g_a=0.5, g_b=2.0)
     gw = workloads.GroupedWorkload("id", M, K, L, L, w.A, w.sfa, np.full(L, 0.5, np.float32),
                                    np.full(L, 2.0, np.float32), w.b, w.sfb,
                                    np.arange(L, dtype=np.int32), 21)
     d = Dev(gw)
-    for plan in (None, dict(kernel=1), dict(kernel=2), tma_plan(), tma_plan(rv=True)):
+    plans = [None, dict(kernel=1), dict(kernel=2), tma_plan()]
+    if K <= 32768:   # past 32 segments the register-vector kernel needs K split over a cluster
+        plans.append(tma_plan(rv=True))
+    for plan in plans:
         cg = run(pkg, d, M, K, L, L, offsets=np.arange(1, L + 1), plan=plan)
         cb = torch.full((L, M), float("nan"), dtype=torch.float16, device="cuda")
         pkg.nvfp4_gemv_batched_ex(d.A, d.sfa, 0.5, d.b, d.sfb, 2.0, cb, M, K, L, plan=plan)
