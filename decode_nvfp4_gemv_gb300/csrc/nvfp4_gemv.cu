@@ -832,6 +832,11 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
         if (S >= 1) {
           nvfp4_plan f2 = f;
           if (!f2.ctas_per_batch) f2.ctas_per_batch = (int32_t)P;
+          // CTAs of one row group (at most 4 rows) and at most 6 segments: one warp per segment
+          // (four for one or two), not 12 of which most would hold no item
+          const int64_t nseg = ceil_div(K, nvfp4::kStep);
+          if (S == 1 && !f2.warps_per_cta && nseg <= 6 && ceil_div(M, f2.ctas_per_batch) <= 4)
+            f2.warps_per_cta = nseg <= 2 ? 4 : (int32_t)nseg;
           char saved[sizeof g_last_error];
           memcpy(saved, g_last_error, sizeof saved);
           st = plan_tma(d, M, K, L, f2, true, pl, false, S);

@@ -303,6 +303,27 @@ def test_tensor_core_plans():
     assert status_of(7168, 512, 1, forced={"kernel": KERNEL_TC, "k_split": 3}) == UNSUPPORTED
 
 
+def test_one_row_group_ctas_take_one_warp_per_segment():
+    """Small calls whose CTAs hold at most 4 rows (one row group) and at most 6 segments: one
+    consumer warp per segment (four for one or two segments) instead of 12 mostly idle ones."""
+    n = 0
+    for K in (256, 512, 1024, 2048, 3072, 4096, 5120, 6144, 7168, 16384):
+        nseg = -(-K // 1024)
+        for M, L in ((64, 1), (128, 1), (128, 2), (256, 1), (300, 1), (600, 2)):
+            p = plan(M, K, L, forced={"flags": 1})
+            rows = -(-M // p["ctas_per_batch"])
+            if p["k_slices"] > 1 or rows > 4:
+                continue
+            n += 1
+            if nseg <= 6:
+                assert p["warps_per_cta"] == (4 if nseg <= 2 else nseg), (M, K, L, p)
+            else:
+                assert p["warps_per_cta"] >= 7, (M, K, L, p)
+    assert n > 30
+    # c1 (128 x 256 x 1): 76 CTAs of 2 rows, four warps
+    assert plan(128, 256, 1)["warps_per_cta"] == 4
+
+
 def test_tensor_core_ring_keeps_two_ctas_per_sm():
     # five stages of 20,480 bytes plus the tokens' scales and the split-K partials: 114,944 bytes,
     # two CTAs in the 228 KB of an SM
