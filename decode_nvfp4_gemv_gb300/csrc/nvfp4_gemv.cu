@@ -840,6 +840,17 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
           char saved[sizeof g_last_error];
           memcpy(saved, g_last_error, sizeof saved);
           st = plan_tma(d, M, K, L, f2, true, pl, false, S);
+          // With early weights a ring of two stages requests one tile before the launch wait; a
+          // small call whose CTAs hold more tiles than that takes a third stage where it fits
+          if (st == NVFP4_OK && (f.flags & NVFP4_FLAG_EARLY_WEIGHTS) && !f.stages &&
+              pl->stages == 2 && ceil_div(ceil_div(M, pl->ctas_per_batch), pl->tile_rows) > 1) {
+            nvfp4_plan f3 = f2;
+            f3.warps_per_cta = pl->warps_per_cta;
+            f3.tile_rows = pl->tile_rows;
+            f3.stages = 3;
+            nvfp4_plan p3;
+            if (plan_tma(d, M, K, L, f3, true, &p3, false, S) == NVFP4_OK) *pl = p3;
+          }
           memcpy(g_last_error, saved, sizeof saved);
           if (st == NVFP4_OK) break;
           memset(pl, 0, sizeof *pl);

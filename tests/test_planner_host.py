@@ -324,6 +324,20 @@ def test_one_row_group_ctas_take_one_warp_per_segment():
     assert plan(128, 256, 1)["warps_per_cta"] == 4
 
 
+def test_small_calls_with_early_weights_request_two_tiles_early():
+    """With early weights a two-stage ring requests one tile before the launch wait; small calls
+    whose CTAs hold more than one tile take a third stage, so two go out early.  Strict-order plans
+    and one-tile CTAs keep theirs."""
+    for shape, strict_stages in (((2048, 7168, 1), 4), ((4096, 2048, 1), 2), ((768, 7168, 3), 4),
+                                 ((2048, 3072, 2), 2)):
+        ew = plan(*shape, forced={"flags": 1})
+        st = plan(*shape, forced={"flags": 0})
+        assert ew["stages"] == 3, (shape, ew)
+        assert st["stages"] == strict_stages, (shape, st)
+        assert -(-(-(-shape[0] // ew["ctas_per_batch"])) // ew["tile_rows"]) > 1
+    assert plan(128, 7168, 1, forced={"flags": 1})["stages"] == 2      # one tile a CTA
+
+
 def test_tensor_core_ring_keeps_two_ctas_per_sm():
     # five stages of 20,480 bytes plus the tokens' scales and the split-K partials: 114,944 bytes,
     # two CTAs in the 228 KB of an SM
