@@ -559,6 +559,7 @@ void small_call_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, int64
 // ring that leaves room for only one CTA per SM was much slower.
 constexpr int64_t kTmaStageTarget = 57344;  // stage bytes (A + sfa rows) the planner aims for
 constexpr int64_t kTmaSmallStage = 24576;   // stages below this get up to 4 ring slots
+constexpr int64_t kTmaLargeStage = 32768;   // from this on: 3 slots if a CTA holds <= 4 stages
 
 // ua: operands not 16-byte aligned (register-vector kernel only; stages carry 32 bytes of slack).
 // S: K slices over a cluster of S CTAs (register-vector kernel, aligned operands, at most
@@ -626,7 +627,17 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots, ua, S).stage_bytes;
       // three CTAs per SM keep two stages (4-stage rings of small tiles measured 5-10% slower);
       // one CTA per SM (where the registers allow no more) takes four, the bytes in flight of two
-      const int64_t want = (stage < kTmaSmallStage && occ_try < 3) || occ_try == 1 ? 4 : 2;
+      int64_t want = (stage < kTmaSmallStage && occ_try < 3) || occ_try == 1 ? 4 : 2;
+      // large stages (>= 32 KB) of at least 8 rows, of a CTA that holds at most four of them: a
+      // third stage where it fits.  Measured on GB300 (K = 8192, 8-row tiles, 8 warps; us per
+      // call, two stages against three, early weights / strict order): 8192 x 8192 9.33 -> 8.28
+      // / 10.15 -> 8.22, 9216 x 8192 10.09 -> 8.88 / 11.08 -> 8.89, 3072 x 8192 x 3 10.10 -> 8.81
+      // / 11.09 -> 8.90, 5120 x 8192 6.77 -> 6.85 / 8.86 -> 6.68.  Stages of 4 rows (K = 16384)
+      // measured 6-10% slower with early weights, and 27.6 KB stages (c4, K = 4096 on 12 rows)
+      // 1-5% slower.
+      if (want == 2 && occ_try == 2 && stage >= kTmaLargeStage && TR >= 8 &&
+          ceil_div(rows_cap, TR) <= 4)
+        want = 3;
       for (int64_t ns = want; ns >= 2; --ns)
         if (tma_layout(rv, K, TR, ns, rows_cap, slots, ua, S).total <= budget) {
           NS = ns;

@@ -338,6 +338,18 @@ def test_small_calls_with_early_weights_request_two_tiles_early():
     assert plan(128, 7168, 1, forced={"flags": 1})["stages"] == 2      # one tile a CTA
 
 
+def test_few_large_tiles_take_a_third_stage():
+    """Stages of at least 32 KB and 8 rows, at most four a CTA, two CTAs per SM: three stages
+    where they fit (K = 8192 on 8-row tiles); 4-row stages (K = 16384) and smaller stages keep
+    two."""
+    for shape in ((8192, 8192, 1), (7168, 8192, 1), (4096, 8192, 2), (3072, 8192, 3)):
+        for flags in (0, 1):
+            p = plan(*shape, forced={"flags": flags})
+            assert (p["tile_rows"], p["stages"]) == (8, 3), (shape, flags, p)
+    for shape in ((4096, 16384, 1), (7168, 16384, 1), (8192, 4096, 1)):
+        assert plan(*shape, forced={"flags": 1})["stages"] == 2, shape
+
+
 def test_tensor_core_ring_keeps_two_ctas_per_sm():
     # five stages of 20,480 bytes plus the tokens' scales and the split-K partials: 114,944 bytes,
     # two CTAs in the 228 KB of an SM
