@@ -615,12 +615,21 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       TR = std::min<int64_t>(256, std::max<int64_t>(1, kTmaStageTarget / row_bytes));
       if (TR >= unit) TR -= TR % unit;
       else if (TR >= 4) TR -= TR % 4;
+      // a warp's item is 4 rows: a tile of fewer re-reads its last row for the rest, so rows of
+      // more than a quarter of the stage target (K past 24 segments) still take 4-row tiles
+      // (shrunk below if two stages do not fit).  Measured on GB300 (13 warps of two segments,
+      // one CTA per SM, 152 CTAs; us per call, 3-row tiles x 4 stages against 4-row tiles x 3 or
+      // 4, early weights / strict order): 3584 x 25600 12.91 -> 11.36 / 12.49 -> 10.83, 8192 x
+      // 25600 24.33 -> 20.03 / 24.69 -> 20.57, 14336 x 26624 42.13 -> 33.18 / 42.68 -> 33.73.
+      else TR = 4;
       TR = std::min<int64_t>(TR, std::max<int64_t>(4, align_up(rows_cap, 4)));
       // at least ~4 tiles per CTA, so the last tile's compute is a small part of the CTA's time
       TR = std::min<int64_t>(TR, std::max<int64_t>(unit, align_up(ceil_div(rows_cap, 4), unit)));
       // shrink by whole rounds until two stages fit this occupancy's budget
       while (TR > unit && tma_layout(rv, K, TR, 2, rows_cap, slots, ua, S).total > budget) TR -= unit;
       while (TR > 4 && tma_layout(rv, K, TR, 2, rows_cap, slots, ua, S).total > budget) TR -= 4;
+      // rows so long that two stages of 4 do not fit (the shared-memory-vector kernel at large K)
+      while (TR > 1 && tma_layout(rv, K, TR, 2, rows_cap, slots, ua, S).total > budget) --TR;
     }
     int64_t NS = f.stages;
     if (NS == 0) {
@@ -852,9 +861,13 @@ int make_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_
           memcpy(saved, g_last_error, sizeof saved);
           st = plan_tma(d, M, K, L, f2, true, pl, false, S);
           // With early weights a ring of two stages requests one tile before the launch wait; a
-          // small call whose CTAs hold more tiles than that takes a third stage where it fits
+          // small call whose CTAs hold more tiles than that takes a third stage where it fits, on
+          // grids of at most 3/4 of the CTA slots (on full grids of 4-row stages a third stage
+          // measured 9-10% slower: 2000 x 16384 5.27 -> 5.73 us; on 152: 1024 x 16384 3.79 ->
+          // 3.28)
           if (st == NVFP4_OK && (f.flags & NVFP4_FLAG_EARLY_WEIGHTS) && !f.stages &&
-              pl->stages == 2 && ceil_div(ceil_div(M, pl->ctas_per_batch), pl->tile_rows) > 1) {
+              pl->stages == 2 && ceil_div(ceil_div(M, pl->ctas_per_batch), pl->tile_rows) > 1 &&
+              (int64_t)pl->ctas_per_batch * L * S <= (int64_t)d.sms * 3 / 2) {
             nvfp4_plan f3 = f2;
             f3.warps_per_cta = pl->warps_per_cta;
             f3.tile_rows = pl->tile_rows;

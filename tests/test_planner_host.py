@@ -336,6 +336,26 @@ def test_small_calls_with_early_weights_request_two_tiles_early():
         assert st["stages"] == strict_stages, (shape, st)
         assert -(-(-(-shape[0] // ew["ctas_per_batch"])) // ew["tile_rows"]) > 1
     assert plan(128, 7168, 1, forced={"flags": 1})["stages"] == 2      # one tile a CTA
+    # full grids (more than 3/4 of the CTA slots) keep two: 2000 x 16384 on 304 CTAs
+    assert plan(2000, 16384, 1, forced={"flags": 1})["stages"] == 2
+    assert plan(1024, 16384, 1, forced={"flags": 1})["stages"] == 3    # on 152
+
+
+def test_tiles_hold_whole_row_groups():
+    """A warp's item is 4 rows: automatic tiles hold a multiple of 4 rows (or the CTA's rows),
+    also where a row is more than a quarter of the stage target (K of 25-26 segments)."""
+    for M, K, L in ((3584, 25600, 1), (8192, 25600, 1), (14336, 26624, 1), (2048, 26624, 1)):
+        p = plan(M, K, L, forced={"flags": 1})
+        assert p["tile_rows"] % 4 == 0 and p["k_slices"] == 1, (M, K, L, p)
+    n = 0
+    for K in range(256, 32768 + 1, 1024):
+        for M in (2432, 4096, 8192, 20000):
+            p = plan(M, K, 1)
+            if p["kernel"] in (KERNEL_TMA, KERNEL_TMA_RV):
+                n += 1
+                rows = -(-M // p["ctas_per_batch"])
+                assert p["tile_rows"] % 4 == 0 or p["tile_rows"] >= rows, (M, K, p)
+    assert n > 100
 
 
 def test_few_large_tiles_take_a_third_stage():
