@@ -608,6 +608,10 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   // Tile rows and ring depth for P CTAs per batch within `budget` bytes of shared memory; false
   // if the partial sums and a two-stage ring do not fit.
   int occ_try = 2;  // the occupancy being tried (set by the loop below)
+  // a call of at least 8 rows per CTA slot and 85 KB per SM: small stages keep two slots (four
+  // measured slower on such calls)
+  const bool large_call =
+      (M * L) / std::max<int64_t>(1, 2 * (int64_t)d.sms) >= 8 && !small_call(d, M, K, L);
   auto shape = [&](int64_t P, int64_t budget, int64_t* TR_out, int64_t* NS_out) -> bool {
     const int64_t rows_cap = ceil_div(M, P);
     int64_t TR = f.tile_rows;
@@ -636,7 +640,8 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       const int64_t stage = tma_layout(rv, K, TR, 1, rows_cap, slots, ua, S).stage_bytes;
       // three CTAs per SM keep two stages (4-stage rings of small tiles measured 5-10% slower);
       // one CTA per SM (where the registers allow no more) takes four, the bytes in flight of two
-      int64_t want = (stage < kTmaSmallStage && occ_try < 3) || occ_try == 1 ? 4 : 2;
+      int64_t want =
+          (stage < kTmaSmallStage && occ_try < 3 && !large_call) || occ_try == 1 ? 4 : 2;
       // large stages (>= 32 KB) of at least 8 rows, of a CTA that holds at most four of them: a
       // third stage where it fits.  Measured on GB300 (K = 8192, 8-row tiles, 8 warps; us per
       // call, two stages against three, early weights / strict order): 8192 x 8192 9.33 -> 8.28

@@ -368,6 +368,12 @@ def test_few_large_tiles_take_a_third_stage():
             assert (p["tile_rows"], p["stages"]) == (8, 3), (shape, flags, p)
     for shape in ((4096, 16384, 1), (7168, 16384, 1), (8192, 4096, 1)):
         assert plan(*shape, forced={"flags": 1})["stages"] == 2, shape
+    # large calls (>= 8 rows per CTA slot, >= 85 KB per SM) keep two stages also when they are
+    # small (below 24 KB: K = 3584 on 12 rows, K = 5120 on 8)
+    for shape in ((5120, 5120, 1), (7168, 3584, 1), (14336, 3584, 1), (3584, 3584, 4)):
+        for flags in (0, 1):
+            p = plan(*shape, forced={"flags": flags})
+            assert p["stages"] == 2 and p["k_slices"] == 1, (shape, flags, p)
 
 
 def test_tensor_core_ring_keeps_two_ctas_per_sm():
