@@ -559,6 +559,7 @@ void small_call_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, int64
 // ring that leaves room for only one CTA per SM was much slower.
 constexpr int64_t kTmaStageTarget = 57344;  // stage bytes (A + sfa rows) the planner aims for
 constexpr int64_t kTmaSmallStage = 24576;   // stages below this get up to 4 ring slots
+constexpr int64_t kTmaSmallStageLarge = 20480;  // the same on large calls
 constexpr int64_t kTmaLargeStage = 32768;   // from this on: 3 slots if a CTA holds <= 4 stages
 
 // ua: operands not 16-byte aligned (register-vector kernel only; stages carry 32 bytes of slack).
@@ -608,8 +609,9 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   // Tile rows and ring depth for P CTAs per batch within `budget` bytes of shared memory; false
   // if the partial sums and a two-stage ring do not fit.
   int occ_try = 2;  // the occupancy being tried (set by the loop below)
-  // a call of at least 8 rows per CTA slot and 85 KB per SM: small stages keep two slots (four
-  // measured slower on such calls)
+  // a call of at least 8 rows per CTA slot and 85 KB per SM: stages of 20-24 KB keep two slots
+  // (four measured slower on such calls: K = 3584 on 12 rows, K = 5120 on 8), smaller ones four
+  // (K = 8192 on 4 rows, 18 KB: two measured 5-7% slower)
   const bool large_call =
       (M * L) / std::max<int64_t>(1, 2 * (int64_t)d.sms) >= 8 && !small_call(d, M, K, L);
   auto shape = [&](int64_t P, int64_t budget, int64_t* TR_out, int64_t* NS_out) -> bool {
@@ -641,7 +643,10 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       // three CTAs per SM keep two stages (4-stage rings of small tiles measured 5-10% slower);
       // one CTA per SM (where the registers allow no more) takes four, the bytes in flight of two
       int64_t want =
-          (stage < kTmaSmallStage && occ_try < 3 && !large_call) || occ_try == 1 ? 4 : 2;
+          (stage < (large_call ? kTmaSmallStageLarge : kTmaSmallStage) && occ_try < 3) ||
+                  occ_try == 1
+              ? 4
+              : 2;
       // large stages (>= 32 KB) of at least 8 rows, of a CTA that holds at most four of them: a
       // third stage where it fits.  Measured on GB300 (K = 8192, 8-row tiles, 8 warps; us per
       // call, two stages against three, early weights / strict order): 8192 x 8192 9.33 -> 8.28
