@@ -558,6 +558,13 @@ void small_call_plan(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, int64
 // (A and sfa rows) per CTA and two CTAs per SM; deeper rings of smaller stages were slower, and a
 // ring that leaves room for only one CTA per SM was much slower.
 constexpr int64_t kTmaStageTarget = 57344;  // stage bytes (A + sfa rows) the planner aims for
+// ... and for an unsplit CTA alone on its SM (by registers) on 19-22 segments with early
+// weights: two stages of about 120 KB in place of four of 56.  Measured on GB300 (10-11 warps of
+// two segments, 152 CTAs; us per call, 4-row tiles x 4 stages against 8-row tiles x 2): 2048 x
+// 18944 7.70 -> 6.98, 3584 x 18944 9.89 -> 9.43, 14336 x 18944 28.71 -> 27.55, 3584 x 20480
+// 10.11 -> 9.58, 3584 x 22528 10.31 -> 9.91; at 24 segments it lost up to 1.4%, and in strict
+// order 2-3% on 2048-3584 rows.
+constexpr int64_t kTmaStageTargetOneCta = 122880;
 constexpr int64_t kTmaSmallStage = 24576;   // stages below this get up to 4 ring slots
 constexpr int64_t kTmaSmallStageLarge = 20480;  // the same on large calls
 constexpr int64_t kTmaLargeStage = 32768;   // from this on: 3 slots if a CTA holds <= 4 stages
@@ -617,8 +624,13 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
   auto shape = [&](int64_t P, int64_t budget, int64_t* TR_out, int64_t* NS_out) -> bool {
     const int64_t rows_cap = ceil_div(M, P);
     int64_t TR = f.tile_rows;
+    // one unsplit CTA per SM (by registers) on 19-22 segments with early weights: two stages of
+    // about twice the bytes in place of four
+    const bool one_cta = rv && S == 1 && occ_try == 1 && nseg <= 22 &&
+                         (f.flags & NVFP4_FLAG_EARLY_WEIGHTS);
     if (TR == 0) {
-      TR = std::min<int64_t>(256, std::max<int64_t>(1, kTmaStageTarget / row_bytes));
+      TR = std::min<int64_t>(
+          256, std::max<int64_t>(1, (one_cta ? kTmaStageTargetOneCta : kTmaStageTarget) / row_bytes));
       if (TR >= unit) TR -= TR % unit;
       else if (TR >= 4) TR -= TR % 4;
       // a warp's item is 4 rows: a tile of fewer re-reads its last row for the rest, so rows of
@@ -644,7 +656,7 @@ int plan_tma(const DeviceInfo& d, int64_t M, int64_t K, int64_t L, const nvfp4_p
       // one CTA per SM (where the registers allow no more) takes four, the bytes in flight of two
       int64_t want =
           (stage < (large_call ? kTmaSmallStageLarge : kTmaSmallStage) && occ_try < 3) ||
-                  occ_try == 1
+                  (occ_try == 1 && !one_cta)
               ? 4
               : 2;
       // large stages (>= 32 KB) of at least 8 rows, of a CTA that holds at most four of them: a

@@ -107,12 +107,16 @@ def test_plans_follow_the_sm_count():
 def test_register_capped_rings_take_one_wave():
     """K of 20-24 segments unsplit: 10-12 consumer warps of two segments each hold ~90 registers a
     thread, so the register file takes one CTA per SM; the grid is one wave of 152 CTAs, with a
-    four-stage ring to keep the SM's loads in flight."""
+    four-stage ring to keep the SM's loads in flight (in strict order; with early weights two
+    stages of twice the rows up to 22 segments)."""
     for M, K, L in ((8192, 20480, 1), (8192, 24576, 1), (4096, 24576, 4)):
-        p = plan(M, K, L, forced={"flags": 1})
+        p = plan(M, K, L, forced={"flags": 0})
         assert p["kernel"] == KERNEL_TMA_RV and p["k_slices"] == 1, (M, K, L, p)
         assert p["ctas_per_batch"] * L == 152 and p["stages"] == 4, (M, K, L, p)
         assert p["k_split"] == 2 and p["warps_per_cta"] == K // 2048, (M, K, L, p)
+        q = plan(M, K, L, forced={"flags": 1})
+        assert q["ctas_per_batch"] * L == 152 and q["warps_per_cta"] == p["warps_per_cta"]
+        assert (q["tile_rows"], q["stages"]) == ((8, 2) if K // 1024 <= 22 else (4, 4)), q
 
 
 def test_odd_segment_counts_take_warps_of_two_with_one_idle():
@@ -128,6 +132,18 @@ def test_odd_segment_counts_take_warps_of_two_with_one_idle():
     # a forced warp count must still divide the segments (or be a multiple of them)
     assert status_of(8192, 17 * 1024, 1, forced={"kernel": KERNEL_TMA_RV, "warps_per_cta": 9}) \
         == UNSUPPORTED
+
+
+def test_one_cta_rings_with_early_weights_take_two_large_stages():
+    """One unsplit CTA per SM on 19-22 segments with early weights: two stages of about twice the
+    bytes (8-row tiles where the CTA's rows allow) in place of four; strict order keeps four."""
+    for M, K, L in ((3584, 18944, 1), (14336, 22528, 1), (1792, 18944, 8)):
+        ew = plan(M, K, L, forced={"flags": 1})
+        st = plan(M, K, L, forced={"flags": 0})
+        assert ew["ctas_per_batch"] * L == 152 and (ew["tile_rows"], ew["stages"]) == (8, 2), ew
+        assert (st["tile_rows"], st["stages"]) == (4, 4), st
+    # 24 segments keep four stages also with early weights
+    assert plan(8192, 24576, 1, forced={"flags": 1})["stages"] == 4
 
 
 def test_wide_k_splits_over_a_cluster_of_two():
